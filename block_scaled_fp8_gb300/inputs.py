@@ -1,0 +1,217 @@
+"""Seeded synthetic inputs for the block-scaled FP8 GEMM.
+
+Shared by the tests, the smoke check and the benchmark, for both the CUDA
+library and the CPU oracle.  It holds none of the GEMM's arithmetic: it only
+plays the upstream quantiser that the pages leave to the caller ("DeepGEMM
+does not cast; it consumes already-quantised FP8 tensors and their scales",
+PaperTrace DeepGEMM §1.1), on CPU with a seeded ``torch.Generator``.
+
+Quantisation recipe (one reading, stated in the design notes):
+  * activations: one FP32 scale per 1x128 K-group of each row; weights: one
+    per 128x128 block (PaperTrace DeepGEMM §1.1);
+  * scale s = 2^ceil(log2(amax/448)), i.e. absmax/448 rounded up to a power of
+    two, so it is exact in UE8M0; s = 1 for an all-zero group;
+  * codes q = float8_e4m3fn(x / s) with torch's CPU cast (round to nearest
+    even); |x/s| <= 448 so nothing saturates.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+E4M3_MAX = 448.0
+GRAN = 128
+
+
+def cdiv(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def pow2_scale(amax: torch.Tensor) -> torch.Tensor:
+    """Smallest power of two s (FP32, normal) with amax / s <= 448; 1 where amax == 0."""
+    v = amax.double() / E4M3_MAX
+    mant, exp = torch.frexp(v)                      # v = mant * 2^exp, mant in [0.5, 1)
+    e = torch.where(mant == 0.5, exp - 1, exp)      # ceil(log2 v)
+    e = torch.clamp(e, min=-126, max=127)
+    s = torch.ldexp(torch.ones_like(v), e)
+    s = torch.where(amax.double() > E4M3_MAX * s, s * 2, s)   # guard, never expected
+    s = torch.where(amax == 0, torch.ones_like(s), s)
+    return s.float()
+
+
+def quantize_1x128(x: torch.Tensor):
+    """x fp32 [R, K] -> (codes float8_e4m3fn [R, K], scales fp32 [R, ceil(K/128)])."""
+    R, K = x.shape
+    sf_k = cdiv(K, GRAN)
+    xp = torch.nn.functional.pad(x, (0, sf_k * GRAN - K)).view(R, sf_k, GRAN)
+    s = pow2_scale(xp.abs().amax(-1))
+    q = (xp / s[..., None]).view(R, sf_k * GRAN)[:, :K].contiguous()
+    return q.to(torch.float8_e4m3fn), s
+
+
+def quantize_128x128(w: torch.Tensor):
+    """w fp32 [N, K] -> (codes float8_e4m3fn [N, K], scales fp32 [ceil(N/128), ceil(K/128)])."""
+    N, K = w.shape
+    nb, kb = cdiv(N, GRAN), cdiv(K, GRAN)
+    wp = torch.nn.functional.pad(w, (0, kb * GRAN - K, 0, nb * GRAN - N))
+    blocks = wp.view(nb, GRAN, kb, GRAN)
+    s = pow2_scale(blocks.abs().amax(dim=(1, 3)))
+    q = (blocks / s[:, None, :, None]).reshape(nb * GRAN, kb * GRAN)[:N, :K].contiguous()
+    return q.to(torch.float8_e4m3fn), s
+
+
+def random_finite_e4m3(shape, g: torch.Generator) -> torch.Tensor:
+    """Uniformly random E4M3fn codes, NaN codes (0x7f, 0xff) excluded."""
+    codes = torch.randint(0, 254, shape, generator=g, dtype=torch.int32)
+    codes = codes + (codes >= 0x7f).int()          # skip 0x7f; 0xff is never reached
+    return codes.to(torch.uint8).view(torch.float8_e4m3fn)
+
+
+@dataclass
+class DenseCase:
+    """D = C + A @ B^T inputs (NT layout, PaperTrace DeepGEMM §1.1)."""
+    a: torch.Tensor          # float8_e4m3fn [M, K]
+    sfa: torch.Tensor        # fp32 [M, ceil(K/128)]
+    b: torch.Tensor          # float8_e4m3fn [N, K]
+    sfb: torch.Tensor        # fp32 [ceil(N/128), ceil(K/128)]
+    c: torch.Tensor | None   # bf16 [M, N] or None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def shape(self):
+        return self.a.shape[0], self.b.shape[0], self.a.shape[1]
+
+
+def dense_case(M: int, N: int, K: int, seed: int = 0, with_c: bool = False,
+               b_scale_exp_range: tuple[int, int] | None = None) -> DenseCase:
+    """Dense NT problem: A, B from N(0,1) quantised per 1x128 / 128x128.
+
+    b_scale_exp_range=(lo, hi) replaces every B block scale by 2^u with u a
+    uniform integer in [lo, hi] (the C-accumulate workload's spread of weight
+    scale exponents over 2^-8..2^4)."""
+    g = generator(seed)
+    x = torch.randn(M, K, generator=g, dtype=torch.float32)
+    w = torch.randn(N, K, generator=g, dtype=torch.float32)
+    a, sfa = quantize_1x128(x)
+    del x
+    b, sfb = quantize_128x128(w)
+    del w
+    if b_scale_exp_range is not None:
+        lo, hi = b_scale_exp_range
+        u = torch.randint(lo, hi + 1, sfb.shape, generator=g, dtype=torch.int64)
+        sfb = torch.ldexp(torch.ones(sfb.shape, dtype=torch.float64), u).float()
+    c = torch.randn(M, N, generator=g, dtype=torch.float32).to(torch.bfloat16) if with_c else None
+    return DenseCase(a, sfa, b, sfb, c, {"M": M, "N": N, "K": K, "seed": seed})
+
+
+def integer_exact_case(M: int, N: int, K: int, seed: int = 0, max_shift: int = 2) -> DenseCase:
+    """Codes for integers in [-8, 8] and scales 2^j (j in [-max_shift, 0] for A,
+    [0, max_shift] for B): every partial sum is an integer multiple of
+    2^-max_shift well inside 2^24, so FP32 accumulation is exact and the bf16
+    result is exactly bf16_rne(integer matmul)."""
+    g = generator(seed)
+    ai = torch.randint(-8, 9, (M, K), generator=g).float()
+    bi = torch.randint(-8, 9, (N, K), generator=g).float()
+    sf_k = cdiv(K, GRAN)
+    ja = torch.randint(-max_shift, 1, (M, sf_k), generator=g)
+    jb = torch.randint(0, max_shift + 1, (cdiv(N, GRAN), sf_k), generator=g)
+    sfa = torch.ldexp(torch.ones(M, sf_k, dtype=torch.float64), ja).float()
+    sfb = torch.ldexp(torch.ones(cdiv(N, GRAN), sf_k, dtype=torch.float64), jb).float()
+    a = ai.to(torch.float8_e4m3fn)
+    b = bi.to(torch.float8_e4m3fn)
+    return DenseCase(a, sfa, b, sfb, None, {"M": M, "N": N, "K": K, "seed": seed})
+
+
+@dataclass
+class ContiguousCase:
+    """M-grouped contiguous MoE inputs (PaperTrace DeepGEMM §5.1)."""
+    a: torch.Tensor              # float8 [M_total, K]
+    sfa: torch.Tensor            # fp32 [M_total, sf_k]
+    b: torch.Tensor              # float8 [E, N, K]
+    sfb: torch.Tensor            # fp32 [E, ceil(N/128), sf_k]
+    grouped_layout: torch.Tensor  # int32 [M_total], expert id or -1 (padding row)
+    m_per_expert: list[int]
+    meta: dict = field(default_factory=dict)
+
+
+def contiguous_case(num_groups: int, N: int, K: int, seed: int = 0, m_lo: int = 128,
+                    m_hi: int = 4096, align: int = 128,
+                    m_per_expert: list[int] | None = None) -> ContiguousCase:
+    g = generator(seed)
+    if m_per_expert is None:
+        m_per_expert = [int(v) for v in torch.randint(m_lo, m_hi + 1, (num_groups,), generator=g)]
+    padded = [cdiv(m, align) * align for m in m_per_expert]
+    M_total = sum(padded)
+    sf_k = cdiv(K, GRAN)
+    a = torch.zeros(M_total, K, dtype=torch.float8_e4m3fn)
+    sfa = torch.ones(M_total, sf_k, dtype=torch.float32)
+    layout = torch.full((M_total,), -1, dtype=torch.int32)
+    row = 0
+    for e, (m, mp) in enumerate(zip(m_per_expert, padded)):
+        if m:
+            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32))
+            a[row:row + m] = q
+            sfa[row:row + m] = s
+            layout[row:row + m] = e
+        row += mp
+    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn)
+    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32)
+    for e in range(num_groups):
+        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32))
+    return ContiguousCase(a, sfa, b, sfb, layout, m_per_expert,
+                          {"E": num_groups, "N": N, "K": K, "M_total": M_total, "seed": seed})
+
+
+@dataclass
+class MaskedCase:
+    """M-grouped masked MoE inputs (PaperTrace DeepGEMM §5.2)."""
+    a: torch.Tensor          # float8 [E, max_m, K]
+    sfa: torch.Tensor        # fp32 [E, max_m, sf_k]
+    b: torch.Tensor          # float8 [E, N, K]
+    sfb: torch.Tensor        # fp32 [E, ceil(N/128), sf_k]
+    masked_m: torch.Tensor   # int32 [E]
+    expected_m: int
+    meta: dict = field(default_factory=dict)
+
+
+def masked_case(num_groups: int, max_m: int, N: int, K: int, seed: int = 0,
+                masked_m: list[int] | None = None) -> MaskedCase:
+    """Valid rows per expert uniform in [0, max_m]; rows past masked_m[e] hold
+    random finite codes and random scales (they must not affect anything)."""
+    g = generator(seed)
+    if masked_m is None:
+        mm = torch.randint(0, max_m + 1, (num_groups,), generator=g, dtype=torch.int32)
+    else:
+        mm = torch.tensor(masked_m, dtype=torch.int32)
+    sf_k = cdiv(K, GRAN)
+    a = random_finite_e4m3((num_groups, max_m, K), g)
+    sfa = torch.ldexp(torch.ones(num_groups, max_m, sf_k, dtype=torch.float64),
+                      torch.randint(-10, 4, (num_groups, max_m, sf_k), generator=g)).float()
+    for e in range(num_groups):
+        m = int(mm[e])
+        if m:
+            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32))
+            a[e, :m] = q
+            sfa[e, :m] = s
+    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn)
+    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32)
+    for e in range(num_groups):
+        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32))
+    expected_m = max(1, math.ceil(float(mm.float().mean())))
+    return MaskedCase(a, sfa, b, sfb, mm, expected_m,
+                      {"E": num_groups, "max_m": max_m, "N": N, "K": K, "seed": seed})
+
+
+# Workload shapes of the pages' models ("DeepSeek V4 源码剖析 第13章" §13.16:
+# the test tables carry DeepSeek's real shapes such as (24576, 1536) and
+# (7168, 16384)).
+V3_NK = [(2112, 7168), (24576, 1536), (7168, 16384)]
+V3_M = [128, 4096]

@@ -1,0 +1,269 @@
+"""Oracle: plain fp64 CPU restatement of the block-scaled FP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the CUDA library (``block_scaled_fp8_gb300``) and never imports it;
+the library never imports this.
+
+The arithmetic lives in ``oracle.c`` (built here with gcc into
+``oracle/_build/liboracle.so``); this module only marshals numpy arrays.
+Every function cites the page passage it restates; see ``oracle.c`` for the
+readings taken where the pages are silent.
+
+Pins (tests that tie the oracle to something other than itself) are in
+``tests/test_oracle_pins.py``.  Parity status: every function here is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (OpenMP, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64 = ctypes.c_int, ctypes.c_int64
+            lib.orc_e4m3_decode.restype = ctypes.c_double
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_ue8m0_decode.restype = ctypes.c_double
+            lib.orc_ue8m0_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_fp32_to_ue8m0.restype = ctypes.c_uint8
+            lib.orc_fp32_to_ue8m0.argtypes = [ctypes.c_float]
+            lib.orc_fp32_is_exact_ue8m0.restype = ctypes.c_int
+            lib.orc_fp32_is_exact_ue8m0.argtypes = [ctypes.c_float]
+            lib.orc_bf16_from_double.restype = ctypes.c_uint16
+            lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
+            lib.orc_bf16_decode.restype = ctypes.c_double
+            lib.orc_bf16_decode.argtypes = [ctypes.c_uint16]
+            lib.orc_transform_sf.restype = i64
+            lib.orc_transform_sf.argtypes = [P, i32, i32, i32, i32, i32, i32, P]
+            lib.orc_unpack_sf.restype = None
+            lib.orc_unpack_sf.argtypes = [P, i32, i32, i32, P]
+            lib.orc_expand_block_rows.restype = None
+            lib.orc_expand_block_rows.argtypes = [P, i32, i32, P]
+            lib.orc_gemm_nt.restype = None
+            lib.orc_gemm_nt.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, P, i32]
+            lib.orc_gemm_nt_sampled.restype = None
+            lib.orc_gemm_nt_sampled.argtypes = [i32, P, i64, P, P, i64, P, P, i64, i64, P, P, P, P,
+                                                i32]
+            lib.orc_m_grouped_contiguous.restype = None
+            lib.orc_m_grouped_contiguous.argtypes = [i32, i32, i32, i32, P, i64, P, P, i64, P, P, P,
+                                                     i64, i32]
+            lib.orc_m_grouped_masked.restype = None
+            lib.orc_m_grouped_masked.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, i32]
+            lib.orc_max_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        a = a.view(np.uint8) if a.itemsize == 1 else a.astype(np.uint8)
+    return a
+
+
+def max_threads() -> int:
+    return int(_get().orc_max_threads())
+
+
+# --- number formats --------------------------------------------------------
+
+def e4m3_decode(code: int) -> float:
+    """OCP FP8 E4M3fn code -> value ("FP8 e4m3" of the pages; torch.float8_e4m3fn)."""
+    return float(_get().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_table() -> np.ndarray:
+    """All 256 decoded E4M3fn values, indexed by code."""
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def ue8m0_decode(e: int) -> float:
+    """UE8M0 byte -> 2^(e-127); 0xff is NaN (PaperTrace DeepGEMM §3.1)."""
+    return float(_get().orc_ue8m0_decode(int(e) & 0xFF))
+
+
+def fp32_to_ue8m0(s: float) -> int:
+    """Byte kept when an FP32 scale is packed: its exponent bits (>>23), per
+    "DeepSeek V4 源码剖析 第13章" §13.3; 0.75 -> 0.5, 3 -> 2."""
+    return int(_get().orc_fp32_to_ue8m0(float(s)))
+
+
+def fp32_is_exact_ue8m0(s: float) -> bool:
+    """(bits & 0x807fffff) == 0: a positive normal power of two (§3.1)."""
+    return bool(_get().orc_fp32_is_exact_ue8m0(float(s)))
+
+
+def bf16_from_double(x: float) -> int:
+    """Single round-to-nearest-even of an fp64 value to bf16 bits."""
+    return int(_get().orc_bf16_from_double(float(x)))
+
+
+def bf16_decode(h: int) -> float:
+    return float(_get().orc_bf16_decode(int(h) & 0xFFFF))
+
+
+# --- scale layout ------------------------------------------------------------
+
+def align4(x: int) -> int:
+    return (x + 3) // 4 * 4
+
+
+def transform_sf(sf: np.ndarray, gran_mn: int, mn: int, packed: bool = True):
+    """FP32 scales [batch?, mn_rows, sf_k] -> MN-major TMA-aligned layout.
+
+    PaperTrace DeepGEMM §3.1-3.2: packed UE8M0 (4 K-groups per int32,
+    little-endian by K), shape [mn, psf_k] with strides [1, align(mn,4)],
+    batch stride psf_k*align(mn,4); rows broadcast from gran_mn to 1.
+    Returns (out, n_inexact) with out int32 [batch, psf_k, align4(mn)] (packed)
+    or float32 [batch, sf_k, align4(mn)].
+    """
+    sf = np.ascontiguousarray(sf, dtype=np.float32)
+    squeeze = sf.ndim == 2
+    if squeeze:
+        sf = sf[None]
+    batch, mn_rows, sf_k = sf.shape
+    if packed:
+        out = np.empty((batch, (sf_k + 3) // 4, align4(mn)), dtype=np.int32)
+    else:
+        out = np.empty((batch, sf_k, align4(mn)), dtype=np.float32)
+    n = _get().orc_transform_sf(_ptr(sf), batch, mn_rows, sf_k, gran_mn, mn, 1 if packed else 0,
+                                _ptr(out))
+    return (out[0] if squeeze else out), int(n)
+
+
+def unpack_sf(packed: np.ndarray, mn: int, sf_k: int) -> np.ndarray:
+    """Packed MN-major UE8M0 int32 -> fp64 scales [batch?, mn, sf_k]."""
+    p = np.ascontiguousarray(packed)
+    squeeze = p.ndim == 2
+    if squeeze:
+        p = p[None]
+    batch = p.shape[0]
+    assert p.shape[1:] == ((sf_k + 3) // 4, align4(mn)), p.shape
+    out = np.empty((batch, mn, sf_k), dtype=np.float64)
+    _get().orc_unpack_sf(_ptr(p.view(np.uint32)), batch, mn, sf_k, _ptr(out))
+    return out[0] if squeeze else out
+
+
+def expand_block_rows(sb: np.ndarray, n_rows: int) -> np.ndarray:
+    """128x128 block scales [ceil(N/128), sf_k] -> one row per N index."""
+    sb = np.ascontiguousarray(sb, dtype=np.float64)
+    out = np.empty((n_rows, sb.shape[1]), dtype=np.float64)
+    _get().orc_expand_block_rows(_ptr(sb), n_rows, sb.shape[1], _ptr(out))
+    return out
+
+
+# --- GEMM --------------------------------------------------------------------
+
+def gemm_nt(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
+            c: np.ndarray | None = None, want_pre: bool = False, nthreads: int = 0):
+    """D = C + A @ B^T with per-element expanded scales, fp64 sum, one RNE to bf16.
+
+    a: uint8 E4M3 codes [M, K]; sa: fp64 [M, sf_k]; b: uint8 [N, K];
+    sb_rows: fp64 [N, sf_k] (one row per N index); c: uint16 bf16 bits [M, N].
+    Returns uint16 bf16 bits [M, N] (and the fp64 pre-rounding values).
+    "DeepSeek V4 源码剖析 第13章" §13.3 pseudocode; LinearQuant page.
+    """
+    a, b = _u8(a), _u8(b)
+    M, K = a.shape
+    N = b.shape[0]
+    sf_k = (K + 127) // 128
+    sa = np.ascontiguousarray(sa, dtype=np.float64)
+    sb_rows = np.ascontiguousarray(sb_rows, dtype=np.float64)
+    assert sa.shape == (M, sf_k) and sb_rows.shape == (N, sf_k) and b.shape[1] == K
+    if c is not None:
+        c = np.ascontiguousarray(c).view(np.uint16)
+        assert c.shape == (M, N)
+    d = np.empty((M, N), dtype=np.uint16)
+    pre = np.empty((M, N), dtype=np.float64) if want_pre else None
+    _get().orc_gemm_nt(M, N, K, _ptr(a), K, _ptr(sa), _ptr(b), K, _ptr(sb_rows), _ptr(c), N,
+                       _ptr(d), N, _ptr(pre), nthreads)
+    return (d, pre) if want_pre else d
+
+
+def gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, c=None, want_pre=False, nthreads: int = 0):
+    """The elements (rows[i], cols[i]) of gemm_nt, computed one by one."""
+    a, b = _u8(a), _u8(b)
+    M, K = a.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    sa = np.ascontiguousarray(sa, dtype=np.float64)
+    sb_rows = np.ascontiguousarray(sb_rows, dtype=np.float64)
+    ldc = 0
+    if c is not None:
+        c = np.ascontiguousarray(c).view(np.uint16)
+        ldc = c.shape[1]
+    out = np.empty(rows.shape[0], dtype=np.uint16)
+    pre = np.empty(rows.shape[0], dtype=np.float64) if want_pre else None
+    _get().orc_gemm_nt_sampled(K, _ptr(a), K, _ptr(sa), _ptr(b), K, _ptr(sb_rows), _ptr(c), ldc,
+                               rows.shape[0], _ptr(rows), _ptr(cols), _ptr(out), _ptr(pre),
+                               nthreads)
+    return (out, pre) if want_pre else out
+
+
+def m_grouped_contiguous(a, sa, b, sb_rows, grouped_layout, d_init=None, nthreads: int = 0):
+    """Contiguous M-grouped GEMM (PaperTrace DeepGEMM §5.1): row m uses expert
+    grouped_layout[m]; rows marked -1 are left as in d_init (default 0)."""
+    a, b = _u8(a), _u8(b)
+    M, K = a.shape
+    E, N, _ = b.shape
+    layout = np.ascontiguousarray(grouped_layout, dtype=np.int32)
+    d = (np.zeros((M, N), dtype=np.uint16) if d_init is None
+         else np.ascontiguousarray(d_init).view(np.uint16).copy())
+    _get().orc_m_grouped_contiguous(M, N, K, E, _ptr(a), K,
+                                    _ptr(np.ascontiguousarray(sa, dtype=np.float64)), _ptr(b), K,
+                                    _ptr(np.ascontiguousarray(sb_rows, dtype=np.float64)),
+                                    _ptr(layout), _ptr(d), N, nthreads)
+    return d
+
+
+def m_grouped_masked(a, sa, b, sb_rows, masked_m, d_init=None, nthreads: int = 0):
+    """Masked M-grouped GEMM (PaperTrace DeepGEMM §5.2): a [E, max_m, K]; only
+    rows m < masked_m[e] are computed; other rows keep d_init (default 0)."""
+    a, b = _u8(a), _u8(b)
+    E, max_m, K = a.shape
+    N = b.shape[1]
+    mm = np.ascontiguousarray(masked_m, dtype=np.int32)
+    d = (np.zeros((E, max_m, N), dtype=np.uint16) if d_init is None
+         else np.ascontiguousarray(d_init).view(np.uint16).copy())
+    _get().orc_m_grouped_masked(E, max_m, N, K, _ptr(a),
+                                _ptr(np.ascontiguousarray(sa, dtype=np.float64)), _ptr(b),
+                                _ptr(np.ascontiguousarray(sb_rows, dtype=np.float64)), _ptr(mm),
+                                _ptr(d), nthreads)
+    return d

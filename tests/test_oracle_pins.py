@@ -1,0 +1,464 @@
+"""Pins: the oracle checked against things other than itself.
+
+Each test ties an oracle function to a library routine, a worked example on
+the pages, a closed form, an invariant or brute force in exact rationals, so
+that a dropped term, a wrong sign or index, or a transposed operand in the
+oracle fails at least one of them.  CPU only.
+"""
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- E4M3 decode
+
+def test_e4m3_all_codes_match_torch(orc):
+    """All 256 codes against torch's float8_e4m3fn -> float64 conversion."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = orc.e4m3_table()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+
+
+def test_e4m3_textbook_values(orc):
+    """OCP E4M3 fn: max 448, min normal 2^-6, min subnormal 2^-9, no inf."""
+    assert orc.e4m3_decode(0x7E) == 448.0
+    assert orc.e4m3_decode(0xFE) == -448.0
+    assert orc.e4m3_decode(0x08) == 2.0 ** -6
+    assert orc.e4m3_decode(0x01) == 2.0 ** -9
+    assert orc.e4m3_decode(0x38) == 1.0
+    assert orc.e4m3_decode(0xB8) == -1.0
+    assert orc.e4m3_decode(0x80) == 0.0 and math.copysign(1, orc.e4m3_decode(0x80)) == -1
+    assert not any(math.isinf(orc.e4m3_decode(c)) for c in range(256))
+
+
+# ---------------------------------------------------------------- UE8M0
+
+def test_ue8m0_truncation_worked_example(orc):
+    """The page's own example: packing keeps the exponent, 0.75 -> 0.5, 3 -> 2."""
+    rows = _golden("ue8m0_truncation.txt")
+    assert len(rows) == 2
+    for s, v in rows:
+        assert orc.ue8m0_decode(orc.fp32_to_ue8m0(float(s))) == float(v)
+        assert not orc.fp32_is_exact_ue8m0(float(s))
+
+
+def test_ue8m0_power_of_two_round_trip(orc):
+    """Every normal FP32 power of two survives packing exactly and is flagged exact."""
+    for e in range(-126, 128):
+        s = math.ldexp(1.0, e)
+        byte = orc.fp32_to_ue8m0(s)
+        assert byte == e + 127
+        assert orc.ue8m0_decode(byte) == s
+        assert orc.fp32_is_exact_ue8m0(s)
+    assert math.isnan(orc.ue8m0_decode(0xFF))
+    assert orc.ue8m0_decode(0) == math.ldexp(1.0, -127)
+    # sign and mantissa are what make a scale inexact
+    for s in (-2.0, 1.5, 3.0, 0.3, float(np.float32(2.0 ** -127))):
+        assert not orc.fp32_is_exact_ue8m0(s)
+
+
+def test_scale_size_ratios_closed_form():
+    """"DeepSeek V4 源码剖析 第13章" §13.3: a 128x128-block FP8 weight's (1-byte)
+    scales are 1/16384 of its bytes; 1x128 activation scales 1/128."""
+    M = N = K = 1024
+    weight_bytes, act_bytes = N * K, M * K
+    assert Fraction((N // 128) * (K // 128), weight_bytes) == Fraction(1, 16384)
+    assert Fraction(M * (K // 128), act_bytes) == Fraction(1, 128)
+
+
+# ---------------------------------------------------------------- transform
+
+def test_transform_hand_worked_layout(orc):
+    """Hand-worked fixture of the packed MN-major layout (PaperTrace §3.1)."""
+    sf = np.array([[2.0 ** (i - k) for k in range(6)] for i in range(5)], dtype=np.float32)
+    out, inexact = orc.transform_sf(sf, gran_mn=1, mn=5, packed=True)
+    assert inexact == 0
+    assert out.shape == (2, 8)
+    expected = {int(i): int(h, 16) for i, h in _golden("sf_layout_small.txt")}
+    flat = out.reshape(-1).view(np.uint32)
+    assert {i: int(flat[i]) for i in range(16)} == expected
+
+
+@pytest.mark.parametrize("mn,stride", [(2112, 2112), (30, 32), (4096, 4096), (5, 8), (1, 4)])
+def test_transform_strides(orc, mn, stride):
+    """Stride of a K-slice is align(mn, 4) int32 (16 B / sizeof(int32), §3.1)."""
+    sf = np.ones((mn, 9), dtype=np.float32)
+    out, _ = orc.transform_sf(sf, gran_mn=1, mn=mn)
+    assert out.shape == (3, stride)
+    assert np.all(out[:, mn:] == 0)
+
+
+def test_transform_broadcast_and_fp32_mode(orc):
+    """gran_mn=128 weights broadcast to one row per N index; the FP32 MN-major
+    mode is the transpose (strides [1, align4(mn)])."""
+    rng = np.random.default_rng(0)
+    N, sf_k = 300, 5
+    sfb = np.ldexp(1.0, rng.integers(-8, 5, (3, sf_k))).astype(np.float32)
+    packed, _ = orc.transform_sf(sfb, gran_mn=128, mn=N)
+    back = orc.unpack_sf(packed, N, sf_k)
+    assert np.array_equal(back, sfb[np.arange(N) // 128].astype(np.float64))
+    f32, _ = orc.transform_sf(sfb, gran_mn=128, mn=N, packed=False)
+    assert f32.shape == (sf_k, 300)
+    assert np.array_equal(f32[:, :N].T, sfb[np.arange(N) // 128])
+
+
+def test_transform_counts_inexact(orc):
+    sf = np.array([[0.75, 1.0, 3.0, 2.0 ** -3]], dtype=np.float32)
+    out, inexact = orc.transform_sf(sf, gran_mn=1, mn=1)
+    assert inexact == 2
+    vals = orc.unpack_sf(out, 1, 4)[0]
+    assert list(vals) == [0.5, 1.0, 2.0, 0.125]
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def _bf16_value(h):
+    return struct.unpack("<f", struct.pack("<I", (h & 0xFFFF) << 16))[0]
+
+
+def _bf16_nearest_bruteforce(x: Fraction) -> int:
+    """Nearest bf16 to an exact rational by searching the neighbourhood of its
+    float32 approximation; ties go to the even bit pattern."""
+    f = float(x)
+    if f == 0.0 and x == 0:
+        return 0
+    approx = struct.unpack("<I", struct.pack("<f", np.float32(f)))[0] >> 16
+    best = None
+    for h in range(approx - 3, approx + 4):
+        h &= 0xFFFF
+        v = _bf16_value(h)
+        if math.isnan(v) or math.isinf(v):
+            continue
+        d = abs(Fraction(v) - x)
+        key = (d, h & 1)
+        if best is None or key < best[0]:
+            best = (key, h)
+    return best[1]
+
+
+def test_bf16_rne_bruteforce(orc):
+    rng = np.random.default_rng(1)
+    vals = []
+    for e in list(range(-140, -120)) + list(range(-10, 12)) + [100, 126, 127]:
+        for _ in range(40):
+            vals.append(math.ldexp(rng.uniform(1, 2), e) * rng.choice([-1, 1]))
+    for x in vals:
+        got = orc.bf16_from_double(x)
+        want = _bf16_nearest_bruteforce(Fraction(x))
+        if x < 0 and want == 0:
+            want = 0x8000
+        assert got == want, (x, hex(got), hex(want))
+
+
+def test_bf16_rne_ties_and_overflow(orc):
+    """Exact midpoints between neighbouring bf16 values go to the even one."""
+    rng = np.random.default_rng(2)
+    for h in rng.integers(0x0001, 0x7F7F, 400):
+        lo, hi = _bf16_value(int(h)), _bf16_value(int(h) + 1)
+        mid = (lo + hi) / 2  # exact in fp64
+        want = int(h) if int(h) % 2 == 0 else int(h) + 1
+        assert orc.bf16_from_double(mid) == want
+        assert orc.bf16_from_double(-mid) == want | 0x8000
+    big = _bf16_value(0x7F7F)
+    assert orc.bf16_from_double(big) == 0x7F7F
+    assert orc.bf16_from_double(big + math.ldexp(1, 127 - 8)) == 0x7F80   # tie -> even -> inf
+    assert orc.bf16_from_double(big + math.ldexp(1, 127 - 9)) == 0x7F7F
+    assert orc.bf16_from_double(float("inf")) == 0x7F80
+    assert orc.bf16_from_double(math.ldexp(1, -134)) == 0x0000            # tie at half min subnormal
+    assert orc.bf16_from_double(math.ldexp(1.5, -134)) == 0x0001
+
+
+def test_bf16_rne_matches_torch_on_float32_values(orc):
+    """For values already in float32, torch's f32 -> bf16 cast is one RNE step."""
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(4096, generator=g) * torch.exp2(torch.randint(-30, 30, (4096,), generator=g).float())
+    ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.bf16_from_double(float(v)) for v in x.tolist()], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- GEMM
+
+def _decode_codes_torch(t):
+    return t.view(torch.float8_e4m3fn).double().numpy()
+
+
+def _exact_gemm_fractions(a_codes, sa, b_codes, sb_rows, c=None):
+    """Brute force: D_pre[m][n] = C + sum_k a*sa[m][k//128] * b*sb[n][k//128] in rationals."""
+    A = _decode_codes_torch(torch.from_numpy(a_codes))
+    B = _decode_codes_torch(torch.from_numpy(b_codes))
+    M, K = A.shape
+    N = B.shape[0]
+    out = [[None] * N for _ in range(M)]
+    for m in range(M):
+        arow = [Fraction(float(A[m, k])) * Fraction(float(sa[m, k // 128])) for k in range(K)]
+        for n in range(N):
+            s = Fraction(0) if c is None else Fraction(_bf16_value(int(c[m, n])))
+            for k in range(K):
+                if arow[k]:
+                    s += arow[k] * Fraction(float(B[n, k])) * Fraction(float(sb_rows[n, k // 128]))
+            out[m][n] = s
+    return out
+
+
+def _case_np(case):
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    return a, b
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(3, 4, 256, 0), (2, 130, 384, 1), (4, 3, 200, 2),
+                                         (1, 1, 128, 3)])
+def test_gemm_bruteforce_rationals(orc, M, N, K, seed):
+    """Oracle pre-rounding sum vs exact rational sum (tiny shapes, N=130 has a
+    partial 128-row block of B scales; K=200 a short last K-group), with
+    non-power-of-two FP32 scales and a C term."""
+    case = inputs.dense_case(M, N, K, seed=seed, with_c=True)
+    a, b = _case_np(case)
+    rng = np.random.default_rng(seed)
+    sa = case.sfa.double().numpy() * rng.choice([1.0, 0.75, 3.0, 1.1], case.sfa.shape)
+    sfb = case.sfb.double().numpy() * rng.choice([1.0, 0.625, 5.0], case.sfb.shape)
+    sb_rows = sfb[np.arange(N) // 128]
+    c = case.c.view(torch.int16).numpy().view(np.uint16)
+    d, pre = orc.gemm_nt(a, sa, b, sb_rows, c=c, want_pre=True)
+    exact = _exact_gemm_fractions(a, sa, b, sb_rows, c)
+    for m in range(M):
+        for n in range(N):
+            ex = exact[m][n]
+            # fp64 error bound: each term carries one product rounding and the
+            # running sum one addition rounding -> (K + 2) * 2^-52 * sum|terms|
+            bound = Fraction(K + 2, 2 ** 52) * (abs(ex) + 64)
+            assert abs(Fraction(pre[m, n]) - ex) <= bound
+            # the bf16 result is the single RNE of the pre-rounding value ...
+            assert d[m, n] == _bf16_nearest_bruteforce(Fraction(pre[m, n]))
+            # ... and equals the RNE of the exact value unless that sits within
+            # the fp64 error of a bf16 rounding boundary
+            want = _bf16_nearest_bruteforce(ex)
+            if d[m, n] != want:
+                mid = (Fraction(_bf16_value(int(d[m, n]))) + Fraction(_bf16_value(want))) / 2
+                assert abs(mid - ex) <= bound, (m, n)
+
+
+def test_gemm_pow2_scales_bruteforce_exact(orc):
+    """With power-of-two scales every product is exact; at this size the fp64
+    sum is exact too, so pre-rounding values equal the rationals exactly."""
+    case = inputs.dense_case(3, 5, 384, seed=7)
+    a, b = _case_np(case)
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(5) // 128]
+    d, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    exact = _exact_gemm_fractions(a, sa, b, sb_rows)
+    for m in range(3):
+        for n in range(5):
+            assert Fraction(pre[m, n]) == exact[m][n]
+            assert d[m, n] == _bf16_nearest_bruteforce(exact[m][n])
+
+
+def test_gemm_integer_exact(orc):
+    """Integer-valued codes and 2^j scales: D == bf16_rne(exact integer matmul),
+    the exact value computed with an int64 matmul at a common denominator."""
+    M, N, K = 33, 150, 640
+    case = inputs.integer_exact_case(M, N, K, seed=5)
+    a, b = _case_np(case)
+    sa = case.sfa.double().numpy()
+    sfb = case.sfb.double().numpy()
+    sb_rows = sfb[np.arange(N) // 128]
+    d = orc.gemm_nt(a, sa, b, sb_rows)
+    ai = case.a.float().numpy().astype(np.int64)
+    bi = case.b.float().numpy().astype(np.int64)
+    # scale exponents times 4 -> integers; common denominator 2^4
+    ea = np.log2(sa).astype(np.int64)
+    eb = np.log2(sb_rows).astype(np.int64)
+    kk = np.arange(K) // 128
+    a_scaled = ai * (2 ** (ea[:, kk] + 2))            # [M, K] ints (ea >= -2)
+    b_scaled = bi * (2 ** (eb[:, kk] + 2))            # [N, K] ints (eb >= 0)
+    num = a_scaled @ b_scaled.T                       # exact int64, value = num / 16
+    for m in range(M):
+        for n in range(N):
+            ex = Fraction(int(num[m, n]), 16)
+            want = _bf16_nearest_bruteforce(ex)
+            if ex < 0 and want == 0:
+                want = 0x8000
+            assert d[m, n] == want
+
+
+def test_gemm_unit_scales_matches_torch_matmul(orc):
+    """All scales 1: the definition reduces to a plain float64 matmul of the
+    decoded operands (a library routine), up to fp64 summation order."""
+    M, N, K = 17, 40, 512
+    case = inputs.dense_case(M, N, K, seed=11)
+    a, b = _case_np(case)
+    sa = np.ones((M, K // 128))
+    sb_rows = np.ones((N, K // 128))
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    ref = (case.a.double() @ case.b.double().T).numpy()
+    assert np.allclose(pre, ref, rtol=1e-13, atol=1e-12)
+
+
+def test_gemm_scaled_matches_expanded_torch_matmul(orc):
+    """With scales, the definition is (A*S_A)(B*S_B)^T with the scale tables
+    spread to every element (LinearQuant page) -- here via torch float64."""
+    M, N, K = 20, 260, 384
+    case = inputs.dense_case(M, N, K, seed=12, with_c=True, b_scale_exp_range=(-8, 4))
+    a, b = _case_np(case)
+    kk = torch.arange(K) // 128
+    nn = torch.arange(N) // 128
+    A = case.a.double() * case.sfa.double()[:, kk]
+    B = case.b.double() * case.sfb.double()[nn][:, kk]
+    ref = (case.c.double() + A @ B.T).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[nn.numpy()]
+    c = case.c.view(torch.int16).numpy().view(np.uint16)
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, c=c, want_pre=True)
+    assert np.allclose(pre, ref, rtol=1e-12, atol=1e-9)
+
+
+def test_gemm_pow2_linearity(orc):
+    """Scaling one row's A scales by 2^t scales that output row by 2^t exactly;
+    scaling one B block row's scales scales exactly its 128 output columns."""
+    M, N, K = 6, 260, 256
+    case = inputs.dense_case(M, N, K, seed=13)
+    a, b = _case_np(case)
+    sa = case.sfa.double().numpy()
+    sfb = case.sfb.double().numpy()
+    sb_rows = sfb[np.arange(N) // 128]
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    sa2 = sa.copy()
+    sa2[2] *= 8.0
+    _, pre2 = orc.gemm_nt(a, sa2, b, sb_rows, want_pre=True)
+    assert np.array_equal(pre2[2], pre[2] * 8.0)
+    assert np.array_equal(np.delete(pre2, 2, 0), np.delete(pre, 2, 0))
+    sfb3 = sfb.copy()
+    sfb3[1] *= 0.25
+    _, pre3 = orc.gemm_nt(a, sa, b, sfb3[np.arange(N) // 128], want_pre=True)
+    assert np.array_equal(pre3[:, 128:256], pre[:, 128:256] * 0.25)
+    assert np.array_equal(pre3[:, :128], pre[:, :128])
+    assert np.array_equal(pre3[:, 256:], pre[:, 256:])
+
+
+def test_gemm_single_k_group_isolated(orc):
+    """Only K-group 1 of A row 0 is non-zero: the result is that group's partial
+    dot product alone (catches k/128 <-> scale index mix-ups and transposes)."""
+    M, N, K = 2, 3, 384
+    case = inputs.dense_case(M, N, K, seed=14)
+    a, b = _case_np(case)
+    a = a.copy()
+    a[0, :128] = 0
+    a[0, 256:] = 0
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(N) // 128]
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    A = _decode_codes_torch(torch.from_numpy(a))
+    B = _decode_codes_torch(torch.from_numpy(b))
+    for n in range(N):
+        want = sum(Fraction(float(A[0, k])) * Fraction(float(B[n, k])) for k in range(128, 256))
+        want *= Fraction(float(sa[0, 1])) * Fraction(float(sb_rows[n, 1]))
+        assert Fraction(pre[0, n]) == want
+
+
+def test_promotion_regrouping_equals_flat_sum(orc):
+    """PaperTrace §2.2: sum over 128-K blocks of sa*sb*(block dot) equals the
+    flat per-element sum (checked in rationals against the oracle)."""
+    M, N, K = 2, 2, 512
+    case = inputs.dense_case(M, N, K, seed=15)
+    a, b = _case_np(case)
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(N) // 128]
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    A = _decode_codes_torch(torch.from_numpy(a))
+    B = _decode_codes_torch(torch.from_numpy(b))
+    for m in range(M):
+        for n in range(N):
+            final = Fraction(0)
+            for kb in range(K // 128):
+                accum = sum(Fraction(float(A[m, k])) * Fraction(float(B[n, k]))
+                            for k in range(kb * 128, kb * 128 + 128))
+                final += Fraction(float(sa[m, kb])) * Fraction(float(sb_rows[n, kb])) * accum
+            assert Fraction(pre[m, n]) == final
+
+
+def test_gemm_sampled_equals_full(orc):
+    case = inputs.dense_case(40, 300, 640, seed=16, with_c=True)
+    a, b = _case_np(case)
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(300) // 128]
+    c = case.c.view(torch.int16).numpy().view(np.uint16)
+    d = orc.gemm_nt(a, sa, b, sb_rows, c=c)
+    rng = np.random.default_rng(0)
+    rows, cols = rng.integers(0, 40, 500), rng.integers(0, 300, 500)
+    s = orc.gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, c=c)
+    assert np.array_equal(s, d[rows, cols])
+
+
+# ---------------------------------------------------------------- grouped
+
+def test_contiguous_equals_dense_per_expert(orc):
+    """Contiguous grouped GEMM == dense GEMM of each expert's segment; padding
+    rows (-1) untouched (PaperTrace §5.1)."""
+    case = inputs.contiguous_case(3, 200, 256, seed=17, m_per_expert=[5, 130, 0])
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[:, np.arange(200) // 128]
+    layout = case.grouped_layout.numpy()
+    sentinel = np.full((a.shape[0], 200), 0x7FC1, dtype=np.uint16)
+    d = orc.m_grouped_contiguous(a, sa, b, sb_rows, layout, d_init=sentinel)
+    for e in range(3):
+        rows = np.nonzero(layout == e)[0]
+        if len(rows):
+            ref = orc.gemm_nt(a[rows], sa[rows], b[e], sb_rows[e])
+            assert np.array_equal(d[rows], ref)
+    assert np.all(d[layout < 0] == 0x7FC1)
+    assert case.a.shape[0] == 128 + 256 + 0
+
+
+def test_masked_equals_dense_per_expert(orc):
+    case = inputs.masked_case(3, 40, 136, 256, seed=18, masked_m=[0, 40, 7])
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[:, np.arange(136) // 128]
+    sentinel = np.full((3, 40, 136), 0x7FC1, dtype=np.uint16)
+    d = orc.m_grouped_masked(a, sa, b, sb_rows, case.masked_m.numpy(), d_init=sentinel)
+    for e, m in enumerate([0, 40, 7]):
+        if m:
+            assert np.array_equal(d[e, :m], orc.gemm_nt(a[e, :m], sa[e, :m], b[e], sb_rows[e]))
+        assert np.all(d[e, m:] == 0x7FC1)
+
+
+# ---------------------------------------------------------------- generator
+
+def test_generator_recipe_scales_are_pow2_and_codes_fit():
+    case = inputs.dense_case(64, 256, 384, seed=0)
+    for s in (case.sfa, case.sfb):
+        m, e = torch.frexp(s.double())
+        assert torch.all(m == 0.5)
+    x = torch.randn(64, 384, generator=inputs.generator(0))
+    assert torch.equal(inputs.quantize_1x128(x)[0].view(torch.uint8), case.a.view(torch.uint8))
+    assert not torch.isnan(case.a.float()).any() and not torch.isnan(case.b.float()).any()
+    # amax of each group lands in (224, 448]
+    deq = case.a.float().view(64, 3, 128).abs().amax(-1)
+    assert torch.all(deq <= 448) and torch.all(deq > 224 - 32)
