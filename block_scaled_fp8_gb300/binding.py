@@ -1,0 +1,215 @@
+"""Thin Python binding of the C ABI in include/dg.h (argument marshalling only).
+
+Every function takes torch tensors that already live on the current CUDA
+device, passes their data pointers and the current torch stream to the
+library, and raises DGError on a non-OK status.  All arithmetic happens in
+the library's CUDA kernels; nothing here computes.  The library must have
+been built (block_scaled_fp8_gb300.build) -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdg_gb300.so")
+
+DG_SF_FP32 = 0
+DG_SF_UE8M0_PACKED = 1
+DG_DEV_TIMEOUT = 1
+DG_DEV_INEXACT_SCALE = 2
+DG_DEV_BAD_GROUP = 4
+DG_DEBUG_DROP_ONE_LOAD = 1
+DG_DEBUG_PRINT_CONFIGS = 2
+
+# Every symbol include/dg.h declares.
+EXPORTS = (
+    "dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
+    "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
+    "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
+    "dg_set_wait_timeout_ms", "dg_set_debug_flags", "dg_status_string", "dg_get_last_config",
+)
+
+
+class DGError(RuntimeError):
+    def __init__(self, fn: str, status: int, name: str):
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+        self.name = name
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library not built: {LIB_PATH} is missing "
+                    "(run block_scaled_fp8_gb300.build.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32
+            L.dg_fp8_gemm_nt.argtypes = [P, i64, P, i32, P, i64, P, i32, P, i64, P, i64, i32, i32,
+                                         i32, P, P]
+            L.dg_transform_sf.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P]
+            L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes = [P, i64, P, i32, P, i64, P, i32, P,
+                                                              i64, P, i32, i32, i32, i32, P, P]
+            L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
+                                                          i32, i32, i32, P, P]
+            for f in ("dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
+                      "dg_m_grouped_fp8_gemm_nt_masked"):
+                getattr(L, f).restype = i32
+            L.dg_get_mk_alignment_for_contiguous_layout.restype = i32
+            L.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
+            L.dg_get_tma_aligned_size.restype = i64
+            L.dg_get_tma_aligned_size.argtypes = [i64, i32]
+            L.dg_packed_sf_words.restype = i64
+            L.dg_packed_sf_words.argtypes = [i32, i32, i32]
+            L.dg_set_num_sms.restype = None
+            L.dg_set_num_sms.argtypes = [i32]
+            L.dg_get_num_sms.restype = i32
+            L.dg_get_num_sms.argtypes = []
+            L.dg_set_wait_timeout_ms.restype = None
+            L.dg_set_wait_timeout_ms.argtypes = [i32]
+            L.dg_set_debug_flags.restype = None
+            L.dg_set_debug_flags.argtypes = [u32]
+            L.dg_status_string.restype = ctypes.c_char_p
+            L.dg_status_string.argtypes = [i32]
+            L.dg_get_last_config.restype = None
+            L.dg_get_last_config.argtypes = [ctypes.POINTER(ctypes.c_int)]
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DGError(fn, status, lib().dg_status_string(status).decode())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _sf_fmt(t):
+    return DG_SF_FP32 if t.dtype == torch.float32 else DG_SF_UE8M0_PACKED
+
+
+# --------------------------------------------------------------------- utilities
+
+def get_mk_alignment_for_contiguous_layout() -> int:
+    return int(lib().dg_get_mk_alignment_for_contiguous_layout())
+
+
+def get_tma_aligned_size(mn: int, elem_size: int) -> int:
+    return int(lib().dg_get_tma_aligned_size(mn, elem_size))
+
+
+def packed_sf_words(batch: int, mn: int, k: int) -> int:
+    return int(lib().dg_packed_sf_words(batch, mn, k))
+
+
+def set_num_sms(n: int):
+    lib().dg_set_num_sms(n)
+
+
+def get_num_sms() -> int:
+    return int(lib().dg_get_num_sms())
+
+
+def set_wait_timeout_ms(ms: int):
+    lib().dg_set_wait_timeout_ms(ms)
+
+
+def set_debug_flags(flags: int):
+    lib().dg_set_debug_flags(flags)
+
+
+def last_config() -> dict:
+    arr = (ctypes.c_int * 6)()
+    lib().dg_get_last_config(arr)
+    return {"block_m": arr[0], "block_n": arr[1], "stages": arr[2], "grid": arr[3],
+            "kind": arr[4], "launches": arr[5]}
+
+
+# --------------------------------------------------------------------- entry points
+
+def dg_transform_sf(sf: torch.Tensor, gran_mn: int, mn: int, out: torch.Tensor,
+                    packed: bool = True, status: torch.Tensor | None = None, stream=None):
+    """sf: float32 [batch?, mn_rows, sf_k] -> out (int32 packed [batch?, psf_k, align4(mn)]
+    or float32 [batch?, sf_k, align4(mn)])."""
+    assert sf.dtype == torch.float32 and sf.is_contiguous() and out.is_contiguous()
+    s = sf if sf.dim() == 3 else sf.unsqueeze(0)
+    batch, mn_rows, sf_k = s.shape
+    _check("dg_transform_sf", lib().dg_transform_sf(
+        _p(s), batch, mn_rows, sf_k, gran_mn, mn, DG_SF_UE8M0_PACKED if packed else DG_SF_FP32,
+        _p(out), _p(status), _stream(stream)))
+    return out
+
+
+def transform_sf(sf: torch.Tensor, gran_mn: int, mn: int, packed: bool = True,
+                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Allocates the output with torch and calls dg_transform_sf."""
+    batch = () if sf.dim() == 2 else (sf.shape[0],)
+    sf_k = sf.shape[-1]
+    stride = (mn + 3) // 4 * 4
+    if packed:
+        out = torch.empty(*batch, (sf_k + 3) // 4, stride, dtype=torch.int32, device=sf.device)
+    else:
+        out = torch.empty(*batch, sf_k, stride, dtype=torch.float32, device=sf.device)
+    return dg_transform_sf(sf, gran_mn, mn, out, packed=packed, status=status, stream=stream)
+
+
+def dg_fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                   d: torch.Tensor, c: torch.Tensor | None = None,
+                   status: torch.Tensor | None = None, stream=None):
+    """D = C + A @ B^T.  a [M, K] and b [N, K] float8_e4m3fn (row stride = stride(0));
+    sfa/sfb packed int32 (MN-major) or float32 ([M, sf_k] / [ceil(N/128), sf_k]);
+    d (and c) bf16 [M, N] with unit column stride."""
+    M, K = a.shape
+    N = b.shape[0]
+    assert a.stride(1) == 1 and b.stride(1) == 1 and d.stride(1) == 1
+    assert d.dtype == torch.bfloat16 and (c is None or (c.dtype == torch.bfloat16 and c.stride(1) == 1))
+    _check("dg_fp8_gemm_nt", lib().dg_fp8_gemm_nt(
+        _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(0), _p(sfb), _sf_fmt(sfb),
+        _p(c), 0 if c is None else c.stride(0), _p(d), d.stride(0), M, N, K, _p(status),
+        _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, grouped_layout,
+                                        status: torch.Tensor | None = None, stream=None):
+    """a [M_total, K]; b [E, N, K]; sfa packed [psf_k, align4(M_total)];
+    sfb packed [E, psf_k, align4(N)]; d bf16 [M_total, N]; grouped_layout int32 [M_total]."""
+    M, K = a.shape
+    E, N, _ = b.shape
+    assert b.stride(0) == N * b.stride(1) and b.stride(2) == 1
+    _check("dg_m_grouped_fp8_gemm_nt_contiguous", lib().dg_m_grouped_fp8_gemm_nt_contiguous(
+        _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(1), _p(sfb), _sf_fmt(sfb),
+        _p(d), d.stride(0), _p(grouped_layout), M, N, K, E, _p(status), _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, expected_m: int,
+                                    status: torch.Tensor | None = None, stream=None):
+    """a [E, max_m, K]; b [E, N, K]; sfa packed [E, psf_k, align4(max_m)];
+    sfb packed [E, psf_k, align4(N)]; d bf16 [E, max_m, N]; masked_m int32 [E] (device)."""
+    E, max_m, K = a.shape
+    N = b.shape[1]
+    assert a.is_contiguous() and b.is_contiguous() and d.is_contiguous()
+    _check("dg_m_grouped_fp8_gemm_nt_masked", lib().dg_m_grouped_fp8_gemm_nt_masked(
+        _p(a), _p(sfa), _sf_fmt(sfa), _p(b), _p(sfb), _sf_fmt(sfb), _p(d), _p(masked_m), E, max_m,
+        expected_m, N, K, _p(status), _stream(stream)))
+    return d

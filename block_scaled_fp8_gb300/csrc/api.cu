@@ -1,0 +1,398 @@
+// Host side of the C ABI: argument validation, TMA descriptors, tile-shape
+// choice and kernel launch.  Declarations and contracts are in include/dg.h.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+// ------------------------------------------------------------------ settings
+
+std::atomic<int> g_num_sms_override{0};
+std::atomic<int> g_timeout_ms{2000};
+std::atomic<uint32_t> g_debug_flags{0};
+thread_local int g_last_config[6] = {0, 0, 0, 0, 0, 0};
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int checked = 0;     // 0 unknown, 1 ok, -1 unsupported
+    int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// cuTensorMapEncodeTiled, reached through the runtime so that the library does
+// not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn get_encode() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+// Current device must be an sm_103 GPU; fills its SM count.
+dg_status check_device(int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &di = g_devices[dev];
+    if (di.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DG_ERR_CUDA;
+        di.checked = (major == 10 && minor == 3) ? 1 : -1;
+        di.num_sms = sms;
+    }
+    if (di.checked < 0) return DG_ERR_UNSUPPORTED;
+    int ov = g_num_sms_override.load();
+    *num_sms = (ov > 0 && ov < di.num_sms) ? ov : di.num_sms;
+    return DG_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t align4(int64_t x) { return (x + 3) / 4 * 4; }
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base,
+               uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    EncodeTiledFn enc = get_encode();
+    if (enc == nullptr) return false;
+    (void)elem_bytes;
+    cuuint64_t dims[2] = {dim0, dim1};
+    cuuint64_t strides[1] = {stride1_bytes};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Block-N values compiled into the block-scaled kernel family.
+constexpr int kBsBlockN[] = {16, 32, 48, 64, 96, 128, 160, 176, 192, 224, 256};
+constexpr int kMaxBlockNWithC = 192;
+
+// Tile-shape choice: maximise the fraction of SM-time spent on useful tiles
+// (wave quantisation x N padding) weighted by a per-tile efficiency that grows
+// with BLOCK_N (larger tiles re-read less operand data per FLOP).  Split-K is
+// never used: with few M blocks, narrow BLOCK_N is what fills the SMs (the
+// non-power-of-two block idea of PaperTrace §4.3).
+int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c) {
+    double best = -1.0;
+    int best_bn = 128;
+    for (int bn : kBsBlockN) {
+        if (with_c && bn > kMaxBlockNWithC) continue;
+        const int64_t nb = cdiv64(n, bn);
+        const int64_t tiles = m_blocks * nb;
+        const int64_t waves = cdiv64(tiles, num_sms);
+        const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
+        const double pad_eff = static_cast<double>(n) / static_cast<double>(nb * bn);
+        const double tile_eff = static_cast<double>(bn) / (bn + 64.0);
+        const double score = wave_eff * pad_eff * tile_eff;
+        if (score > best + 1e-9) {
+            best = score;
+            best_bn = bn;
+        }
+    }
+    return best_bn;
+}
+
+__global__ void dg_fill_d_kernel(const uint16_t *c, int64_t ldc, uint16_t *d, int64_t ldd, int m,
+                                 int n) {
+    const int64_t total = static_cast<int64_t>(m) * n;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / n, col = i % n;
+        d[r * ldd + col] = c ? c[r * ldc + col] : static_cast<uint16_t>(0);
+    }
+}
+
+// Operand views of one block-scaled launch (all 2-D, K or MN contiguous).
+struct BsOperands {
+    const void *a;  int64_t lda;  uint64_t a_rows;
+    const void *b;  int64_t ldb;  uint64_t b_rows;
+    const void *sfa; uint64_t sfa_mn; uint64_t sfa_slices;  // inner = MN rows, outer = K slices
+    const void *sfb; uint64_t sfb_mn; uint64_t sfb_slices;
+    void *d;        int64_t ldd;  uint64_t d_rows;
+};
+
+dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_blocks_hint,
+                              int64_t max_tiles_per_n_block, int num_sms, cudaStream_t stream) {
+    const bool with_c = p.c != nullptr;
+    const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
+    KernelInfo info;
+    if (!get_bs_kernel_info(bn, with_c, &info)) return DG_ERR_UNSUPPORTED;
+    TensorMaps maps;
+    const int k = p.k;
+    bool ok = true;
+    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
+                    kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
+                    align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    ok &= encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfb, o.sfb_mn, o.sfb_slices,
+                    align4(o.sfb_mn) * 4, bn, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
+                    32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (!ok) return DG_ERR_CUDA;
+    p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
+    p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
+    p.group_m = 8;
+    p.d = static_cast<uint16_t *>(o.d);
+    p.ldd = o.ldd;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
+    uint32_t dbg = g_debug_flags.load();
+    if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
+    p.debug_flags = dbg;
+    const int64_t tiles = max_tiles_per_n_block * p.num_n_blocks;
+    const int grid = static_cast<int>(tiles < num_sms ? (tiles < 1 ? 1 : tiles) : num_sms);
+    if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
+        std::fprintf(stderr, "[dg] mode=%d rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d grid=%d\n",
+                     p.mode, p.rows, p.n, k, kBlockM, bn, info.stages, info.smem_bytes, grid);
+    g_last_config[0] = kBlockM;
+    g_last_config[1] = bn;
+    g_last_config[2] = info.stages;
+    g_last_config[3] = grid;
+    g_last_config[4] = 0;
+    g_last_config[5] = 1;
+    cudaError_t e = launch_bs_gemm(bn, maps, p, grid, stream);
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+GemmParams base_params(int mode, int rows, int n, int k, int32_t *status) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.mode = mode;
+    p.rows = rows;
+    p.n = n;
+    p.k = k;
+    p.num_groups = 1;
+    p.status = status;
+    p.sf_k = static_cast<int>(cdiv64(k, kGran));
+    return p;
+}
+
+dg_status check_operand_rules(const void *a, int64_t lda, const void *b, int64_t ldb, int n, int k) {
+    if (a == nullptr || b == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b)) return DG_ERR_ALIGNMENT;
+    if (k % 16 != 0 || n % 8 != 0) return DG_ERR_ALIGNMENT;
+    if (lda < k || ldb < k) return DG_ERR_INVALID_ARG;
+    if (lda % 16 != 0 || ldb % 16 != 0) return DG_ERR_ALIGNMENT;
+    return DG_OK;
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+const char *dg_status_string(int s) {
+    switch (s) {
+        case DG_OK: return "DG_OK";
+        case DG_ERR_INVALID_ARG: return "DG_ERR_INVALID_ARG";
+        case DG_ERR_ALIGNMENT: return "DG_ERR_ALIGNMENT";
+        case DG_ERR_LAYOUT: return "DG_ERR_LAYOUT";
+        case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
+        case DG_ERR_CUDA: return "DG_ERR_CUDA";
+        case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+        case DG_ERR_INEXACT_SCALE: return "DG_ERR_INEXACT_SCALE";
+        case DG_ERR_BAD_GROUP: return "DG_ERR_BAD_GROUP";
+        default: return "DG_ERR_UNKNOWN";
+    }
+}
+
+int dg_get_mk_alignment_for_contiguous_layout(void) { return kBlockM; }
+
+int64_t dg_get_tma_aligned_size(int64_t mn, int elem_size) {
+    if (elem_size <= 0 || 16 % elem_size != 0) return -1;
+    const int64_t align = 16 / elem_size;
+    return (mn + align - 1) / align * align;
+}
+
+int64_t dg_packed_sf_words(int batch, int mn, int k) {
+    if (batch < 0 || mn < 0 || k < 0) return -1;
+    const int64_t sf_k = cdiv64(k, kGran);
+    return static_cast<int64_t>(batch) * cdiv64(sf_k, 4) * align4(mn);
+}
+
+void dg_set_num_sms(int n) { g_num_sms_override.store(n > 0 ? n : 0); }
+
+int dg_get_num_sms(void) {
+    int n = 0;
+    if (check_device(&n) != DG_OK) return 0;
+    return n;
+}
+
+void dg_set_wait_timeout_ms(int ms) { g_timeout_ms.store(ms > 0 ? ms : 2000); }
+
+void dg_set_debug_flags(uint32_t flags) { g_debug_flags.store(flags); }
+
+void dg_get_last_config(int out[6]) {
+    for (int i = 0; i < 6; ++i) out[i] = g_last_config[i];
+}
+
+dg_status dg_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn, int mn,
+                          int out_fmt, void *out, int32_t *status_dev, void *stream) {
+    if (batch < 0 || mn < 0 || sf_k < 0 || mn_rows < 0) return DG_ERR_INVALID_ARG;
+    if (gran_mn != 1 && gran_mn != kGran) return DG_ERR_UNSUPPORTED;
+    if (out_fmt != DG_SF_FP32 && out_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(mn_rows) != cdiv64(mn, gran_mn)) return DG_ERR_LAYOUT;
+    if (batch == 0 || mn == 0 || sf_k == 0) return DG_OK;
+    if (batch > 65535 || sf_k > 65535 * 4) return DG_ERR_UNSUPPORTED;
+    if (sf == nullptr || out == nullptr) return DG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(sf) & 3u) || !aligned16(out)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    dg_status st = check_device(&sms);
+    if (st != DG_OK) return st;
+    cudaError_t e = launch_transform_sf(sf, batch, mn_rows, sf_k, gran_mn, mn, out_fmt, out,
+                                        status_dev, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+dg_status dg_fp8_gemm_nt(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                         int64_t ldb, const void *sfb, int sfb_fmt, const void *c, int64_t ldc,
+                         void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev,
+                         void *stream) {
+    if (m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != sfb_fmt) return DG_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0) return DG_OK;
+    if (d == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || ldd < n || ldd % 8 != 0 || n % 8 != 0) return DG_ERR_ALIGNMENT;
+    if (c != nullptr && (!aligned16(c) || ldc < n || ldc % 8 != 0)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    if (k == 0) {
+        dg_status st = check_device(&sms);
+        if (st != DG_OK) return st;
+        dg_fill_d_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint16_t *>(c), ldc, static_cast<uint16_t *>(d), ldd, m, n);
+        g_last_config[5] = 1;
+        return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    }
+    dg_status st = check_operand_rules(a, lda, b, ldb, n, k);
+    if (st != DG_OK) return st;
+    if (sfa == nullptr || sfb == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeDense, m, n, k, status_dev);
+    p.c = static_cast<const uint16_t *>(c);
+    p.ldc = ldc;
+    if (sfa_fmt == DG_SF_FP32) return DG_ERR_UNSUPPORTED;  // promotion kernel: see below
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    p.num_m_blocks = static_cast<int>(cdiv64(m, kBlockM));
+    BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),
+                 sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(psf_k),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k),
+                 d,   ldd, static_cast<uint64_t>(m)};
+    return launch_block_scaled(p, o, p.num_m_blocks, p.num_m_blocks, sms,
+                               static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,
+                                              int sfa_fmt, const void *b, int64_t ldb,
+                                              const void *sfb, int sfb_fmt, void *d, int64_t ldd,
+                                              const int32_t *grouped_layout, int m_total, int n,
+                                              int k, int num_groups, int32_t *status_dev,
+                                              void *stream) {
+    if (m_total < 0 || n < 0 || k < 0 || num_groups < 1) return DG_ERR_INVALID_ARG;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != DG_SF_UE8M0_PACKED || sfb_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_UNSUPPORTED;
+    if (m_total % kBlockM != 0) return DG_ERR_LAYOUT;
+    if (m_total == 0 || n == 0) return DG_OK;
+    if (k == 0) return DG_ERR_UNSUPPORTED;
+    dg_status st = check_operand_rules(a, lda, b, ldb, n, k);
+    if (st != DG_OK) return st;
+    if (d == nullptr || sfa == nullptr || sfb == nullptr || grouped_layout == nullptr)
+        return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || !aligned16(sfa) || !aligned16(sfb) || ldd < n || ldd % 8 != 0)
+        return DG_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(num_groups) * n > INT32_MAX) return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeContiguous, m_total, n, k, status_dev);
+    p.num_groups = num_groups;
+    p.grouped_layout = grouped_layout;
+    p.num_m_blocks = m_total / kBlockM;
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    BsOperands o{a,   lda, static_cast<uint64_t>(m_total),
+                 b,   ldb, static_cast<uint64_t>(num_groups) * n,
+                 sfa, static_cast<uint64_t>(m_total), static_cast<uint64_t>(psf_k),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k * num_groups),
+                 d,   ldd, static_cast<uint64_t>(m_total)};
+    return launch_block_scaled(p, o, p.num_m_blocks, p.num_m_blocks, sms,
+                               static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void *a, const void *sfa, int sfa_fmt,
+                                          const void *b, const void *sfb, int sfb_fmt, void *d,
+                                          const int32_t *masked_m, int num_groups, int max_m,
+                                          int expected_m, int n, int k, int32_t *status_dev,
+                                          void *stream) {
+    if (num_groups < 1 || max_m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if (num_groups > kMaxGroupsMasked) return DG_ERR_UNSUPPORTED;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != DG_SF_UE8M0_PACKED || sfb_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_UNSUPPORTED;
+    if (max_m == 0 || n == 0) return DG_OK;
+    if (k == 0) return DG_ERR_UNSUPPORTED;
+    dg_status st = check_operand_rules(a, k, b, k, n, k);
+    if (st != DG_OK) return st;
+    if (d == nullptr || sfa == nullptr || sfb == nullptr || masked_m == nullptr)
+        return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(num_groups) * max_m > INT32_MAX ||
+        static_cast<int64_t>(num_groups) * n > INT32_MAX)
+        return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeMasked, max_m, n, k, status_dev);
+    p.num_groups = num_groups;
+    p.masked_m = masked_m;
+    p.num_m_blocks = static_cast<int>(cdiv64(max_m, kBlockM));
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    const int exp_m = expected_m > 0 ? (expected_m < max_m ? expected_m : max_m) : max_m;
+    const int64_t m_blocks_hint = static_cast<int64_t>(num_groups) * cdiv64(exp_m, kBlockM);
+    BsOperands o{a,   k,   static_cast<uint64_t>(num_groups) * max_m,
+                 b,   k,   static_cast<uint64_t>(num_groups) * n,
+                 sfa, static_cast<uint64_t>(max_m), static_cast<uint64_t>(psf_k * num_groups),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k * num_groups),
+                 d,   n,   static_cast<uint64_t>(num_groups) * max_m};
+    return launch_block_scaled(p, o, m_blocks_hint,
+                               static_cast<int64_t>(num_groups) * p.num_m_blocks, sms,
+                               static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+
+namespace dg {
+
+constexpr int kBlockM = 128;   // rows per tile (one UMMA M=128, TMEM lanes)
+constexpr int kBlockK = 128;   // K per pipeline stage (= scale granularity)
+constexpr int kGran = 128;     // scale granularity along K (and N for FP32 B scales)
+constexpr int kMaxGroupsMasked = 1024;
+
+enum GemmMode : int { kModeDense = 0, kModeContiguous = 1, kModeMasked = 2 };
+
+// Runtime parameters of one GEMM launch (passed by value).
+struct GemmParams {
+    int mode;
+    int rows;            // dense: M; contiguous: M_total; masked: max_m (rows per expert)
+    int n, k;
+    int num_m_blocks;    // blocks of 128 rows (dense/contiguous: over all rows; masked: per expert, max)
+    int num_n_blocks;
+    int num_k_blocks;
+    int num_groups;
+    int group_m;         // tile-order group size along M (L2 reuse)
+    const int32_t *grouped_layout;  // contiguous
+    const int32_t *masked_m;        // masked
+    const uint16_t *c;   // dense: bf16 C or nullptr
+    int64_t ldc;
+    uint16_t *d;         // bf16 D (used for direct stores)
+    int64_t ldd;
+    int32_t *status;
+    uint64_t timeout_ns;
+    uint32_t debug_flags;
+    // FP32-promotion kernel only
+    const float *sfa_f32;   // [rows][sf_k]
+    const float *sfb_f32;   // [ceil(n/128)][sf_k]
+    int sf_k;
+};
+
+struct TensorMaps {
+    CUtensorMap a, b, sfa, sfb, d;
+};
+
+// Per-instantiation launch information.
+struct KernelInfo {
+    int block_n;
+    int stages;
+    int smem_bytes;
+    int threads;
+};
+
+// Block-scaled (UE8M0) tcgen05 kernel family: returns false if block_n is not
+// compiled in.
+bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info);
+cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+                           cudaStream_t stream);
+
+// FP32-scale promotion kernel family.
+bool get_promote_kernel_info(int block_n, KernelInfo *info);
+cudaError_t launch_promote_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+                                cudaStream_t stream);
+
+// Scale-factor transform.
+cudaError_t launch_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn,
+                                int mn, int out_fmt, void *out, int32_t *status,
+                                cudaStream_t stream);
+
+}  // namespace dg

@@ -1,0 +1,385 @@
+// Block-scaled FP8 GEMM for sm_103a: D = C + A @ B^T with UE8M0 scales applied
+// inside the tensor-core MMA.
+//
+// Method (sources: "02 · DeepGEMM 技术解析" §2-§4; "DeepSeek V4 源码剖析 第13章"
+// §13.3-§13.4): per output tile, accumulate over K-blocks of 128 the products
+// sa * sb * (A_kb @ B_kb^T) in FP32 and write bf16.  On this GPU the scale
+// multiply happens in the MMA itself: tcgen05.mma kind::mxf8f6f4.block_scale
+// reads one UE8M0 exponent per row of A and per row of B for every 32-wide K
+// step from tensor memory, so with power-of-two scales the first-level product
+// is exact and the FP32 accumulator in TMEM runs over the whole K (the
+// Blackwell form of the pages' two-level accumulation, §13.3 point 1).
+//
+// CTA layout (one CTA per SM, persistent):
+//   warp 0      TMA producer: A, B and the packed scale words into a ring of
+//               STAGES shared-memory stages (full/empty mbarriers).
+//   warp 1      TMEM owner and MMA issuer: re-orders each stage's scale words
+//               for tcgen05.cp, copies them to TMEM, issues 4 MMAs (K=32 each)
+//               per stage, and signals the accumulator to the epilogue.
+//   warps 2..9  epilogue: TMEM -> registers (then the accumulator is released
+//               at once), optional + C, bf16 RNE, swizzled staging in shared
+//               memory, TMA store (direct stores where masked rows end inside
+//               the tile).
+// Accumulators: NUM_ACC buffers of BLOCK_N TMEM columns each, so the next
+// tile's MMAs overlap this tile's stores.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "dg_internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace dg {
+
+template <int BN>
+struct BsConfig {
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128 is 16..256, step 16");
+    static constexpr int kThreads = 320;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kSfbChunks = (BN + 127) / 128;        // 128-word tcgen05.cp chunks
+    static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per stage
+    static constexpr int kABytes = kBlockM * kBlockK;           // 16 KB
+    static constexpr int kBBytes = BN * kBlockK;
+    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfbBytes = 512 * kSfbChunks;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + BN * 4;
+    static constexpr int kEpiChunk = 16;                        // columns per epilogue chunk
+    static constexpr int kNumChunks = BN / kEpiChunk;
+    static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;  // 16 KB
+    static constexpr int kMaskedPrefixBytes = (kMaxGroupsMasked + 1) * 4;
+    static constexpr int kSmemLimit = 232448;                   // 227 KB per CTA
+    static constexpr int kFixedBytes = 1024 /*align*/ + kStagingBytes + 512 /*barriers*/ +
+                                       kMaskedPrefixBytes;
+    static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
+    static constexpr int kStages = kStagesBySmem > 8 ? 8 : kStagesBySmem;
+    static constexpr int kNumAcc = (2 * BN + kStages * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = 512;
+    static_assert(kNumAcc * BN + kStages * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kStages >= 3, "pipeline too shallow");
+    static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+};
+
+// Reorder 128 scale words (row i at word i, as TMA lands them from the
+// MN-major tensor) into the 32x128b tcgen05.cp source layout: 16-byte row r
+// holds the words of MN rows r, r+32, r+64, r+96.  After the copy, TMEM lane
+// r (in each 32-lane sub-partition) column j holds the word of row 32*j + r.
+// One warp; in place.  The XOR spreads the accesses over the banks.
+__device__ __forceinline__ void sf_transpose_for_cp(uint32_t *buf, uint32_t lane) {
+    uint32_t v[4];
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) v[i] = buf[((i ^ (lane >> 3)) & 3) * 32 + lane];
+    __syncwarp();
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) buf[lane * 4 + ((i ^ (lane >> 3)) & 3)] = v[i];
+}
+
+template <int BN, bool WITH_C>
+__global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
+    dg_bs_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                      const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_sfa,
+                      const __grid_constant__ CUtensorMap tm_sfb,
+                      const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
+    using Cfg = BsConfig<BN>;
+    constexpr int S = Cfg::kStages;
+    constexpr int NUM_ACC = Cfg::kNumAcc;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem_a = smem;
+    uint8_t *smem_b = smem_a + S * Cfg::kABytes;
+    uint8_t *smem_sfa = smem_b + S * Cfg::kBBytes;
+    uint8_t *smem_sfb = smem_sfa + S * Cfg::kSfaBytes;
+    uint8_t *smem_stage_out = smem_sfb + S * Cfg::kSfbBytes;  // 1024-aligned (all sizes are)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_stage_out + Cfg::kStagingBytes);
+    uint64_t *full_bar = bars;
+    uint64_t *empty_bar = bars + S;
+    uint64_t *tfull_bar = bars + 2 * S;
+    uint64_t *tempty_bar = tfull_bar + NUM_ACC;
+    uint64_t *drain_bar = tempty_bar + NUM_ACC;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const int psf_k = (p.num_k_blocks + 3) >> 2;
+    WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            mbar_init(&tfull_bar[a], 1);
+            mbar_init(&tempty_bar[a], Cfg::kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_sfa);
+        tma_prefetch_desc(&tm_sfb);
+        tma_prefetch_desc(&tm_d);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    if (p.mode == kModeMasked) build_masked_prefix(p, prefix);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+    const int num_tiles = total_tiles(p, prefix);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;
+            bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+                Tile tile;
+                if (!get_tile<BN>(p, prefix, t, psf_k, tile, true)) continue;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
+                    if (drop) {
+                        drop = false;  // diagnostic: leave this stage empty
+                    } else {
+                        mbar_arrive_expect_tx(&full_bar[stage], Cfg::kTxBytes);
+                        tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
+                                    kb * kBlockK, tile.a_row0);
+                        tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[stage],
+                                    kb * kBlockK, tile.b_row0);
+                        tma_load_2d(smem_sfa + stage * Cfg::kSfaBytes, &tm_sfa, &full_bar[stage],
+                                    tile.sfa_x, tile.sfa_y0 + (kb >> 2));
+                        tma_load_2d(smem_sfb + stage * Cfg::kSfbBytes, &tm_sfb, &full_bar[stage],
+                                    tile.n0, tile.sfb_y0 + (kb >> 2));
+                        issued |= 1u << stage;
+                    }
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+        prod_done:
+            // never leave the CTA with loads in flight: wait for the last fill of every stage
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s))
+                    mbar_wait(&full_bar[s], s < stage ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const uint32_t sf_col0 = NUM_ACC * BN;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            Tile tile;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)))
+                goto mma_done;
+            tc_fence_after_sync();
+            {
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
+                        goto mma_done;
+                    uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sfa + stage * Cfg::kSfaBytes);
+                    uint32_t *sfb_buf = reinterpret_cast<uint32_t *>(smem_sfb + stage * Cfg::kSfbBytes);
+                    sf_transpose_for_cp(sfa_buf, lane);
+#pragma unroll
+                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc_fence_after_sync();
+                        const uint32_t sfa_tmem = tmem_base + sf_col0 + stage * Cfg::kSfCols;
+                        const uint32_t sfb_tmem = sfa_tmem + 4;
+                        tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+#pragma unroll
+                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                            tc_cp_32x128b_warpx4(sfb_tmem + 4 * c,
+                                                 make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                        const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
+                        const uint64_t a_desc =
+                            make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
+                        const uint64_t b_desc =
+                            make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
+                                        sfb_tmem, (kb | k) != 0);
+                        tc_commit(&empty_bar[stage]);
+                    }
+                    __syncwarp();
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (lane == 0) tc_commit(&tfull_bar[acc]);
+            __syncwarp();
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+        }
+    mma_done:
+        // all MMAs and copies this thread issued must finish before TMEM is freed
+        if (lane == 0) {
+            tc_commit(drain_bar);
+            mbar_wait(drain_bar, 0, ctl, DG_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t ew = warp - 2;          // 0..7
+        const uint32_t quad = warp & 3;        // TMEM lane quadrant this warp may access
+        const uint32_t half = ew >> 2;         // which interleaved half of the column chunks
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t buf = 0;
+        uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            Tile tile;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            const int local_row = quad * 32 + lane;
+            const int row = tile.a_row0 + local_row;       // row in the 2-D view of D
+            const bool row_ok = local_row < tile.valid_rows && (p.mode == kModeMasked || row < p.rows);
+            const bool direct = tile.valid_rows < kBlockM;
+            // C does not depend on the accumulator: fetch it before waiting for the MMAs.
+            uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
+            constexpr bool has_c = WITH_C;
+            if constexpr (WITH_C) {
+#pragma unroll
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                    const int c = 2 * j + half;
+                    const int col0 = tile.n0 + c * Cfg::kEpiChunk;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+                        if (c < Cfg::kNumChunks && row_ok && col0 + 8 * h < p.n)
+                            cv = __ldg(reinterpret_cast<const uint4 *>(
+                                p.c + static_cast<int64_t>(row) * p.ldc + col0 + 8 * h));
+                        cpk[j][4 * h + 0] = cv.x;
+                        cpk[j][4 * h + 1] = cv.y;
+                        cpk[j][4 * h + 2] = cv.z;
+                        cpk[j][4 * h + 3] = cv.w;
+                    }
+                }
+            }
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
+            tc_fence_after_sync();
+            // TMEM -> registers, two chunks per wait; + C in FP32; one RNE to bf16.
+            uint32_t out[Cfg::kChunksPerWarp][8];
+#pragma unroll
+            for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
+                uint32_t v[2][16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int c = 2 * (j0 + u) + half;
+                    if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
+                        tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (j0 + u >= Cfg::kChunksPerWarp) continue;
+                    reg_fence16(v[u]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float lo = __uint_as_float(v[u][2 * i]);
+                        float hi = __uint_as_float(v[u][2 * i + 1]);
+                        if constexpr (has_c) {
+                            lo += __uint_as_float(cpk[j0 + u][i] << 16);
+                            hi += __uint_as_float(cpk[j0 + u][i] & 0xFFFF0000u);
+                        }
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                        out[j0 + u][i] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+
+#pragma unroll
+            for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                const int c = 2 * j + half;
+                if (c >= Cfg::kNumChunks) continue;
+                const int col0 = tile.n0 + c * Cfg::kEpiChunk;
+                if (direct) {
+                    if (row_ok) {
+                        uint16_t *drow = p.d + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (col0 + 8 * h < p.n)
+                                *reinterpret_cast<uint4 *>(drow + 8 * h) =
+                                    make_uint4(out[j][4 * h], out[j][4 * h + 1], out[j][4 * h + 2],
+                                               out[j][4 * h + 3]);
+                    }
+                } else {
+                    uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
+                    if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // 32-byte swizzle: 16-byte unit h of row r sits at unit h ^ ((r >> 2) & 1)
+                        const uint32_t off = lane * 32 + ((h ^ ((lane >> 2) & 1)) * 16);
+                        *reinterpret_cast<uint4 *>(sbuf + off) =
+                            make_uint4(out[j][4 * h], out[j][4 * h + 1], out[j][4 * h + 2], out[j][4 * h + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, sbuf, col0, tile.a_row0 + quad * 32);
+                        bulk_commit_group();
+                    }
+                    buf ^= 1;
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <int BN, bool WITH_C>
+cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
+                                cudaStream_t stream) {
+    using Cfg = BsConfig<BN>;
+    // The attribute is per device; setting it on every launch costs ~1 us of
+    // host time only, and keeps multi-device processes correct.
+    cudaError_t e = cudaFuncSetAttribute(dg_bs_gemm_kernel<BN, WITH_C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dg_bs_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
+        maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
+    return cudaGetLastError();
+}
+
+template <int BN>
+void fill_bs_info(KernelInfo *info) {
+    using Cfg = BsConfig<BN>;
+    info->block_n = BN;
+    info->stages = Cfg::kStages;
+    info->smem_bytes = Cfg::kSmemBytes;
+    info->threads = Cfg::kThreads;
+}
+
+}  // namespace dg

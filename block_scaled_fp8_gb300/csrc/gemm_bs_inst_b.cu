@@ -1,0 +1,11 @@
+// Instantiations of the block-scaled GEMM kernel (compiled in parallel, one group per file).
+#include "gemm_bs.cuh"
+
+namespace dg {
+template cudaError_t launch_bs_gemm_impl<96, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<96, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<128, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<128, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<160, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<160, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+}  // namespace dg

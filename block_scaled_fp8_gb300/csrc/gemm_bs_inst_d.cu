@@ -1,0 +1,7 @@
+// Instantiations of the block-scaled GEMM kernel (compiled in parallel, one group per file).
+#include "gemm_bs.cuh"
+
+namespace dg {
+template cudaError_t launch_bs_gemm_impl<224, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs_gemm_impl<256, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+}  // namespace dg

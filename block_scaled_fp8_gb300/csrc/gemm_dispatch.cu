@@ -1,0 +1,62 @@
+// Maps a runtime BLOCK_N to the compiled block-scaled kernel instantiations
+// (which live in the gemm_bs_inst_*.cu units).
+#include "gemm_bs.cuh"
+
+namespace dg {
+
+// BLOCK_N values compiled without C, and the subset also compiled with C
+// (the C-accumulate epilogue holds C in registers, which caps BLOCK_N).
+#define DG_BS_BLOCK_N_LIST(X) X(16) X(32) X(48) X(64) X(96) X(128) X(160) X(176) X(192) X(224) X(256)
+#define DG_BS_BLOCK_N_LIST_C(X) X(16) X(32) X(48) X(64) X(96) X(128) X(160) X(176) X(192)
+
+#define DG_EXTERN(BN) \
+    extern template cudaError_t launch_bs_gemm_impl<BN, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+DG_BS_BLOCK_N_LIST(DG_EXTERN)
+#undef DG_EXTERN
+#define DG_EXTERN(BN) \
+    extern template cudaError_t launch_bs_gemm_impl<BN, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
+#undef DG_EXTERN
+
+bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info) {
+    if (with_c) {
+        switch (block_n) {
+#define DG_CASE(BN) case BN: fill_bs_info<BN>(info); return true;
+            DG_BS_BLOCK_N_LIST_C(DG_CASE)
+#undef DG_CASE
+            default: return false;
+        }
+    }
+    switch (block_n) {
+#define DG_CASE(BN) case BN: fill_bs_info<BN>(info); return true;
+        DG_BS_BLOCK_N_LIST(DG_CASE)
+#undef DG_CASE
+        default: return false;
+    }
+}
+
+cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+                           cudaStream_t stream) {
+    if (p.c != nullptr) {
+        switch (block_n) {
+#define DG_CASE(BN) case BN: return launch_bs_gemm_impl<BN, true>(maps, p, grid, stream);
+            DG_BS_BLOCK_N_LIST_C(DG_CASE)
+#undef DG_CASE
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (block_n) {
+#define DG_CASE(BN) case BN: return launch_bs_gemm_impl<BN, false>(maps, p, grid, stream);
+        DG_BS_BLOCK_N_LIST(DG_CASE)
+#undef DG_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// The FP32-scale promotion kernel family is not compiled in this build.
+bool get_promote_kernel_info(int, KernelInfo *) { return false; }
+cudaError_t launch_promote_gemm(int, const TensorMaps &, const GemmParams &, int, cudaStream_t) {
+    return cudaErrorNotSupported;
+}
+
+}  // namespace dg

@@ -1,0 +1,71 @@
+// Scale-factor transform: FP32 scales -> MN-major, TMA-aligned layout.
+//
+// PaperTrace "02 · DeepGEMM 技术解析" §3.1-3.2 and "DeepSeek V4 源码剖析 第13章"
+// §13.3: the packed form keeps the 8 exponent bits of each FP32 scale
+// ((bits >> 23) & 0xff, so a non-power-of-two scale is truncated: 0.75 -> 0.5),
+// puts four consecutive K-groups in one int32 little-endian by K, and stores the
+// words MN-major with a K-slice stride of align(mn, 4) words; the scale rows are
+// broadcast from gran_mn to one per MN index.  Memory bound: one thread per
+// output word, consecutive threads write consecutive MN rows (coalesced).
+#include "dg_internal.h"
+
+namespace dg {
+
+__global__ void __launch_bounds__(256) dg_transform_sf_packed_kernel(
+    const float *__restrict__ sf, int mn_rows, int sf_k, int gran_mn, int mn, int psf_k,
+    int stride, uint32_t *__restrict__ out, int32_t *status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int pslice = blockIdx.y;
+    const int b = blockIdx.z;
+    uint32_t word = 0;
+    bool inexact = false;
+    if (i < mn) {
+        const float *row = sf + (static_cast<int64_t>(b) * mn_rows + i / gran_mn) * sf_k;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = 4 * pslice + j;
+            if (k < sf_k) {
+                const uint32_t bits = __float_as_uint(__ldg(row + k));
+                word |= ((bits >> 23) & 0xFFu) << (8 * j);
+                inexact |= (bits & 0x807FFFFFu) != 0u;
+            }
+        }
+    }
+    if (i < stride) out[(static_cast<int64_t>(b) * psf_k + pslice) * stride + i] = word;
+    if (status != nullptr) {
+        const unsigned any = __ballot_sync(0xFFFFFFFFu, inexact);
+        if (any != 0u && (threadIdx.x & 31) == 0) atomicOr(status, DG_DEV_INEXACT_SCALE);
+    }
+}
+
+__global__ void __launch_bounds__(256) dg_transform_sf_f32_kernel(
+    const float *__restrict__ sf, int mn_rows, int sf_k, int gran_mn, int mn, int stride,
+    float *__restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int k = blockIdx.y;
+    const int b = blockIdx.z;
+    if (i >= stride) return;
+    float v = 0.0f;
+    if (i < mn) v = __ldg(sf + (static_cast<int64_t>(b) * mn_rows + i / gran_mn) * sf_k + k);
+    out[(static_cast<int64_t>(b) * sf_k + k) * stride + i] = v;
+}
+
+cudaError_t launch_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn,
+                                int mn, int out_fmt, void *out, int32_t *status,
+                                cudaStream_t stream) {
+    const int stride = (mn + 3) / 4 * 4;
+    const int psf_k = (sf_k + 3) / 4;
+    const dim3 block(256);
+    if (out_fmt == DG_SF_UE8M0_PACKED) {
+        const dim3 grid((stride + 255) / 256, psf_k, batch);
+        dg_transform_sf_packed_kernel<<<grid, block, 0, stream>>>(
+            sf, mn_rows, sf_k, gran_mn, mn, psf_k, stride, static_cast<uint32_t *>(out), status);
+    } else {
+        const dim3 grid((stride + 255) / 256, sf_k, batch);
+        dg_transform_sf_f32_kernel<<<grid, block, 0, stream>>>(sf, mn_rows, sf_k, gran_mn, mn,
+                                                               stride, static_cast<float *>(out));
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,207 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) block-scaled FP8 GEMM library.
+ *
+ * The library computes D = C + A @ B^T ("NT": A row-major [M,K], B stored as
+ * [N,K], both K-contiguous), where A and B are FP8 E4M3 ("fn" flavour), A
+ * carries one scale per 1x128 K-group of each row and B one scale per 128x128
+ * block, accumulation is FP32 and D is bf16.  Sources: "02 · DeepGEMM 技术解析"
+ * (PaperTrace) §1.1, §2, §3, §5 and "DeepSeek V4 源码剖析 第13章 DeepGEMM"
+ * §13.3, §13.6.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named a, b, c, d, sfa, sfb, out, grouped_layout, masked_m,
+ *    status_dev are DEVICE pointers; the caller owns and allocates all of
+ *    them.  The library allocates no device memory on any call.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous: it validates its arguments on the host, enqueues
+ *    its kernels on `stream` and returns.
+ *  - Host-detected errors (bad sizes, strides, alignment, formats, or a
+ *    device that is not sm_103) are returned synchronously as a dg_status
+ *    before anything is enqueued; nothing is written in that case.
+ *  - Device-detected conditions are OR-ed as dg_device_flag bits into
+ *    *status_dev (an int32 in device memory, nullable) and are visible
+ *    after the stream is synchronised.  Kernels never trap: every wait on the
+ *    device has a time limit, after which the kernel sets DG_DEV_TIMEOUT and
+ *    returns.
+ *  - Scale factors have granularity 128 along K (and 128 along N for B, in
+ *    the FP32 form).  sf_k = ceil(K/128), psf_k = ceil(sf_k/4),
+ *    align4(x) = ceil(x/4)*4.
+ *  - Packed UE8M0 scales (DG_SF_UE8M0_PACKED) are int32 words holding the
+ *    exponent bytes of four consecutive K-groups, little-endian by K index,
+ *    laid out MN-major: word (row i, slice p) at p*align4(mn) + i, batch
+ *    stride psf_k*align4(mn) (PaperTrace §3.1).  B's packed scales are one row
+ *    per N index (the 128x128 block scale broadcast along N, §3.2).
+ *  - Operand preconditions: 16-byte aligned base pointers; K % 16 == 0;
+ *    lda, ldb (in elements = bytes) multiples of 16; N % 8 == 0 and ldc, ldd
+ *    (bf16 elements) multiples of 8.
+ *  - No split-K: each output element is reduced by one CTA in a fixed K
+ *    order, so a row's result does not depend on M or on the other rows of
+ *    the batch (batch invariance, §13.1).
+ */
+#ifndef DG_GB300_H
+#define DG_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,   /* a size, pointer or enum value is out of range */
+    DG_ERR_ALIGNMENT = 2,     /* a pointer or leading dimension breaks the 16-byte rules */
+    DG_ERR_LAYOUT = 3,        /* a scale layout does not match the contract */
+    DG_ERR_UNSUPPORTED = 4,   /* valid request outside what this build implements */
+    DG_ERR_CUDA = 5,          /* a CUDA runtime call failed (launch, attribute, device) */
+    DG_ERR_TIMEOUT = 6,       /* used by helpers that read back the device status */
+    DG_ERR_INEXACT_SCALE = 7, /* idem */
+    DG_ERR_BAD_GROUP = 8      /* idem */
+} dg_status;
+
+/* Bits OR-ed into *status_dev by the kernels. */
+typedef enum {
+    DG_DEV_TIMEOUT = 1,        /* a bounded device wait ran out; outputs are incomplete */
+    DG_DEV_INEXACT_SCALE = 2,  /* an FP32 scale was not a power of two and was truncated */
+    DG_DEV_BAD_GROUP = 4       /* an expert id >= num_groups, or masked_m[e] > max_m */
+} dg_device_flag;
+
+typedef enum {
+    DG_SF_FP32 = 0,          /* FP32 scales in the caller's natural form (see each call) */
+    DG_SF_UE8M0_PACKED = 1   /* packed MN-major UE8M0 int32 words (see conventions) */
+} dg_sf_format;
+
+/*
+ * dg_fp8_gemm_nt -- D[m,n] = C[m,n] + sum_k A[m,k]*sfa(m,k/128) * B[n,k]*sfb(n,k/128)
+ * ("DeepSeek V4 源码剖析 第13章" §13.3 interface and pseudocode; PaperTrace §2).
+ *
+ *   a     [m, lda]  E4M3 codes, row m at a + m*lda, K contiguous.
+ *   b     [n, ldb]  E4M3 codes (the "column-major B" of the NT layout).
+ *   sfa, sfb formats must match:
+ *     DG_SF_UE8M0_PACKED: sfa int32 [psf_k][align4(m)], sfb int32
+ *       [psf_k][align4(n)] (one row per N index).  Runs the tcgen05
+ *       block-scaled MMA path, exact for power-of-two scales.
+ *     DG_SF_FP32: sfa float [m][sf_k] row-major, sfb float [ceil(n/128)][sf_k]
+ *       row-major.  Any finite FP32 scale is honoured: each 128-K block is
+ *       accumulated on the tensor core and promoted into an FP32 accumulator
+ *       as acc += sa*sb*partial (the two-level accumulation of PaperTrace §2.2).
+ *   c     bf16 [m, ldc] or NULL (C = 0).  c may equal d (in-place accumulate).
+ *   d     bf16 [m, ldd] output.
+ *   m, n, k >= 0; m == 0 or n == 0 is a no-op; k == 0 gives D = C.
+ *   status_dev: nullable int32 device word receiving dg_device_flag bits.
+ */
+dg_status dg_fp8_gemm_nt(const void *a, int64_t lda, const void *sfa, int sfa_fmt,
+                         const void *b, int64_t ldb, const void *sfb, int sfb_fmt,
+                         const void *c, int64_t ldc, void *d, int64_t ldd,
+                         int m, int n, int k, int32_t *status_dev, void *stream);
+
+/*
+ * dg_transform_sf -- FP32 scales into the MN-major, TMA-aligned layout the GEMMs
+ * consume (PaperTrace §3.1-3.2; "DeepSeek V4 源码剖析 第13章" §13.3 constraint 2).
+ *
+ *   sf      float [batch][mn_rows][sf_k] row-major; row r covers MN indices
+ *           r*gran_mn .. r*gran_mn + gran_mn - 1.
+ *   gran_mn 1 (activation, 1x128) or 128 (weight, 128x128); mn_rows must equal
+ *           ceil(mn / gran_mn).  The output has one row per MN index.
+ *   out_fmt DG_SF_UE8M0_PACKED: out int32 [batch][psf_k][align4(mn)]; byte j of
+ *             word (p, i) = (bits(sf[i/gran_mn][4p+j]) >> 23) & 0xff, i.e. the
+ *             exponent byte: a non-power-of-two scale is truncated (0.75 -> 0.5,
+ *             3 -> 2) and DG_DEV_INEXACT_SCALE is set in *status_dev.
+ *           DG_SF_FP32: out float [batch][sf_k][align4(mn)] (transpose only).
+ *           Bytes past sf_k in the last word and pad rows mn..align4(mn)-1 are 0.
+ *   out must not overlap sf.  Size it with dg_packed_sf_words (int32 count) or
+ *   batch*sf_k*align4(mn) floats.
+ */
+dg_status dg_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn, int mn,
+                          int out_fmt, void *out, int32_t *status_dev, void *stream);
+
+/*
+ * dg_m_grouped_fp8_gemm_nt_contiguous -- MoE GEMM grouped along M only
+ * (PaperTrace §5.1; "DeepSeek V4 源码剖析 第13章" §13.6): the rows of all
+ * experts are concatenated along M, each expert's segment starting on a
+ * multiple of dg_get_mk_alignment_for_contiguous_layout() (128) rows.
+ *
+ *   a      [m_total, lda] E4M3; sfa packed int32 [psf_k][align4(m_total)].
+ *   b      [num_groups][n][ldb] E4M3 (expert stride n*ldb);
+ *   sfb    packed int32 [num_groups][psf_k][align4(n)].
+ *   d      bf16 [m_total, ldd].
+ *   grouped_layout int32 [m_total]: expert id of each row, -1 for padding
+ *          rows.  Every 128-row block belongs to one expert, taken from its
+ *          first row; a block whose first row is -1 is skipped and its D rows
+ *          are left unwritten.  D rows marked -1 inside a computed block hold
+ *          unspecified values.  An id >= num_groups sets DG_DEV_BAD_GROUP and
+ *          the block is skipped.
+ *   Only DG_SF_UE8M0_PACKED scales are accepted (else DG_ERR_UNSUPPORTED).
+ */
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,
+                                              int sfa_fmt, const void *b, int64_t ldb,
+                                              const void *sfb, int sfb_fmt, void *d, int64_t ldd,
+                                              const int32_t *grouped_layout, int m_total, int n,
+                                              int k, int num_groups, int32_t *status_dev,
+                                              void *stream);
+
+/*
+ * dg_m_grouped_fp8_gemm_nt_masked -- MoE decode GEMM with static shapes
+ * (PaperTrace §5.2; "DeepSeek V4 源码剖析 第13章" §13.6): expert e multiplies
+ * its first masked_m[e] rows; nothing else of D is read or written.
+ *
+ *   a      [num_groups][max_m][k] E4M3, dense.
+ *   sfa    packed int32 [num_groups][psf_k][align4(max_m)].
+ *   b      [num_groups][n][k] E4M3, dense; sfb packed int32 [num_groups][psf_k][align4(n)].
+ *   d      bf16 [num_groups][max_m][n], dense.
+ *   masked_m int32 [num_groups] in device memory (read by the kernel, so the
+ *          call can be captured in a CUDA graph with changing counts); values
+ *          are clamped to [0, max_m], and a value > max_m sets DG_DEV_BAD_GROUP.
+ *   expected_m  the caller's estimate of the mean valid rows per expert; only
+ *          used to choose the tile shape (it never changes a result).
+ *   num_groups <= 1024.  Only DG_SF_UE8M0_PACKED scales are accepted.
+ */
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void *a, const void *sfa, int sfa_fmt,
+                                          const void *b, const void *sfb, int sfb_fmt, void *d,
+                                          const int32_t *masked_m, int num_groups, int max_m,
+                                          int expected_m, int n, int k, int32_t *status_dev,
+                                          void *stream);
+
+/* Row alignment of each expert segment in the contiguous layout (the tile
+ * height, PaperTrace §5.1): 128. */
+int dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* mn rounded up so that mn * elem_size is a multiple of 16 bytes (the TMA
+ * stride rule behind align(mn, 4) for int32, PaperTrace §3.1). */
+int64_t dg_get_tma_aligned_size(int64_t mn, int elem_size);
+
+/* Number of int32 words of a packed scale tensor: batch * psf_k * align4(mn)
+ * for a K extent of k elements. */
+int64_t dg_packed_sf_words(int batch, int mn, int k);
+
+/* Number of SMs the persistent kernels use (default: all SMs of the current
+ * device).  n <= 0 restores the default. */
+void dg_set_num_sms(int n);
+int dg_get_num_sms(void);
+
+/* Time limit of every bounded device wait, in milliseconds (default 2000). */
+void dg_set_wait_timeout_ms(int ms);
+
+/* Diagnostics.  DG_DEBUG_DROP_ONE_LOAD makes the first CTA of the next GEMM
+ * launch skip its first operand load, so its consumer's bounded wait runs
+ * out and DG_DEV_TIMEOUT is reported (used by the failure-detection test;
+ * the flag clears itself after one launch).  DG_DEBUG_PRINT_CONFIGS prints
+ * the chosen tile configuration of each GEMM to stderr. */
+enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2 };
+void dg_set_debug_flags(uint32_t flags);
+
+/* Human-readable name of a dg_status value. */
+const char *dg_status_string(int status);
+
+/* Tile configuration the last GEMM call on this thread launched:
+ * out[0]=BLOCK_M, out[1]=BLOCK_N, out[2]=stages, out[3]=grid size,
+ * out[4]=kernel kind (0 block-scaled, 1 FP32-promotion), out[5]=number of
+ * kernel launches of that call. */
+void dg_get_last_config(int out[6]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_GB300_H */

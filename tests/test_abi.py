@@ -1,0 +1,86 @@
+"""The C-ABI library loads and exports every symbol include/dg.h declares, and
+its host-side validation answers without a GPU (no compute is run here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_scaled_fp8_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_fp8_gb300 import build
+    build.build()
+    return binding.lib()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dg.h")).read()
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(binding.EXPORTS) == _declared_symbols()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_layout_helpers(lib):
+    assert binding.get_mk_alignment_for_contiguous_layout() == 128
+    assert binding.get_tma_aligned_size(30, 4) == 32
+    assert binding.get_tma_aligned_size(2112, 4) == 2112
+    assert binding.get_tma_aligned_size(3, 2) == 8
+    # batch * ceil(ceil(K/128)/4) * align4(mn)
+    assert binding.packed_sf_words(1, 4096, 16384) == 32 * 4096
+    assert binding.packed_sf_words(32, 256, 7168) == 32 * 14 * 256
+    assert binding.packed_sf_words(1, 30, 128) == 32
+    assert lib.dg_status_string(3) == b"DG_ERR_LAYOUT"
+
+
+def _gemm(lib, **kw):
+    args = dict(a=16, lda=128, sfa=16, sfa_fmt=1, b=16, ldb=128, sfb=16, sfb_fmt=1, c=None,
+                ldc=0, d=16, ldd=64, m=8, n=64, k=128)
+    args.update(kw)
+    P = ctypes.c_void_p
+    return lib.dg_fp8_gemm_nt(P(args["a"]), args["lda"], P(args["sfa"]), args["sfa_fmt"],
+                              P(args["b"]), args["ldb"], P(args["sfb"]), args["sfb_fmt"],
+                              P(args["c"]), args["ldc"], P(args["d"]), args["ldd"], args["m"],
+                              args["n"], args["k"], None, None)
+
+
+def test_host_validation_without_gpu(lib):
+    """Bad arguments are rejected before any CUDA call (the pointers here are
+    never dereferenced)."""
+    assert _gemm(lib, m=-1) == 1                       # DG_ERR_INVALID_ARG
+    assert _gemm(lib, sfa_fmt=5) == 1
+    assert _gemm(lib, sfa_fmt=0) == 4                  # mixed formats: DG_ERR_UNSUPPORTED
+    assert _gemm(lib, m=0) == 0                        # empty problem: no-op
+    assert _gemm(lib, n=0) == 0
+    assert _gemm(lib, d=24) == 2                       # misaligned D: DG_ERR_ALIGNMENT
+    assert _gemm(lib, ldd=60) == 2
+    assert _gemm(lib, n=60, ldd=64) == 2               # N % 8 != 0
+    assert _gemm(lib, k=120, lda=128, ldb=128) == 2    # K % 16 != 0
+    assert _gemm(lib, lda=120) == 1                    # lda < K
+    assert _gemm(lib, lda=136, k=128) == 2             # lda % 16 != 0
+    assert _gemm(lib, a=0) == 1                        # null A
+    P = ctypes.c_void_p
+    # transform: granularity and row-count rules
+    assert lib.dg_transform_sf(P(16), 1, 4, 2, 2, 4, 1, P(16), None, None) == 4
+    assert lib.dg_transform_sf(P(16), 1, 5, 2, 128, 300, 1, P(16), None, None) == 3
+    assert lib.dg_transform_sf(P(16), 1, 4, 2, 1, 4, 9, P(16), None, None) == 1
+    assert lib.dg_transform_sf(P(16), 0, 0, 2, 1, 0, 1, P(16), None, None) == 0
+    # grouped
+    assert lib.dg_m_grouped_fp8_gemm_nt_contiguous(P(16), 128, P(16), 1, P(16), 128, P(16), 1,
+                                                   P(16), 64, P(16), 100, 64, 128, 2, None,
+                                                   None) == 3   # M_total % 128 != 0
+    assert lib.dg_m_grouped_fp8_gemm_nt_masked(P(16), P(16), 1, P(16), P(16), 1, P(16), P(16),
+                                               2000, 64, 32, 64, 128, None, None) == 4
+    assert lib.dg_m_grouped_fp8_gemm_nt_masked(P(16), P(16), 0, P(16), P(16), 0, P(16), P(16),
+                                               2, 64, 32, 64, 128, None, None) == 4
