@@ -1,0 +1,445 @@
+"""Benchmark of the block-scaled FP8 GEMM hot path on GB300.
+
+One step = one pass of the hot path over the V3-like linear workload: for each
+of the six GEMMs M in {128, 4096} x (N, K) in {(2112, 7168), (24576, 1536),
+(7168, 16384)}, the activation's FP32 1x128 scales are packed to the MN-major
+UE8M0 layout (dg_transform_sf) and D = A @ B^T is computed (dg_fp8_gemm_nt).
+Weights (B and their 128x128 scales, packed once) stay resident, as in serving.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job TFLOP/s (2*M*N*K summed
+over the six GEMMs, all ranks) with inputs resident in HBM; `e2e` is the same
+metric through the public API with the activations copied from pinned host
+memory and D copied back inside the timed region.  --impl reference times the
+CPU oracle (fp64, all host cores) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s and % of GB300 dense FP8 peak (1 GPU)"
+UNIT = "TFLOP/s"
+WORKLOAD = "dense NT V3-like linear shapes M in {128,4096} x (N,K) in {(2112,7168),(24576,1536),(7168,16384)}"
+SHAPES = [(m, n, k) for m in (128, 4096) for (n, k) in ((2112, 7168), (24576, 1536), (7168, 16384))]
+NOMINAL_FP8_TFLOPS = 4500.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def flops(m, n, k):
+    return 2.0 * m * n * k
+
+
+def gemm_bytes(m, n, k):
+    """Algorithmic bytes of one GEMM: A + B + D + logical 1-byte scales."""
+    return m * k + n * k + 2 * m * n + m * (k // 128) + (n // 128) * (k // 128)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def load_traffic():
+    """Per-launch DRAM traffic of the GEMM kernel from an ncu capture, valid
+    only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "gemm_dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        from block_scaled_fp8_gb300.build import source_digest
+        if rec.get("source_digest") != source_digest():
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from block_scaled_fp8_gb300 import binding, build, inputs
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # Problems: seeded synthetic data of the workload's shapes (rank-distinct seeds).
+    probs = []
+    for i, (m, n, k) in enumerate(SHAPES):
+        case = inputs.dense_case(m, n, k, seed=1000 * rank + i)
+        sfb = binding.transform_sf(case.sfb.to(dev), 128, n)           # weights: packed once
+        p = {
+            "shape": (m, n, k),
+            "a": case.a.to(dev), "sfa_f32": case.sfa.to(dev), "b": case.b.to(dev), "sfb": sfb,
+            "sfa": torch.empty((case.sfa.shape[1] + 3) // 4, (m + 3) // 4 * 4, dtype=torch.int32,
+                               device=dev),
+            "d": torch.empty(m, n, dtype=torch.bfloat16, device=dev),
+            # host side for the end-to-end leg
+            "a_host": case.a.pin_memory(), "sfa_host": case.sfa.pin_memory(),
+            "d_host": torch.empty(m, n, dtype=torch.bfloat16).pin_memory(),
+        }
+        probs.append(p)
+        del case
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    step_flops = sum(flops(*p["shape"]) for p in probs)
+    launches_per_step = 2 * len(probs)
+
+    gemm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in probs]
+
+    def step(record=False):
+        for i, p in enumerate(probs):
+            m, n, k = p["shape"]
+            binding.dg_transform_sf(p["sfa_f32"], 1, m, p["sfa"], status=status)
+            if record:
+                gemm_ev[i][0].record(stream)
+            binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
+            if record:
+                gemm_ev[i][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    bn_used = []
+    for p in probs:
+        binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
+        bn_used.append(binding.last_config())
+    torch.cuda.synchronize()
+
+    # ---------------- device-timed steps (inputs resident, L2 flushed between steps)
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    gemm_ms = [0.0] * len(probs)
+    for s in range(args.steps):
+        flush.fill_(s)
+        ev[s][0].record(stream)
+        step(record=True)
+        ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        for i in range(len(probs)):
+            gemm_ms[i] += gemm_ev[i][0].elapsed_time(gemm_ev[i][1])
+    barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    local_ms = sum(step_ms)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in timed region")
+
+    # ---------------- end to end through the public API with host buffers
+    h2d = sum(p["a_host"].numel() * p["a_host"].element_size() +
+              p["sfa_host"].numel() * 4 for p in probs)
+    d2h = sum(p["d_host"].numel() * 2 for p in probs)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for p in probs:
+            m = p["shape"][0]
+            p["a"].copy_(p["a_host"], non_blocking=True)
+            p["sfa_f32"].copy_(p["sfa_host"], non_blocking=True)
+            binding.dg_transform_sf(p["sfa_f32"], 1, m, p["sfa"], status=status)
+            binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
+            p["d_host"].copy_(p["d"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---------------- reductions over ranks (max time)
+    t = torch.tensor([local_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_total_ms = float(t[0]), float(t[1])
+    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    e2e_value = step_flops * e2e_steps * world / (e2e_total_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_TFLOPS / NOMINAL_BF16_TFLOPS
+    gemm_total_ms = sum(gemm_ms) / args.steps
+    achieved = step_flops / (gemm_total_ms * 1e-3) / 1e12
+    per_gemm = []
+    for p, ms, cfg in zip(probs, gemm_ms, bn_used):
+        m, n, k = p["shape"]
+        ms /= args.steps
+        per_gemm.append({"m": m, "n": n, "k": k, "us": round(ms * 1e3, 2),
+                         "tflops": round(flops(m, n, k) / (ms * 1e-3) / 1e12, 1),
+                         "gbs": round(gemm_bytes(m, n, k) / (ms * 1e-3) / 1e9, 1),
+                         "block_n": cfg["block_n"], "grid": cfg["grid"]})
+    traffic = load_traffic()
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 (fp32 accumulate, bf16 out)",
+            "data": "synthetic (seeded N(0,1) quantised per 1x128 / 128x128, power-of-two scales)",
+            "config": {"workload": WORKLOAD, "shapes_mnk": SHAPES,
+                       "step": "per GEMM: dg_transform_sf(activation scales) + dg_fp8_gemm_nt",
+                       "l2": "flushed between steps (256 MB write)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_nominal_fp8_peak": round(100.0 * value / NOMINAL_FP8_TFLOPS, 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_peak, 4),
+                         "peak_note": f"fp8 = {peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio), of {peaks['source']}",
+                         "kernel": "dg_bs_gemm_kernel (sum over the six GEMMs of the step)",
+                         "traffic": None if traffic is None else traffic.get("bytes_per_step")},
+            "per_gemm": per_gemm,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+    return result
+
+
+# --------------------------------------------------------------------- oracle (CPU)
+
+def oracle_sample(target_s: float, seed: int = 0):
+    """Times the oracle (as it stands) on sampled elements of the six GEMMs.
+    Returns (TFLOP/s, threads, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from block_scaled_fp8_gb300 import inputs
+
+    oracle.build()
+    threads = oracle.max_threads()
+    # Small operands suffice for sampling: the oracle reads one A row and one B
+    # row per element, so rows beyond the sample are never touched.
+    rng = np.random.default_rng(seed)
+    prepared = []
+    for i, (m, n, k) in enumerate(SHAPES):
+        rows_a, rows_b = min(m, 64), min(n, 256)
+        case = inputs.dense_case(rows_a, rows_b, k, seed=seed + i)
+        a = case.a.view(torch.uint8).numpy()
+        b = case.b.view(torch.uint8).numpy()
+        sa = case.sfa.double().numpy()
+        sb = case.sfb.double().numpy()[np.arange(rows_b) // 128]
+        prepared.append((m, n, k, a, b, sa, sb, rows_a, rows_b))
+    # calibrate: time a small sample, then size the run to target_s
+    def run(samples_per_gemm):
+        fl, t0 = 0.0, time.perf_counter()
+        for (m, n, k, a, b, sa, sb, ra, rb) in prepared:
+            rows = rng.integers(0, ra, samples_per_gemm)
+            cols = rng.integers(0, rb, samples_per_gemm)
+            oracle.gemm_nt_sampled(a, sa, b, sb, rows, cols)
+            fl += 2.0 * k * samples_per_gemm
+        return fl, time.perf_counter() - t0
+    fl, dt = run(256)
+    per_sample = dt / (256 * len(prepared))
+    n = max(256, int(target_s / max(per_sample, 1e-9) / len(prepared)))
+    fl, dt = run(n)
+    desc = (f"{n} sampled output elements of each of the six GEMMs (full-K fp64 dot products, "
+            f"{threads} OpenMP threads), {dt:.1f} s")
+    return fl / dt / 1e12, threads, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    target = max(3.0, 20.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(target * 0.3, seed=1)
+    vals, thr, desc = [], 0, ""
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        v, thr, desc = oracle_sample(target, seed=100 + s)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes_mnk": SHAPES,
+                   "step": "oracle on a bounded sample of the workload"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_case(args):
+    """One dense GEMM shape, `warmup` + `steps` launches (for ncu captures and
+    per-shape timing); prints per-launch device time."""
+    import torch
+
+    from block_scaled_fp8_gb300 import binding, build, inputs
+    build.build()
+    m, n, k = (int(x) for x in args.case.split(","))
+    dev = torch.device("cuda", 0)
+    case = inputs.dense_case(m, n, k, seed=0, with_c=args.with_c)
+    a, b = case.a.to(dev), case.b.to(dev)
+    sfa = binding.transform_sf(case.sfa.to(dev), 1, m)
+    sfb = binding.transform_sf(case.sfb.to(dev), 128, n)
+    c = case.c.to(dev) if args.with_c else None
+    d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        binding.dg_fp8_gemm_nt(a, sfa, b, sfb, d, c=c, status=status)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        binding.dg_fp8_gemm_nt(a, sfa, b, sfb, d, c=c, status=status)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert int(status.item()) == 0, int(status.item())
+    us = statistics.median(times) * 1e3
+    cfg = binding.last_config()
+    print(json.dumps({"case": [m, n, k], "with_c": args.with_c, "median_us": round(us, 2),
+                      "tflops": round(flops(m, n, k) / (us * 1e-6) / 1e12, 1),
+                      "gbs": round(gemm_bytes(m, n, k) / (us * 1e-6) / 1e9, 1), "config": cfg}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None, help="M,N,K: time one dense GEMM shape only")
+    ap.add_argument("--with-c", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        world = max(world, 1)
+
+    if args.case:
+        run_case(args)
+        return
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            v, thr, desc = oracle_sample(10.0)
+            res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+                                   "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

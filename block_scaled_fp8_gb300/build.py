@@ -37,6 +37,19 @@ def _deps():
         os.path.join(CSRC, "*.h")) + [os.path.join(HERE, "..", "include", "dg.h"), __file__]
 
 
+def source_digest() -> str:
+    """sha256 over the kernel and ABI sources (identifies the compiled kernels)."""
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+                   + glob.glob(os.path.join(CSRC, "*.h")))
+    for f in files + [os.path.join(HERE, "..", "include", "dg.h")]:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
