@@ -182,6 +182,57 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
+// FP32 scales: the two-level promotion kernel.  BLOCK_N must divide 128 so a
+// tile's columns share one B block scale.
+dg_status launch_promotion(GemmParams &p, const void *a, int64_t lda, const void *b, int64_t ldb,
+                           void *d, int64_t ldd, int num_sms, cudaStream_t stream) {
+    const int64_t m_blocks = cdiv64(p.rows, kBlockM);
+    int bn = 128;
+    double best = -1.0;
+    for (int cand : {32, 64, 128}) {
+        const int64_t nb = cdiv64(p.n, cand);
+        const int64_t tiles = m_blocks * nb;
+        const int64_t waves = cdiv64(tiles, num_sms);
+        const double score = static_cast<double>(tiles) / static_cast<double>(waves * num_sms) *
+                             static_cast<double>(p.n) / static_cast<double>(nb * cand) *
+                             (cand / (cand + 64.0));
+        if (score > best + 1e-9) { best = score; bn = cand; }
+    }
+    KernelInfo info;
+    if (!get_promote_kernel_info(bn, &info)) return DG_ERR_UNSUPPORTED;
+    TensorMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    bool ok = true;
+    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, p.k, p.rows, lda, kBlockK, kBlockM,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, p.k, p.n, ldb, kBlockK, bn,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.n, p.rows, ldd * 2, 16, 32,
+                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (!ok) return DG_ERR_CUDA;
+    p.num_m_blocks = static_cast<int>(m_blocks);
+    p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
+    p.num_k_blocks = static_cast<int>(cdiv64(p.k, kBlockK));
+    p.group_m = 8;
+    p.d = static_cast<uint16_t *>(d);
+    p.ldd = ldd;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
+    p.debug_flags = 0;
+    const int64_t tiles = m_blocks * p.num_n_blocks;
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    if (std::getenv("DG_PRINT_CONFIGS") || (g_debug_flags.load() & DG_DEBUG_PRINT_CONFIGS))
+        std::fprintf(stderr, "[dg] promote rows=%d n=%d k=%d -> BLOCK_N=%d stages=%d grid=%d\n",
+                     p.rows, p.n, p.k, bn, info.stages, grid);
+    g_last_config[0] = kBlockM;
+    g_last_config[1] = bn;
+    g_last_config[2] = info.stages;
+    g_last_config[3] = grid;
+    g_last_config[4] = 1;
+    g_last_config[5] = 1;
+    cudaError_t e = launch_promote_gemm(bn, maps, p, grid, stream);
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
 GemmParams base_params(int mode, int rows, int n, int k, int32_t *status) {
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -299,13 +350,19 @@ dg_status dg_fp8_gemm_nt(const void *a, int64_t lda, const void *sfa, int sfa_fm
     dg_status st = check_operand_rules(a, lda, b, ldb, n, k);
     if (st != DG_OK) return st;
     if (sfa == nullptr || sfb == nullptr) return DG_ERR_INVALID_ARG;
-    if (!aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    if (sfa_fmt == DG_SF_UE8M0_PACKED && (!aligned16(sfa) || !aligned16(sfb))) return DG_ERR_ALIGNMENT;
     st = check_device(&sms);
     if (st != DG_OK) return st;
     GemmParams p = base_params(kModeDense, m, n, k, status_dev);
     p.c = static_cast<const uint16_t *>(c);
     p.ldc = ldc;
-    if (sfa_fmt == DG_SF_FP32) return DG_ERR_UNSUPPORTED;  // promotion kernel: see below
+    if (sfa_fmt == DG_SF_FP32) {
+        if (reinterpret_cast<uintptr_t>(sfa) & 3u || reinterpret_cast<uintptr_t>(sfb) & 3u)
+            return DG_ERR_ALIGNMENT;
+        p.sfa_f32 = static_cast<const float *>(sfa);
+        p.sfb_f32 = static_cast<const float *>(sfb);
+        return launch_promotion(p, a, lda, b, ldb, d, ldd, sms, static_cast<cudaStream_t>(stream));
+    }
     const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
     p.num_m_blocks = static_cast<int>(cdiv64(m, kBlockM));
     BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),

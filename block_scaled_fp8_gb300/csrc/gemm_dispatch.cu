@@ -1,6 +1,7 @@
 // Maps a runtime BLOCK_N to the compiled block-scaled kernel instantiations
 // (which live in the gemm_bs_inst_*.cu units).
 #include "gemm_bs.cuh"
+#include "gemm_promote.cuh"
 
 namespace dg {
 
@@ -53,10 +54,38 @@ cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams
     }
 }
 
-// The FP32-scale promotion kernel family is not compiled in this build.
-bool get_promote_kernel_info(int, KernelInfo *) { return false; }
-cudaError_t launch_promote_gemm(int, const TensorMaps &, const GemmParams &, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+#define DG_PROMOTE_BLOCK_N_LIST(X) X(32) X(64) X(128)
+#define DG_EXTERN(BN)                                                                              \
+    extern template cudaError_t launch_promote_gemm_impl<BN, false>(const TensorMaps &,             \
+                                                                    const GemmParams &, int,         \
+                                                                    cudaStream_t);                   \
+    extern template cudaError_t launch_promote_gemm_impl<BN, true>(const TensorMaps &,              \
+                                                                   const GemmParams &, int,          \
+                                                                   cudaStream_t);
+DG_PROMOTE_BLOCK_N_LIST(DG_EXTERN)
+#undef DG_EXTERN
+
+bool get_promote_kernel_info(int block_n, KernelInfo *info) {
+    switch (block_n) {
+#define DG_CASE(BN) case BN: fill_promote_info<BN>(info); return true;
+        DG_PROMOTE_BLOCK_N_LIST(DG_CASE)
+#undef DG_CASE
+        default: return false;
+    }
+}
+
+cudaError_t launch_promote_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+                                cudaStream_t stream) {
+    const bool with_c = p.c != nullptr;
+    switch (block_n) {
+#define DG_CASE(BN)                                                                    \
+    case BN:                                                                           \
+        return with_c ? launch_promote_gemm_impl<BN, true>(maps, p, grid, stream)      \
+                      : launch_promote_gemm_impl<BN, false>(maps, p, grid, stream);
+        DG_PROMOTE_BLOCK_N_LIST(DG_CASE)
+#undef DG_CASE
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace dg

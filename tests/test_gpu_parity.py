@@ -126,6 +126,41 @@ def test_dense_strided_operands(orc):
     assert bool((d_big[:, N:] == 7.0).all()), "wrote outside [M, N]"
 
 
+@pytest.mark.parametrize("M,N,K,with_c", [(128, 256, 512, False), (200, 264, 640, True),
+                                          (300, 520, 1024, False), (64, 2112, 7168, True),
+                                          (129, 136, 336, False)])
+def test_dense_fp32_scales_promotion(orc, M, N, K, with_c):
+    """FP32 scales that are not powers of two: the two-level promotion kernel
+    honours them exactly (no UE8M0 truncation)."""
+    case = inputs.dense_case(M, N, K, seed=M * 7 + K, with_c=with_c)
+    g = inputs.generator(5)
+    mult = torch.tensor([0.75, 1.0, 3.0, 1.1, 0.6])
+    sfa = case.sfa * mult[torch.randint(0, 5, case.sfa.shape, generator=g)]
+    sfb = case.sfb * mult[torch.randint(0, 5, case.sfb.shape, generator=g)]
+    case.sfa, case.sfb = sfa, sfb
+    d = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    status = _status()
+    binding.dg_fp8_gemm_nt(case.a.to(DEV), sfa.to(DEV), case.b.to(DEV), sfb.to(DEV), d,
+                           c=None if case.c is None else case.c.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert binding.last_config()["kind"] == 1
+    assert_close(bf16_bits(d), _oracle_dense(orc, case), f"fp32 scales {M}x{N}x{K}")
+
+
+def test_fp32_and_packed_paths_agree_on_pow2_scales():
+    """With power-of-two scales both kernels compute the same GEMM; results
+    agree to within the accumulation-order tolerance."""
+    case = inputs.dense_case(256, 512, 2048, seed=21)
+    a, b = case.a.to(DEV), case.b.to(DEV)
+    d1 = torch.empty(256, 512, dtype=torch.bfloat16, device=DEV)
+    d2 = torch.empty_like(d1)
+    binding.dg_fp8_gemm_nt(a, case.sfa.to(DEV), b, case.sfb.to(DEV), d1)
+    binding.dg_fp8_gemm_nt(a, binding.transform_sf(case.sfa.to(DEV), 1, 256), b,
+                           binding.transform_sf(case.sfb.to(DEV), 128, 512), d2)
+    assert_close(bf16_bits(d1), bf16_bits(d2), "fp32 vs packed")
+
+
 def test_dense_k_zero_gives_c():
     c = torch.randn(40, 64, device=DEV).to(torch.bfloat16)
     d = torch.empty_like(c)
