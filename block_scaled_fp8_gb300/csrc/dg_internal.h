@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/dg.h"
+#include "dg.h"  // include/ is on the include path
 
 namespace dg {
 

@@ -11,15 +11,19 @@
 // Blackwell form of the pages' two-level accumulation, §13.3 point 1).
 //
 // CTA layout (one CTA per SM, persistent):
-//   warp 0      TMA producer: A, B and the packed scale words into a ring of
-//               STAGES shared-memory stages (full/empty mbarriers).
-//   warp 1      TMEM owner and MMA issuer: re-orders each stage's scale words
-//               for tcgen05.cp, copies them to TMEM, issues 4 MMAs (K=32 each)
-//               per stage, and signals the accumulator to the epilogue.
+//   warp 0      TMA producer: A and B per K-block, plus the packed scale words
+//               once per 4 K-blocks (one int32 holds 4 K-groups), into a ring
+//               of STAGES shared-memory stages (full/empty mbarriers).
+//   warp 1      TMEM owner and MMA issuer: 4 MMAs (K=32 each) per stage; the
+//               scale byte of K-block kb is selected by the instruction's
+//               scale-factor id (kb % 4); signals the accumulator to the epilogue.
 //   warps 2..9  epilogue: TMEM -> registers (then the accumulator is released
 //               at once), optional + C, bf16 RNE, swizzled staging in shared
 //               memory, TMA store (direct stores where masked rows end inside
 //               the tile).
+//   warp 10     scale-factor warp: re-orders each group's scale words for
+//               tcgen05.cp and copies them into a ring of TMEM scale slots,
+//               off the MMA issuer's critical path.
 // Accumulators: NUM_ACC buffers of BLOCK_N TMEM columns each, so the next
 // tile's MMAs overlap this tile's stores.
 #pragma once
@@ -35,8 +39,10 @@ namespace dg {
 template <int BN>
 struct BsConfig {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128 is 16..256, step 16");
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 352;
     static constexpr int kEpiWarps = 8;
+    static constexpr int kSfWarp = 10;
+    static constexpr int kSfSlots = 4;                          // TMEM scale slots (groups in flight)
     static constexpr int kSfbChunks = (BN + 127) / 128;        // 128-word tcgen05.cp chunks
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per stage
     static constexpr int kABytes = kBlockM * kBlockK;           // 16 KB
@@ -55,9 +61,9 @@ struct BsConfig {
                                        kMaskedPrefixBytes;
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStages = kStagesBySmem > 8 ? 8 : kStagesBySmem;
-    static constexpr int kNumAcc = (2 * BN + kStages * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
-    static_assert(kNumAcc * BN + kStages * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -101,8 +107,10 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     uint64_t *empty_bar = bars + S;
     uint64_t *tfull_bar = bars + 2 * S;
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;
-    uint64_t *drain_bar = tempty_bar + NUM_ACC;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
+    uint64_t *sf_ready_bar = tempty_bar + NUM_ACC;
+    uint64_t *sf_free_bar = sf_ready_bar + Cfg::kSfSlots;
+    uint64_t *drain_bar = sf_free_bar + Cfg::kSfSlots;         // [0] MMA issuer, [1] scale warp
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
 
@@ -120,7 +128,12 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             mbar_init(&tfull_bar[a], 1);
             mbar_init(&tempty_bar[a], Cfg::kEpiWarps);
         }
-        mbar_init(drain_bar, 1);
+        for (int j = 0; j < Cfg::kSfSlots; ++j) {
+            mbar_init(&sf_ready_bar[j], 1);
+            mbar_init(&sf_free_bar[j], 1);
+        }
+        mbar_init(&drain_bar[0], 1);
+        mbar_init(&drain_bar[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -157,15 +170,19 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     if (drop) {
                         drop = false;  // diagnostic: leave this stage empty
                     } else {
-                        mbar_arrive_expect_tx(&full_bar[stage], Cfg::kTxBytes);
+                        const bool sf_stage = (kb & 3) == 0;
+                        mbar_arrive_expect_tx(&full_bar[stage],
+                                              sf_stage ? Cfg::kTxBytes : Cfg::kABytes + Cfg::kBBytes);
                         tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
                                     kb * kBlockK, tile.a_row0);
                         tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[stage],
                                     kb * kBlockK, tile.b_row0);
-                        tma_load_2d(smem_sfa + stage * Cfg::kSfaBytes, &tm_sfa, &full_bar[stage],
-                                    tile.sfa_x, tile.sfa_y0 + (kb >> 2));
-                        tma_load_2d(smem_sfb + stage * Cfg::kSfbBytes, &tm_sfb, &full_bar[stage],
-                                    tile.n0, tile.sfb_y0 + (kb >> 2));
+                        if (sf_stage) {
+                            tma_load_2d(smem_sfa + stage * Cfg::kSfaBytes, &tm_sfa, &full_bar[stage],
+                                        tile.sfa_x, tile.sfa_y0 + (kb >> 2));
+                            tma_load_2d(smem_sfb + stage * Cfg::kSfbBytes, &tm_sfb, &full_bar[stage],
+                                        tile.n0, tile.sfb_y0 + (kb >> 2));
+                        }
                         issued |= 1u << stage;
                     }
                     if (++stage == S) { stage = 0; phase ^= 1; }
@@ -183,6 +200,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int slot = 0;
+        uint32_t slot_phase = 0;
         const uint32_t sf_col0 = NUM_ACC * BN;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             Tile tile;
@@ -193,24 +212,17 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             {
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if ((kb & 3) == 0) {
+                        // scale words of this 4-K-block group are in TMEM slot `slot`
+                        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_ready_bar[slot], slot_phase, ctl, DG_DEV_TIMEOUT)))
+                            goto mma_done;
+                    }
                     if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
                         goto mma_done;
-                    uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sfa + stage * Cfg::kSfaBytes);
-                    uint32_t *sfb_buf = reinterpret_cast<uint32_t *>(smem_sfb + stage * Cfg::kSfbBytes);
-                    sf_transpose_for_cp(sfa_buf, lane);
-#pragma unroll
-                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
-                    fence_proxy_async_smem();
-                    __syncwarp();
                     if (lane == 0) {
                         tc_fence_after_sync();
-                        const uint32_t sfa_tmem = tmem_base + sf_col0 + stage * Cfg::kSfCols;
+                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
                         const uint32_t sfb_tmem = sfa_tmem + 4;
-                        tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
-#pragma unroll
-                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
-                            tc_cp_32x128b_warpx4(sfb_tmem + 4 * c,
-                                                 make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
                         const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
                         const uint64_t a_desc =
                             make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
@@ -221,8 +233,13 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                             tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
                                         sfb_tmem, (kb | k) != 0);
                         tc_commit(&empty_bar[stage]);
+                        // last K-block of the group: the slot is free once these MMAs finish
+                        if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) tc_commit(&sf_free_bar[slot]);
                     }
                     __syncwarp();
+                    if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) {
+                        if (++slot == Cfg::kSfSlots) { slot = 0; slot_phase ^= 1; }
+                    }
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
@@ -231,10 +248,56 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
         }
     mma_done:
-        // all MMAs and copies this thread issued must finish before TMEM is freed
+        // all MMAs this thread issued must finish before TMEM is freed
         if (lane == 0) {
-            tc_commit(drain_bar);
-            mbar_wait(drain_bar, 0, ctl, DG_DEV_TIMEOUT);
+            tc_commit(&drain_bar[0]);
+            mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == Cfg::kSfWarp) {
+        // ------------------------------------------------------------ scale-factor warp
+        int stage = 0;
+        uint32_t phase = 0;
+        int slot = 0;
+        uint32_t slot_phase = 0;
+        const uint32_t sf_col0 = NUM_ACC * BN;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            Tile tile;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                if ((kb & 3) == 0) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
+                        goto sf_done;
+                    uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sfa + stage * Cfg::kSfaBytes);
+                    uint32_t *sfb_buf = reinterpret_cast<uint32_t *>(smem_sfb + stage * Cfg::kSfbBytes);
+                    sf_transpose_for_cp(sfa_buf, lane);
+#pragma unroll
+                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    // the slot's previous group must be fully consumed by the MMAs
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_free_bar[slot], slot_phase ^ 1, ctl, DG_DEV_TIMEOUT)))
+                        goto sf_done;
+                    if (lane == 0) {
+                        tc_fence_after_sync();
+                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                        tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+#pragma unroll
+                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                            tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c,
+                                                 make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                        tc_commit(&sf_ready_bar[slot]);
+                    }
+                    __syncwarp();
+                    if (++slot == Cfg::kSfSlots) { slot = 0; slot_phase ^= 1; }
+                }
+                if (++stage == S) { stage = 0; phase ^= 1; }
+            }
+        }
+    sf_done:
+        if (lane == 0) {
+            tc_commit(&drain_bar[1]);
+            mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
         }
         __syncwarp();
     } else {
