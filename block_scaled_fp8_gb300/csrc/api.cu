@@ -90,7 +90,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, cons
 
 // Block-N values compiled into the block-scaled kernel family.
 constexpr int kBsBlockN[] = {16, 32, 48, 64, 96, 128, 160, 176, 192, 224, 256};
-constexpr int kMaxBlockNWithC = 192;
+constexpr int kMaxBlockNWithC = 160;
 
 // Tile-shape choice: maximise the fraction of SM-time spent on useful tiles
 // (wave quantisation x N padding) weighted by a per-tile efficiency that grows
@@ -136,17 +136,54 @@ struct BsOperands {
     void *d;        int64_t ldd;  uint64_t d_rows;
 };
 
+// Co-resident clusters per (BLOCK_N, C, cluster size), cached per device.
+int cached_max_clusters(int bn, bool with_c, int cluster) {
+    static std::mutex mu;
+    static int cache[kMaxDevices][2][257][9];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn > 256 ||
+        cluster > 8)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int &v = cache[dev][with_c ? 1 : 0][bn][cluster];
+    if (v == 0) v = bs_max_active_clusters(bn, with_c, cluster);
+    return v;
+}
+
+// CTAs per cluster sharing the A tile.  DG_CLUSTER_SIZE (1, 2, 4 or 8)
+// overrides the default of 2 whenever there are at least two n-blocks.
+int choose_cluster(int64_t num_n_blocks) {
+    static const int env = [] {
+        const char *e = std::getenv("DG_CLUSTER_SIZE");
+        return e ? std::atoi(e) : 0;
+    }();
+    int c = (env == 1 || env == 2 || env == 4 || env == 8) ? env : 2;
+    while (c > 1 && num_n_blocks < c) c >>= 1;
+    return c;
+}
+
 dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_blocks_hint,
                               int64_t max_tiles_per_n_block, int num_sms, cudaStream_t stream) {
     const bool with_c = p.c != nullptr;
     const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
     KernelInfo info;
     if (!get_bs_kernel_info(bn, with_c, &info)) return DG_ERR_UNSUPPORTED;
+    int cluster = choose_cluster(cdiv64(p.n, bn));
+    int max_clusters = num_sms;
+    if (cluster > 1) {
+        max_clusters = cached_max_clusters(bn, with_c, cluster);
+        if (max_clusters <= 0) {
+            cluster = 1;
+            max_clusters = num_sms;
+        }
+        if (max_clusters * cluster > num_sms) max_clusters = num_sms / cluster;
+    }
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
+    // each CTA of a cluster loads (and multicasts) kBlockM / cluster rows of A
     ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                    kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                    kBlockM / cluster, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
@@ -160,6 +197,8 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     if (!ok) return DG_ERR_CUDA;
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
+    p.cluster = cluster;
+    p.num_n_groups = static_cast<int>(cdiv64(p.num_n_blocks, cluster));
     p.group_m = 8;
     p.d = static_cast<uint16_t *>(o.d);
     p.ldd = o.ldd;
@@ -167,11 +206,13 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     uint32_t dbg = g_debug_flags.load();
     if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
     p.debug_flags = dbg;
-    const int64_t tiles = max_tiles_per_n_block * p.num_n_blocks;
-    const int grid = static_cast<int>(tiles < num_sms ? (tiles < 1 ? 1 : tiles) : num_sms);
+    const int64_t cluster_tiles = max_tiles_per_n_block * p.num_n_groups;
+    const int64_t clusters = cluster_tiles < max_clusters ? (cluster_tiles < 1 ? 1 : cluster_tiles)
+                                                          : max_clusters;
+    const int grid = static_cast<int>(clusters * cluster);
     if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
-        std::fprintf(stderr, "[dg] mode=%d rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d grid=%d\n",
-                     p.mode, p.rows, p.n, k, kBlockM, bn, info.stages, info.smem_bytes, grid);
+        std::fprintf(stderr, "[dg] mode=%d rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d cluster=%d grid=%d\n",
+                     p.mode, p.rows, p.n, k, kBlockM, bn, info.stages, info.smem_bytes, cluster, grid);
     g_last_config[0] = kBlockM;
     g_last_config[1] = bn;
     g_last_config[2] = info.stages;
@@ -213,6 +254,8 @@ dg_status launch_promotion(GemmParams &p, const void *a, int64_t lda, const void
     p.num_m_blocks = static_cast<int>(m_blocks);
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(p.k, kBlockK));
+    p.cluster = 1;
+    p.num_n_groups = p.num_n_blocks;
     p.group_m = 8;
     p.d = static_cast<uint16_t *>(d);
     p.ldd = ldd;

@@ -118,11 +118,17 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const uint32_t lane = threadIdx.x & 31;
     const int psf_k = (p.num_k_blocks + 3) >> 2;
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    // 1-D clusters along x: the CTAs of a cluster are consecutive blockIdx.x.
+    const int csize = p.cluster;
+    const int rank = csize > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cluster_id = blockIdx.x / csize;
+    const int num_clusters = gridDim.x / csize;
+    const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            mbar_init(&empty_bar[s], csize);   // every CTA of the cluster frees the stage
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(&tfull_bar[a], 1);
@@ -151,6 +157,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     if (p.mode == kModeMasked) build_masked_prefix(p, prefix);
     tc_fence_before_sync();
     __syncthreads();
+    if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
     const int num_tiles = total_tiles(p, prefix);
@@ -162,9 +169,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
-            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
                 Tile tile;
-                if (!get_tile<BN>(p, prefix, t, psf_k, tile, true)) continue;
+                if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, true)) continue;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                     if (drop) {
@@ -173,8 +180,16 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         const bool sf_stage = (kb & 3) == 0;
                         mbar_arrive_expect_tx(&full_bar[stage],
                                               sf_stage ? Cfg::kTxBytes : Cfg::kABytes + Cfg::kBBytes);
-                        tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
-                                    kb * kBlockK, tile.a_row0);
+                        if (csize == 1) {
+                            tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
+                                        kb * kBlockK, tile.a_row0);
+                        } else {
+                            // this CTA's slice of the shared A tile, to every CTA of the cluster
+                            const int rows = kBlockM / csize;
+                            tma_load_2d_multicast(smem_a + stage * Cfg::kABytes + rank * rows * kBlockK,
+                                                  &tm_a, &full_bar[stage], kb * kBlockK,
+                                                  tile.a_row0 + rank * rows, cmask);
+                        }
                         tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[stage],
                                     kb * kBlockK, tile.b_row0);
                         if (sf_stage) {
@@ -203,9 +218,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         int slot = 0;
         uint32_t slot_phase = 0;
         const uint32_t sf_col0 = NUM_ACC * BN;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)))
                 goto mma_done;
             tc_fence_after_sync();
@@ -232,7 +247,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         for (int k = 0; k < kBlockK / 32; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
                                         sfb_tmem, (kb | k) != 0);
-                        tc_commit(&empty_bar[stage]);
+                        if (csize == 1) tc_commit(&empty_bar[stage]);
+                        else tc_commit_multicast(&empty_bar[stage], cmask);
                         // last K-block of the group: the slot is free once these MMAs finish
                         if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) tc_commit(&sf_free_bar[slot]);
                     }
@@ -261,9 +277,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         int slot = 0;
         uint32_t slot_phase = 0;
         const uint32_t sf_col0 = NUM_ACC * BN;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
             for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                 if ((kb & 3) == 0) {
                     if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
@@ -309,9 +325,10 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         uint32_t acc_phase = 0;
         uint32_t buf = 0;
         uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
+            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
+            const bool tile_has_columns = tile.n0 < p.n;  // false past the last n-block of a group
             const int local_row = quad * 32 + lane;
             const int row = tile.a_row0 + local_row;       // row in the 2-D view of D
             const bool row_ok = local_row < tile.valid_rows && (p.mode == kModeMasked || row < p.rows);
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
                 const int c = 2 * j + half;
-                if (c >= Cfg::kNumChunks) continue;
+                if (c >= Cfg::kNumChunks || !tile_has_columns) continue;
                 const int col0 = tile.n0 + c * Cfg::kEpiChunk;
                 if (direct) {
                     if (row_ok) {
@@ -415,6 +432,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // no CTA may leave while a peer can still multicast into it or arrive on its barriers
+    if (csize > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
@@ -431,9 +450,48 @@ cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dg_bs_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-        maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
-    return cudaGetLastError();
+    if (p.cluster <= 1) {
+        dg_bs_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
+            maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.sfa, maps.sfb,
+                              maps.d, p);
+}
+
+// Largest number of clusters of `cluster` CTAs that can be resident at once.
+template <int BN, bool WITH_C>
+int max_active_clusters_impl(int cluster) {
+    using Cfg = BsConfig<BN>;
+    if (cudaFuncSetAttribute(dg_bs_gemm_kernel<BN, WITH_C>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(cluster);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dg_bs_gemm_kernel<BN, WITH_C>, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int BN>

@@ -8,7 +8,7 @@ namespace dg {
 // BLOCK_N values compiled without C, and the subset also compiled with C
 // (the C-accumulate epilogue holds C in registers, which caps BLOCK_N).
 #define DG_BS_BLOCK_N_LIST(X) X(16) X(32) X(48) X(64) X(96) X(128) X(160) X(176) X(192) X(224) X(256)
-#define DG_BS_BLOCK_N_LIST_C(X) X(16) X(32) X(48) X(64) X(96) X(128) X(160) X(176) X(192)
+#define DG_BS_BLOCK_N_LIST_C(X) X(16) X(32) X(48) X(64) X(96) X(128) X(160)
 
 #define DG_EXTERN(BN) \
     extern template cudaError_t launch_bs_gemm_impl<BN, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
@@ -33,6 +33,32 @@ bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info) {
         DG_BS_BLOCK_N_LIST(DG_CASE)
 #undef DG_CASE
         default: return false;
+    }
+}
+
+#define DG_EXTERN(BN) \
+    extern template int max_active_clusters_impl<BN, false>(int);
+DG_BS_BLOCK_N_LIST(DG_EXTERN)
+#undef DG_EXTERN
+#define DG_EXTERN(BN) \
+    extern template int max_active_clusters_impl<BN, true>(int);
+DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
+#undef DG_EXTERN
+
+int bs_max_active_clusters(int block_n, bool with_c, int cluster) {
+    if (with_c) {
+        switch (block_n) {
+#define DG_CASE(BN) case BN: return max_active_clusters_impl<BN, true>(cluster);
+            DG_BS_BLOCK_N_LIST_C(DG_CASE)
+#undef DG_CASE
+            default: return 0;
+        }
+    }
+    switch (block_n) {
+#define DG_CASE(BN) case BN: return max_active_clusters_impl<BN, false>(cluster);
+        DG_BS_BLOCK_N_LIST(DG_CASE)
+#undef DG_CASE
+        default: return 0;
     }
 }
 

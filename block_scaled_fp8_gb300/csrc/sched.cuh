@@ -1,11 +1,15 @@
 // Persistent tile scheduler shared by the GEMM kernels.
 //
-// Every CTA walks tile ids t = blockIdx.x, blockIdx.x + gridDim.x, ... (the
-// persistent loop of PaperTrace "02 · DeepGEMM 技术解析" §4.3); a tile id maps to
-// (m-block, n-block) in groups of `group_m` m-blocks so that CTAs running at
-// the same time share A and B tiles through L2.  There is no split-K: one CTA
-// owns every K-block of its tile.  All roles of a CTA call the scheduler with
-// the same ids and reach the same decisions (including skips), so they stay in
+// Every cluster of `cluster` CTAs walks cluster-tile ids ct = cluster_id,
+// cluster_id + num_clusters, ... (the persistent loop of PaperTrace "02 ·
+// DeepGEMM 技术解析" §4.3).  A cluster tile is one 128-row m-block and a group of
+// `cluster` consecutive n-blocks; the CTA of rank r takes n-block
+// group*cluster + r, so the CTAs of a cluster share the A tile (loaded once
+// and multicast).  Cluster tiles map to (m-block, n-group) in groups of
+// `group_m` m-blocks so that clusters running at the same time share A and B
+// tiles through L2.  There is no split-K: one CTA owns every K-block of its
+// tile.  All roles of a CTA (and all CTAs of a cluster) call the scheduler with
+// the same ids and reach the same decisions, including skips, so they stay in
 // step without talking to each other.
 #pragma once
 
@@ -38,7 +42,7 @@ __device__ __forceinline__ void build_masked_prefix(const GemmParams &p, int *pr
                 if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
                 mm = mm < 0 ? 0 : p.rows;
             }
-            acc += ceil_div_i(mm, kBlockM) * p.num_n_blocks;
+            acc += ceil_div_i(mm, kBlockM) * p.num_n_groups;
         }
         prefix[p.num_groups] = acc;
     }
@@ -46,15 +50,18 @@ __device__ __forceinline__ void build_masked_prefix(const GemmParams &p, int *pr
 
 __device__ __forceinline__ int total_tiles(const GemmParams &p, const int *prefix) {
     if (p.mode == kModeMasked) return prefix[p.num_groups];
-    return p.num_m_blocks * p.num_n_blocks;
+    return p.num_m_blocks * p.num_n_groups;
 }
 
-// Fills `tile` for id t (< total).  Returns false when the tile is skipped
-// (contiguous layout: a padding block or an out-of-range expert).
+// Fills `tile` for cluster-tile id t (< total) and cluster rank `rank`.
+// Returns false when the tile is skipped (contiguous layout: a padding block
+// or an out-of-range expert); all CTAs of a cluster skip together.  The
+// n-block may lie past the last one (a partial final group): its loads read
+// zeros and nothing is stored.
 template <int BN>
-__device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix, int t, int psf_k,
-                                         Tile &tile, bool report) {
-    int mb, nb, group = 0;
+__device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix, int t, int rank,
+                                         int psf_k, Tile &tile, bool report) {
+    int mb, ng, group = 0;
     if (p.mode == kModeMasked) {
         // find the expert: largest e with prefix[e] <= t
         int lo = 0, hi = p.num_groups - 1;
@@ -68,21 +75,21 @@ __device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix,
         int mbe = ceil_div_i(mm, kBlockM);
         int local = t - prefix[group];
         mb = local % mbe;
-        nb = local / mbe;
+        ng = local / mbe;
         tile.a_row0 = group * p.rows + mb * kBlockM;
         tile.sfa_x = mb * kBlockM;
         tile.sfa_y0 = group * psf_k;
         int v = mm - mb * kBlockM;
         tile.valid_rows = v < kBlockM ? v : kBlockM;
     } else {
-        const int per_group = p.group_m * p.num_n_blocks;
+        const int per_group = p.group_m * p.num_n_groups;
         const int g = t / per_group;
         const int first_m = g * p.group_m;
         const int rem_m = p.num_m_blocks - first_m;
         const int gsize = rem_m < p.group_m ? rem_m : p.group_m;
         const int r = t - g * per_group;
         mb = first_m + r % gsize;
-        nb = r / gsize;
+        ng = r / gsize;
         tile.a_row0 = mb * kBlockM;
         tile.sfa_x = mb * kBlockM;
         tile.sfa_y0 = 0;
@@ -96,6 +103,7 @@ __device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix,
             }
         }
     }
+    const int nb = ng * p.cluster + rank;
     tile.group = group;
     tile.n0 = nb * BN;
     tile.b_row0 = group * p.n + nb * BN;
