@@ -151,13 +151,13 @@ int cached_max_clusters(int bn, bool with_c, int cluster) {
 }
 
 // CTAs per cluster sharing the A tile.  DG_CLUSTER_SIZE (1, 2, 4 or 8)
-// overrides the default of 2 whenever there are at least two n-blocks.
+// overrides the default of 1 (A is loaded by every CTA).
 int choose_cluster(int64_t num_n_blocks) {
     static const int env = [] {
         const char *e = std::getenv("DG_CLUSTER_SIZE");
         return e ? std::atoi(e) : 0;
     }();
-    int c = (env == 1 || env == 2 || env == 4 || env == 8) ? env : 2;
+    int c = (env == 1 || env == 2 || env == 4 || env == 8) ? env : 1;
     while (c > 1 && num_n_blocks < c) c >>= 1;
     return c;
 }

@@ -42,23 +42,24 @@ struct BsConfig {
     static constexpr int kThreads = 352;
     static constexpr int kEpiWarps = 8;
     static constexpr int kSfWarp = 10;
-    static constexpr int kSfSlots = 4;                          // TMEM scale slots (groups in flight)
     static constexpr int kSfbChunks = (BN + 127) / 128;        // 128-word tcgen05.cp chunks
-    static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per stage
+    static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per scale slot
+    static constexpr int kSfSlots = 4;                          // scale groups in flight (smem + TMEM)
     static constexpr int kABytes = kBlockM * kBlockK;           // 16 KB
     static constexpr int kBBytes = BN * kBlockK;
-    static constexpr int kSfaBytes = 512;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfaBytes = 512;                       // 128 words
     static constexpr int kSfbBytes = 512 * kSfbChunks;
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-    static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + BN * 4;
+    static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
+    static constexpr int kSfTxBytes = kSfaBytes + BN * 4;
     static constexpr int kEpiChunk = 16;                        // columns per epilogue chunk
     static constexpr int kNumChunks = BN / kEpiChunk;
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
     static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;  // 16 KB
     static constexpr int kMaskedPrefixBytes = (kMaxGroupsMasked + 1) * 4;
     static constexpr int kSmemLimit = 232448;                   // 227 KB per CTA
-    static constexpr int kFixedBytes = 1024 /*align*/ + kStagingBytes + 512 /*barriers*/ +
-                                       kMaskedPrefixBytes;
+    static constexpr int kFixedBytes = 1024 /*align*/ + kStagingBytes + kSfSlots * kSfSlotBytes +
+                                       512 /*barriers*/ + kMaskedPrefixBytes;
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStages = kStagesBySmem > 8 ? 8 : kStagesBySmem;
     static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
@@ -67,13 +68,15 @@ struct BsConfig {
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
 };
 
 // Reorder 128 scale words (row i at word i, as TMA lands them from the
 // MN-major tensor) into the 32x128b tcgen05.cp source layout: 16-byte row r
 // holds the words of MN rows r, r+32, r+64, r+96.  After the copy, TMEM lane
-// r (in each 32-lane sub-partition) column j holds the word of row 32*j + r.
-// One warp; in place.  The XOR spreads the accesses over the banks.
+// r (in each 32-lane sub-partition) column j holds the word of row 32*j + r,
+// which is where the block-scaled MMA reads the scale of row (or column)
+// 32*j + r.  One warp; in place.  The XOR spreads the accesses over the banks.
 __device__ __forceinline__ void sf_transpose_for_cp(uint32_t *buf, uint32_t lane) {
     uint32_t v[4];
 #pragma unroll
@@ -82,6 +85,33 @@ __device__ __forceinline__ void sf_transpose_for_cp(uint32_t *buf, uint32_t lane
 #pragma unroll
     for (uint32_t i = 0; i < 4; ++i) buf[lane * 4 + ((i ^ (lane >> 3)) & 3)] = v[i];
 }
+
+// Walks the (tile, 4-K-block group) sequence of one cluster in scheduler order;
+// the producer runs it ahead of the A/B stream to prefetch scale words.
+template <int BN>
+struct GroupCursor {
+    const GemmParams *p;
+    const int *prefix;
+    int t, j, num_tiles, num_clusters, rank, psf_k, groups_per_tile;
+    bool valid;
+    Tile tile;
+    __device__ __forceinline__ void start(const GemmParams &params, const int *pre, int cluster_id,
+                                          int nclusters, int r, int ntiles, int psf) {
+        p = &params; prefix = pre; num_clusters = nclusters; rank = r; num_tiles = ntiles;
+        psf_k = psf; groups_per_tile = (params.num_k_blocks + 3) >> 2;
+        t = cluster_id - nclusters;
+        next_tile();
+    }
+    __device__ __forceinline__ void next_tile() {
+        j = 0;
+        valid = false;
+        for (t += num_clusters; t < num_tiles; t += num_clusters)
+            if (get_tile<BN>(*p, prefix, t, rank, psf_k, tile, false)) { valid = true; return; }
+    }
+    __device__ __forceinline__ void next() {
+        if (++j == groups_per_tile) next_tile();
+    }
+};
 
 template <int BN, bool WITH_C>
 __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
@@ -93,23 +123,24 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     using Cfg = BsConfig<BN>;
     constexpr int S = Cfg::kStages;
     constexpr int NUM_ACC = Cfg::kNumAcc;
+    constexpr int NSF = Cfg::kSfSlots;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *smem_a = smem;
     uint8_t *smem_b = smem_a + S * Cfg::kABytes;
-    uint8_t *smem_sfa = smem_b + S * Cfg::kBBytes;
-    uint8_t *smem_sfb = smem_sfa + S * Cfg::kSfaBytes;
-    uint8_t *smem_stage_out = smem_sfb + S * Cfg::kSfbBytes;  // 1024-aligned (all sizes are)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_stage_out + Cfg::kStagingBytes);
-    uint64_t *full_bar = bars;
-    uint64_t *empty_bar = bars + S;
-    uint64_t *tfull_bar = bars + 2 * S;
-    uint64_t *tempty_bar = tfull_bar + NUM_ACC;
-    uint64_t *sf_ready_bar = tempty_bar + NUM_ACC;
-    uint64_t *sf_free_bar = sf_ready_bar + Cfg::kSfSlots;
-    uint64_t *drain_bar = sf_free_bar + Cfg::kSfSlots;         // [0] MMA issuer, [1] scale warp
+    uint8_t *smem_stage_out = smem_b + S * Cfg::kBBytes;       // 1024-aligned (all sizes are)
+    uint8_t *smem_sf = smem_stage_out + Cfg::kStagingBytes;     // NSF slots: [SFA 512 B][SFB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_sf + NSF * Cfg::kSfSlotBytes);
+    uint64_t *full_bar = bars;                        // [S]   A/B stage landed
+    uint64_t *empty_bar = bars + S;                   // [S]   A/B stage consumed by the MMAs
+    uint64_t *tfull_bar = bars + 2 * S;               // [NUM_ACC] accumulator complete
+    uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] accumulator drained
+    uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] scale words landed in smem
+    uint64_t *sf_ready_bar = sf_full_bar + NSF;       // [NSF] scale words copied to TMEM
+    uint64_t *sf_free_bar = sf_ready_bar + NSF;       // [NSF] MMAs done with the scale slot
+    uint64_t *drain_bar = sf_free_bar + NSF;          // [2]  MMA issuer, scale warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
@@ -134,7 +165,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             mbar_init(&tfull_bar[a], 1);
             mbar_init(&tempty_bar[a], Cfg::kEpiWarps);
         }
-        for (int j = 0; j < Cfg::kSfSlots; ++j) {
+        for (int j = 0; j < NSF; ++j) {
+            mbar_init(&sf_full_bar[j], 1);
             mbar_init(&sf_ready_bar[j], 1);
             mbar_init(&sf_free_bar[j], 1);
         }
@@ -160,7 +192,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    const uint32_t sf_col0 = NUM_ACC * BN;
     const int num_tiles = total_tiles(p, prefix);
+    const int groups_per_tile = psf_k;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -169,17 +203,38 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
+            GroupCursor<BN> sfc;
+            sfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+            int gs = 0;          // scale groups issued
+            int ga = 0;          // A/B groups started
+            uint32_t sf_issued = 0;
             for (int t = cluster_id; t < num_tiles; t += num_clusters) {
                 Tile tile;
                 if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, true)) continue;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if ((kb & 3) == 0) {
+                        // keep the scale words one group ahead of the A/B stream
+                        while (sfc.valid && gs <= ga + 1) {
+                            const int slot = gs % NSF;
+                            if (!mbar_wait(&sf_free_bar[slot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                                goto prod_done;
+                            uint8_t *sbuf = smem_sf + slot * Cfg::kSfSlotBytes;
+                            mbar_arrive_expect_tx(&sf_full_bar[slot], Cfg::kSfTxBytes);
+                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[slot], sfc.tile.sfa_x,
+                                        sfc.tile.sfa_y0 + sfc.j);
+                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[slot],
+                                        sfc.tile.n0, sfc.tile.sfb_y0 + sfc.j);
+                            sf_issued |= 1u << slot;
+                            ++gs;
+                            sfc.next();
+                        }
+                        ++ga;
+                    }
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                     if (drop) {
                         drop = false;  // diagnostic: leave this stage empty
                     } else {
-                        const bool sf_stage = (kb & 3) == 0;
-                        mbar_arrive_expect_tx(&full_bar[stage],
-                                              sf_stage ? Cfg::kTxBytes : Cfg::kABytes + Cfg::kBBytes);
+                        mbar_arrive_expect_tx(&full_bar[stage], Cfg::kStageBytes);
                         if (csize == 1) {
                             tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
                                         kb * kBlockK, tile.a_row0);
@@ -192,122 +247,102 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         }
                         tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[stage],
                                     kb * kBlockK, tile.b_row0);
-                        if (sf_stage) {
-                            tma_load_2d(smem_sfa + stage * Cfg::kSfaBytes, &tm_sfa, &full_bar[stage],
-                                        tile.sfa_x, tile.sfa_y0 + (kb >> 2));
-                            tma_load_2d(smem_sfb + stage * Cfg::kSfbBytes, &tm_sfb, &full_bar[stage],
-                                        tile.n0, tile.sfb_y0 + (kb >> 2));
-                        }
                         issued |= 1u << stage;
                     }
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
         prod_done:
-            // never leave the CTA with loads in flight: wait for the last fill of every stage
+            // never leave the CTA with loads in flight: wait for the last fill of every buffer
             for (int s = 0; s < S; ++s)
                 if (issued & (1u << s))
                     mbar_wait(&full_bar[s], s < stage ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+            for (int j = 0; j < NSF; ++j)
+                if (sf_issued & (1u << j)) {
+                    // last use of slot j was group g = the largest g < gs with g % NSF == j
+                    const int g = gs - 1 - ((gs - 1 - j) % NSF + NSF) % NSF;
+                    mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
+                }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        int slot = 0;
-        uint32_t slot_phase = 0;
-        const uint32_t sf_col0 = NUM_ACC * BN;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-            Tile tile;
-            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)))
-                goto mma_done;
-            tc_fence_after_sync();
-            {
+        // ------------------------------------------------------------ MMA issuer (one lane)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int g = 0;  // scale groups consumed
+            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+                Tile tile;
+                if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
+                if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    const int slot = g % NSF;
                     if ((kb & 3) == 0) {
                         // scale words of this 4-K-block group are in TMEM slot `slot`
-                        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_ready_bar[slot], slot_phase, ctl, DG_DEV_TIMEOUT)))
+                        if (!mbar_wait(&sf_ready_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
                             goto mma_done;
                     }
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
-                        goto mma_done;
-                    if (lane == 0) {
-                        tc_fence_after_sync();
-                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
-                        const uint32_t sfb_tmem = sfa_tmem + 4;
-                        const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
-                        const uint64_t a_desc =
-                            make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
-                        const uint64_t b_desc =
-                            make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
+                    if (!mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                    tc_fence_after_sync();
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                    const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
+                    const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
+                    const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
 #pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k)
-                            tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
-                                        sfb_tmem, (kb | k) != 0);
-                        if (csize == 1) tc_commit(&empty_bar[stage]);
-                        else tc_commit_multicast(&empty_bar[stage], cmask);
-                        // last K-block of the group: the slot is free once these MMAs finish
-                        if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) tc_commit(&sf_free_bar[slot]);
-                    }
-                    __syncwarp();
+                    for (int k = 0; k < kBlockK / 32; ++k)
+                        tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem, sfa_tmem + 4,
+                                    (kb | k) != 0);
+                    if (csize == 1) tc_commit(&empty_bar[stage]);
+                    else tc_commit_multicast(&empty_bar[stage], cmask);
                     if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) {
-                        if (++slot == Cfg::kSfSlots) { slot = 0; slot_phase ^= 1; }
+                        // last K-block of the group: the slot is free once these MMAs finish
+                        tc_commit(&sf_free_bar[slot]);
+                        ++g;
                     }
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
+                tc_commit(&tfull_bar[acc]);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
             }
-            if (lane == 0) tc_commit(&tfull_bar[acc]);
-            __syncwarp();
-            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
-        }
-    mma_done:
-        // all MMAs this thread issued must finish before TMEM is freed
-        if (lane == 0) {
+        mma_done:
+            // all MMAs this thread issued must finish before TMEM is freed
             tc_commit(&drain_bar[0]);
             mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
         }
         __syncwarp();
     } else if (warp == Cfg::kSfWarp) {
         // ------------------------------------------------------------ scale-factor warp
-        int stage = 0;
-        uint32_t phase = 0;
-        int slot = 0;
-        uint32_t slot_phase = 0;
-        const uint32_t sf_col0 = NUM_ACC * BN;
+        int g = 0;
         for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
             if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                if ((kb & 3) == 0) {
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
-                        goto sf_done;
-                    uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sfa + stage * Cfg::kSfaBytes);
-                    uint32_t *sfb_buf = reinterpret_cast<uint32_t *>(smem_sfb + stage * Cfg::kSfbBytes);
-                    sf_transpose_for_cp(sfa_buf, lane);
+            for (int j = 0; j < groups_per_tile; ++j, ++g) {
+                const int slot = g % NSF;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
+                    goto sf_done;
+                uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
+                uint32_t *sfb_buf = sfa_buf + 128;
+                sf_transpose_for_cp(sfa_buf, lane);
 #pragma unroll
-                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    // the slot's previous group must be fully consumed by the MMAs
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_free_bar[slot], slot_phase ^ 1, ctl, DG_DEV_TIMEOUT)))
-                        goto sf_done;
-                    if (lane == 0) {
-                        tc_fence_after_sync();
-                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
-                        tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+                for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // the slot's previous group was released (sf_free) before its words were
+                    // reloaded, so its MMAs have completed
+                    tc_fence_after_sync();
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                    tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
 #pragma unroll
-                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
-                            tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c,
-                                                 make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
-                        tc_commit(&sf_ready_bar[slot]);
-                    }
-                    __syncwarp();
-                    if (++slot == Cfg::kSfSlots) { slot = 0; slot_phase ^= 1; }
+                    for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                        tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c,
+                                             make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                    tc_commit(&sf_ready_bar[slot]);
                 }
-                if (++stage == S) { stage = 0; phase ^= 1; }
+                __syncwarp();
             }
         }
     sf_done:
