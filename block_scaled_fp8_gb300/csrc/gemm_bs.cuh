@@ -61,7 +61,7 @@ struct BsConfig {
     static constexpr int kFixedBytes = 1024 /*align*/ + kStagingBytes + kSfSlots * kSfSlotBytes +
                                        512 /*barriers*/ + kMaskedPrefixBytes;
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
-    static constexpr int kStages = kStagesBySmem > 8 ? 8 : kStagesBySmem;
+    static constexpr int kStages = kStagesBySmem > 12 ? 12 : kStagesBySmem;
     static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
     static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
@@ -110,6 +110,33 @@ struct GroupCursor {
     }
     __device__ __forceinline__ void next() {
         if (++j == groups_per_tile) next_tile();
+    }
+};
+
+// Walks the (tile, K-block) sequence of one CTA in scheduler order; the
+// producer runs it ahead of its loads to prefetch A/B tiles into L2.
+template <int BN>
+struct KbCursor {
+    const GemmParams *p;
+    const int *prefix;
+    int t, kb, num_tiles, num_clusters, rank, psf_k;
+    bool valid;
+    Tile tile;
+    __device__ __forceinline__ void start(const GemmParams &params, const int *pre, int cluster_id,
+                                          int nclusters, int r, int ntiles, int psf) {
+        p = &params; prefix = pre; num_clusters = nclusters; rank = r; num_tiles = ntiles;
+        psf_k = psf;
+        t = cluster_id - nclusters;
+        next_tile();
+    }
+    __device__ __forceinline__ void next_tile() {
+        kb = 0;
+        valid = false;
+        for (t += num_clusters; t < num_tiles; t += num_clusters)
+            if (get_tile<BN>(*p, prefix, t, rank, psf_k, tile, false)) { valid = true; return; }
+    }
+    __device__ __forceinline__ void next() {
+        if (++kb == p->num_k_blocks) next_tile();
     }
 };
 
@@ -208,6 +235,20 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             int gs = 0;          // scale groups issued
             int ga = 0;          // A/B groups started
             uint32_t sf_issued = 0;
+            // L2 prefetch cursor, p.prefetch_kb K-blocks ahead of the loads
+            KbCursor<BN> pfc;
+            pfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+            auto prefetch_one = [&]() {
+                if (!pfc.valid) return;
+                if (p.prefetch_mask & 1)
+                    tma_prefetch_l2_2d(&tm_a, pfc.kb * kBlockK,
+                                       pfc.tile.a_row0 + rank * (kBlockM / csize));
+                if (p.prefetch_mask & 2)
+                    tma_prefetch_l2_2d(&tm_b, pfc.kb * kBlockK, pfc.tile.b_row0);
+                pfc.next();
+            };
+            if (p.prefetch_mask != 0)
+                for (int i = 0; i < p.prefetch_kb; ++i) prefetch_one();
             for (int t = cluster_id; t < num_tiles; t += num_clusters) {
                 Tile tile;
                 if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, true)) continue;
@@ -249,6 +290,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                                     kb * kBlockK, tile.b_row0);
                         issued |= 1u << stage;
                     }
+                    if (p.prefetch_mask != 0 && p.prefetch_kb > 0) prefetch_one();
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
