@@ -61,11 +61,18 @@ struct BsConfig {
     static constexpr int kFixedBytes = 1024 /*align*/ + kStagingBytes + kSfSlots * kSfSlotBytes +
                                        512 /*barriers*/ + kMaskedPrefixBytes;
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
-    static constexpr int kStages = kStagesBySmem > 12 ? 12 : kStagesBySmem;
+    static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
+    // K-blocks per ring slot: the stages of a slot share one full and one empty
+    // barrier, so the MMA issuer waits and commits once per kGroupKb K-blocks
+    // (each wait or commit costs the issuing thread 70-200 cycles).  Divides 4,
+    // so slots never straddle a 4-K-block scale group.
+    static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : 2;
+    static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
+    static constexpr int kRing = kStages / kGroupKb;             // barrier slots
     static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
     static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
-    static_assert(kStages >= 3, "pipeline too shallow");
+    static_assert(kRing >= 2, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
@@ -160,9 +167,11 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     uint8_t *smem_stage_out = smem_b + S * Cfg::kBBytes;       // 1024-aligned (all sizes are)
     uint8_t *smem_sf = smem_stage_out + Cfg::kStagingBytes;     // NSF slots: [SFA 512 B][SFB]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_sf + NSF * Cfg::kSfSlotBytes);
-    uint64_t *full_bar = bars;                        // [S]   A/B stage landed
-    uint64_t *empty_bar = bars + S;                   // [S]   A/B stage consumed by the MMAs
-    uint64_t *tfull_bar = bars + 2 * S;               // [NUM_ACC] accumulator complete
+    constexpr int R = Cfg::kRing;
+    constexpr int G = Cfg::kGroupKb;
+    uint64_t *full_bar = bars;                        // [R]   a slot's G stages landed
+    uint64_t *empty_bar = bars + R;                   // [R]   a slot's stages consumed by the MMAs
+    uint64_t *tfull_bar = bars + 2 * R;               // [NUM_ACC] accumulator complete
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] accumulator drained
     uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] scale words landed in smem
     uint64_t *sf_ready_bar = sf_full_bar + NSF;       // [NSF] scale words copied to TMEM
@@ -184,9 +193,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < R; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], csize);   // every CTA of the cluster frees the stage
+            mbar_init(&empty_bar[s], csize);   // every CTA of the cluster frees the slot
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(&tfull_bar[a], 1);
@@ -226,7 +235,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int stage = 0;
+            int slot = 0;
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
@@ -252,53 +261,58 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             for (int t = cluster_id; t < num_tiles; t += num_clusters) {
                 Tile tile;
                 if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, true)) continue;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if ((kb & 3) == 0) {
+                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                    if ((kb0 & 3) == 0) {
                         // keep the scale words one group ahead of the A/B stream
                         while (sfc.valid && gs <= ga + 1) {
-                            const int slot = gs % NSF;
-                            if (!mbar_wait(&sf_free_bar[slot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                            const int sslot = gs % NSF;
+                            if (!mbar_wait(&sf_free_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
                                 goto prod_done;
-                            uint8_t *sbuf = smem_sf + slot * Cfg::kSfSlotBytes;
-                            mbar_arrive_expect_tx(&sf_full_bar[slot], Cfg::kSfTxBytes);
-                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[slot], sfc.tile.sfa_x,
+                            uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
+                            mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
+                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], sfc.tile.sfa_x,
                                         sfc.tile.sfa_y0 + sfc.j);
-                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[slot],
+                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot],
                                         sfc.tile.n0, sfc.tile.sfb_y0 + sfc.j);
-                            sf_issued |= 1u << slot;
+                            sf_issued |= 1u << sslot;
                             ++gs;
                             sfc.next();
                         }
                         ++ga;
                     }
-                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
+                    if (!mbar_wait(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                     if (drop) {
-                        drop = false;  // diagnostic: leave this stage empty
+                        drop = false;  // diagnostic: leave this slot empty
                     } else {
-                        mbar_arrive_expect_tx(&full_bar[stage], Cfg::kStageBytes);
-                        if (csize == 1) {
-                            tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[stage],
-                                        kb * kBlockK, tile.a_row0);
-                        } else {
-                            // this CTA's slice of the shared A tile, to every CTA of the cluster
-                            const int rows = kBlockM / csize;
-                            tma_load_2d_multicast(smem_a + stage * Cfg::kABytes + rank * rows * kBlockK,
-                                                  &tm_a, &full_bar[stage], kb * kBlockK,
-                                                  tile.a_row0 + rank * rows, cmask);
+                        mbar_arrive_expect_tx(&full_bar[slot], nk * Cfg::kStageBytes);
+                        for (int j = 0; j < nk; ++j) {
+                            const int kb = kb0 + j;
+                            const int stage = slot * G + j;
+                            if (csize == 1) {
+                                tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[slot],
+                                            kb * kBlockK, tile.a_row0);
+                            } else {
+                                // this CTA's slice of the shared A tile, to every CTA of the cluster
+                                const int rows = kBlockM / csize;
+                                tma_load_2d_multicast(smem_a + stage * Cfg::kABytes + rank * rows * kBlockK,
+                                                      &tm_a, &full_bar[slot], kb * kBlockK,
+                                                      tile.a_row0 + rank * rows, cmask);
+                            }
+                            tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[slot],
+                                        kb * kBlockK, tile.b_row0);
+                            if (p.prefetch_mask != 0 && p.prefetch_kb > 0) prefetch_one();
                         }
-                        tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[stage],
-                                    kb * kBlockK, tile.b_row0);
-                        issued |= 1u << stage;
+                        issued |= 1u << slot;
                     }
-                    if (p.prefetch_mask != 0 && p.prefetch_kb > 0) prefetch_one();
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    if (++slot == R) { slot = 0; phase ^= 1; }
                 }
             }
         prod_done:
             // never leave the CTA with loads in flight: wait for the last fill of every buffer
-            for (int s = 0; s < S; ++s)
+            for (int s = 0; s < R; ++s)
                 if (issued & (1u << s))
-                    mbar_wait(&full_bar[s], s < stage ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+                    mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
             for (int j = 0; j < NSF; ++j)
                 if (sf_issued & (1u << j)) {
                     // last use of slot j was group g = the largest g < gs with g % NSF == j
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (one lane)
         if (lane == 0) {
-            int stage = 0;
+            int slot = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
@@ -320,31 +334,37 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                 if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    const int slot = g % NSF;
-                    if ((kb & 3) == 0) {
-                        // scale words of this 4-K-block group are in TMEM slot `slot`
-                        if (!mbar_wait(&sf_ready_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
+                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                    const int sslot = g % NSF;
+                    if ((kb0 & 3) == 0) {
+                        // scale words of this 4-K-block group are in TMEM slot `sslot`
+                        if (!mbar_wait(&sf_ready_bar[sslot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
                             goto mma_done;
                     }
-                    if (!mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                    if (!mbar_wait(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                     tc_fence_after_sync();
-                    const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
-                    const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
-                    const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
-                    const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + sslot * Cfg::kSfCols;
+                    for (int j = 0; j < nk; ++j) {
+                        const int kb = kb0 + j;
+                        const int stage = slot * G + j;
+                        const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
+                        const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
+                        const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < kBlockK / 32; ++k)
-                        tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem, sfa_tmem + 4,
-                                    (kb | k) != 0);
-                    if (csize == 1) tc_commit(&empty_bar[stage]);
-                    else tc_commit_multicast(&empty_bar[stage], cmask);
-                    if ((kb & 3) == 3 || kb == p.num_k_blocks - 1) {
-                        // last K-block of the group: the slot is free once these MMAs finish
-                        tc_commit(&sf_free_bar[slot]);
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
+                                        sfa_tmem + 4, (kb | k) != 0);
+                    }
+                    if (csize == 1) tc_commit(&empty_bar[slot]);
+                    else tc_commit_multicast(&empty_bar[slot], cmask);
+                    const int kb_last = kb0 + nk - 1;
+                    if ((kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1) {
+                        // last K-block of the scale group: its slot is free once these MMAs finish
+                        tc_commit(&sf_free_bar[sslot]);
                         ++g;
                     }
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    if (++slot == R) { slot = 0; phase ^= 1; }
                 }
                 tc_commit(&tfull_bar[acc]);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
