@@ -179,8 +179,95 @@ void choose_prefetch(GemmParams &p, int64_t m_blocks, int stages) {
     p.prefetch_mask = env_mask >= 0 ? (env_mask & 3) : 0;
 }
 
+// Dense problems with more than one 128-row block run on CTA pairs (256-row
+// tiles, cta_group::2) unless DG_DEBUG_SINGLE_CTA is set.
+bool use_pair_kernel(const GemmParams &p) {
+    return !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA) && p.mode == kModeDense && p.rows > kBlockM;
+}
+
+int cached_max_pairs(int bn, bool with_c) {
+    static std::mutex mu;
+    static int cache[kMaxDevices][2][257];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn > 256) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int &v = cache[dev][with_c ? 1 : 0][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c);
+    return v;
+}
+
+dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStream_t stream) {
+    const bool with_c = p.c != nullptr;
+    const int64_t m_pairs = cdiv64(p.rows, 2 * kBlockM);
+    // same score as choose_block_n, over the co-resident pairs
+    int bn = 0;
+    double best = -1.0;
+    for (int cand : {128, 192, 224, 256}) {
+        KernelInfo ki;
+        if (!get_bs2_kernel_info(cand, with_c, &ki)) continue;
+        int pairs = cached_max_pairs(cand, with_c);
+        if (pairs <= 0) continue;
+        if (pairs * 2 > num_sms) pairs = num_sms / 2;
+        const int64_t nb = cdiv64(p.n, cand);
+        const int64_t tiles = m_pairs * nb;
+        const int64_t waves = cdiv64(tiles, pairs);
+        const double score = static_cast<double>(tiles) / static_cast<double>(waves * pairs) *
+                             static_cast<double>(p.n) / static_cast<double>(nb * cand) *
+                             (cand / (cand + 64.0));
+        if (score > best + 1e-9) { best = score; bn = cand; }
+    }
+    if (bn == 0) return DG_ERR_UNSUPPORTED;
+    KernelInfo info;
+    get_bs2_kernel_info(bn, with_c, &info);
+    int pairs = cached_max_pairs(bn, with_c);
+    if (pairs * 2 > num_sms) pairs = num_sms / 2;
+    TensorMaps maps;
+    const int k = p.k;
+    bool ok = true;
+    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
+                    kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
+                    bn / 2, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
+                    align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    ok &= encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfb, o.sfb_mn, o.sfb_slices,
+                    align4(o.sfb_mn) * 4, bn, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
+                    32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (!ok) return DG_ERR_CUDA;
+    p.num_m_blocks = static_cast<int>(m_pairs);     // the pair kernel counts 256-row blocks
+    p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
+    p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
+    p.cluster = 2;
+    p.num_n_groups = p.num_n_blocks;
+    p.group_m = 8;
+    p.d = static_cast<uint16_t *>(o.d);
+    p.ldd = o.ldd;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
+    uint32_t dbg = g_debug_flags.load();
+    if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
+    p.debug_flags = dbg;
+    const int64_t tiles = m_pairs * p.num_n_blocks;
+    const int64_t used = tiles < pairs ? tiles : pairs;
+    const int grid = static_cast<int>(2 * used);
+    if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
+        std::fprintf(stderr, "[dg] pair rows=%d n=%d k=%d -> BLOCK_M=256 BLOCK_N=%d stages=%d smem=%d grid=%d\n",
+                     p.rows, p.n, k, bn, info.stages, info.smem_bytes, grid);
+    g_last_config[0] = 2 * kBlockM;
+    g_last_config[1] = bn;
+    g_last_config[2] = info.stages;
+    g_last_config[3] = grid;
+    g_last_config[4] = 2;
+    g_last_config[5] = 1;
+    cudaError_t e = launch_bs2_gemm(bn, maps, p, grid, stream);
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
 dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_blocks_hint,
                               int64_t max_tiles_per_n_block, int num_sms, cudaStream_t stream) {
+    if (use_pair_kernel(p)) return launch_pair(p, o, num_sms, stream);
     const bool with_c = p.c != nullptr;
     const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
     KernelInfo info;

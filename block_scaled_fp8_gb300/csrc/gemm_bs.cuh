@@ -64,9 +64,10 @@ struct BsConfig {
     static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
     // K-blocks per ring slot: the stages of a slot share one full and one empty
     // barrier, so the MMA issuer waits and commits once per kGroupKb K-blocks
-    // (each wait or commit costs the issuing thread 70-200 cycles).  Divides 4,
-    // so slots never straddle a 4-K-block scale group.
-    static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : 2;
+    // (each wait or commit costs the issuing thread 70-200 cycles).  The largest
+    // of 4, 2, 1 that still leaves 4 slots in the ring (the load latency needs
+    // that depth); it divides 4, so slots never straddle a scale group.
+    static constexpr int kGroupKb = kStagesCap >= 16 ? 4 : (kStagesCap >= 8 ? 2 : 1);
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;             // barrier slots
     static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         drop = false;  // diagnostic: leave this slot empty
                     } else {
                         mbar_arrive_expect_tx(&full_bar[slot], nk * Cfg::kStageBytes);
-                        for (int j = 0; j < nk; ++j) {
+                        auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
                             const int stage = slot * G + j;
                             if (csize == 1) {
@@ -302,6 +303,12 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                             tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[slot],
                                         kb * kBlockK, tile.b_row0);
                             if (p.prefetch_mask != 0 && p.prefetch_kb > 0) prefetch_one();
+                        };
+                        if (nk == G) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) load_kb(j);
+                        } else {
+                            for (int j = 0; j < nk; ++j) load_kb(j);
                         }
                         issued |= 1u << slot;
                     }
@@ -328,6 +335,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             int g = 0;  // scale groups consumed
+            const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
+            const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
+            constexpr uint32_t idesc_base = make_idesc_mxf8(kBlockM, BN, 0, 0);
             for (int t = cluster_id; t < num_tiles; t += num_clusters) {
                 Tile tile;
                 if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
@@ -345,16 +355,26 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     if (!mbar_wait(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                     tc_fence_after_sync();
                     const uint32_t sfa_tmem = tmem_base + sf_col0 + sslot * Cfg::kSfCols;
-                    for (int j = 0; j < nk; ++j) {
+                    // descriptors of this slot's first stage; a stage further is a fixed
+                    // address step (>> 4), and the scale byte of K-block kb is kb % 4
+                    const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
+                    const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
+                    auto mma_kb = [&](int j) {
                         const int kb = kb0 + j;
-                        const int stage = slot * G + j;
-                        const uint32_t idesc = make_idesc_mxf8(kBlockM, BN, kb & 3, kb & 3);
-                        const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
-                        const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
+                        const uint32_t sf = static_cast<uint32_t>(kb & 3);
+                        const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
+                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
+                        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kBBytes >> 4));
 #pragma unroll
                         for (int k = 0; k < kBlockK / 32; ++k)
                             tc_mma_mxf8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
                                         sfa_tmem + 4, (kb | k) != 0);
+                    };
+                    if (nk == G) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) mma_kb(j);
+                    } else {
+                        for (int j = 0; j < nk; ++j) mma_kb(j);
                     }
                     if (csize == 1) tc_commit(&empty_bar[slot]);
                     else tc_commit_multicast(&empty_bar[slot], cmask);

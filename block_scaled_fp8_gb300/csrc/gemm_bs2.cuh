@@ -1,0 +1,498 @@
+// Block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2), dense layout.
+//
+// Same method as the single-CTA kernel (gemm_bs.cuh; "02 · DeepGEMM 技术解析"
+// §2-§4, "DeepSeek V4 源码剖析 第13章" §13.3): per output tile the block-scaled
+// MMA accumulates sa*sb*(A_kb @ B_kb^T) over all K-blocks in FP32 TMEM.  Here a
+// cluster of two CTAs on two SMs computes one 256 x BN tile with M=256 MMAs
+// issued by the leader CTA:
+//   - each CTA loads its own 128 rows of A and half of the tile's B columns
+//     (BN/2 rows of B) per 128-K stage, so a stage holds 16 KB + 64*BN bytes
+//     instead of 16 KB + 128*BN and the ring is half again as deep; the pair's
+//     loads complete on the leader's barrier;
+//   - the MMA reads A rows 0-127 and B rows 0..BN/2-1 from the leader's shared
+//     memory, A rows 128-255 and B rows BN/2..BN-1 from the peer's, and writes
+//     each CTA's 128 rows of D into that CTA's TMEM;
+//   - each CTA's TMEM holds the A scales of its own rows and the B scales of all
+//     BN columns (lane n%32, column n/32, as in the single-CTA layout);
+//     tcgen05.cp.cta_group::2 copies each CTA's reordered words into its own TMEM;
+//   - commits reach both CTAs (multicast), and the peer's epilogue and scale
+//     warps signal the leader's barriers through their cluster addresses.
+// Ring slots group kGroupKb K-blocks under one barrier pair to keep the single
+// issuing thread's per-K-block work below the tensor time.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "dg_internal.h"
+#include "gemm_bs.cuh"
+#include "ptx.cuh"
+
+namespace dg {
+
+template <int BN>
+struct Bs2Config {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN/2 rows of B per CTA, N <= 256");
+    static constexpr int kThreads = 352;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kSfWarp = 10;
+    static constexpr int kSfbChunks = (BN + 127) / 128;
+    static constexpr int kSfCols = 4 + 4 * kSfbChunks;
+    static constexpr int kSfSlots = 4;
+    static constexpr int kABytes = kBlockM * kBlockK;           // this CTA's 128 rows of A
+    static constexpr int kBBytes = (BN / 2) * kBlockK;          // this CTA's half of B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfbBytes = 512 * kSfbChunks;
+    static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
+    static constexpr int kSfTxBytes = kSfaBytes + BN * 4;
+    static constexpr int kEpiChunk = 16;
+    static constexpr int kNumChunks = BN / kEpiChunk;
+    static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;
+    static constexpr int kSmemLimit = 232448;
+    static constexpr int kFixedBytes = 1024 + kStagingBytes + kSfSlots * kSfSlotBytes + 512;
+    static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
+    static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
+    static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
+    static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
+    static constexpr int kRing = kStages / kGroupKb;
+    static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = 512;
+    static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kRing >= 2, "pipeline too shallow");
+    static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
+};
+
+struct PairTile {
+    int a_row0;   // this CTA's first row of A and D
+    int n0;       // first output column of the tile
+    int b_row0;   // this CTA's first row of B (its half of the tile's columns)
+};
+
+// Pair tile t -> (m-pair, n-block), grouped along M for L2 reuse.
+template <int BN>
+__device__ __forceinline__ void get_pair_tile(const GemmParams &p, int t, int rank, PairTile &tile) {
+    const int per_group = p.group_m * p.num_n_blocks;
+    const int g = t / per_group;
+    const int first = g * p.group_m;
+    const int rem = p.num_m_blocks - first;
+    const int gsize = rem < p.group_m ? rem : p.group_m;
+    const int r = t - g * per_group;
+    const int mp = first + r % gsize;
+    const int nb = r / gsize;
+    tile.a_row0 = mp * 2 * kBlockM + rank * kBlockM;
+    tile.n0 = nb * BN;
+    tile.b_row0 = tile.n0 + rank * (BN / 2);
+}
+
+template <int BN, bool WITH_C>
+__global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2, 1, 1)
+    dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                       const __grid_constant__ CUtensorMap tm_b,
+                       const __grid_constant__ CUtensorMap tm_sfa,
+                       const __grid_constant__ CUtensorMap tm_sfb,
+                       const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
+    using Cfg = Bs2Config<BN>;
+    constexpr int S = Cfg::kStages;
+    constexpr int R = Cfg::kRing;
+    constexpr int G = Cfg::kGroupKb;
+    constexpr int NUM_ACC = Cfg::kNumAcc;
+    constexpr int NSF = Cfg::kSfSlots;
+    constexpr int MMA_M = 2 * kBlockM;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem_a = smem;
+    uint8_t *smem_b = smem_a + S * Cfg::kABytes;
+    uint8_t *smem_stage_out = smem_b + S * Cfg::kBBytes;
+    uint8_t *smem_sf = smem_stage_out + Cfg::kStagingBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_sf + NSF * Cfg::kSfSlotBytes);
+    uint64_t *full_bar = bars;                        // [R] leader: both CTAs' stages landed
+    uint64_t *empty_bar = full_bar + R;               // [R] both: MMAs done with the slot
+    uint64_t *tfull_bar = empty_bar + R;              // [NUM_ACC] both: accumulator complete
+    uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] leader: both epilogues drained
+    uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] both: own scale words landed
+    uint64_t *sf_peer_bar = sf_full_bar + NSF;        // [NSF] leader: peer's words reordered
+    uint64_t *sf_ready_bar = sf_peer_bar + NSF;       // [NSF] leader: words copied to both TMEMs
+    uint64_t *sf_free_bar = sf_ready_bar + NSF;       // [NSF] both: MMAs done with the slot
+    uint64_t *drain_bar = sf_free_bar + NSF;          // [2]
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    const int rank = static_cast<int>(cluster_ctarank());   // 0 = leader
+    const bool leader = rank == 0;
+    const int pair_id = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int num_tiles = p.num_m_blocks * p.num_n_blocks;  // num_m_blocks counts 256-row pairs
+    const int groups_per_tile = (p.num_k_blocks + 3) >> 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            mbar_init(&tfull_bar[a], 1);
+            mbar_init(&tempty_bar[a], 2 * Cfg::kEpiWarps);
+        }
+        for (int j = 0; j < NSF; ++j) {
+            mbar_init(&sf_full_bar[j], 1);
+            mbar_init(&sf_peer_bar[j], 1);
+            mbar_init(&sf_ready_bar[j], 1);
+            mbar_init(&sf_free_bar[j], 1);
+        }
+        mbar_init(&drain_bar[0], 1);
+        mbar_init(&drain_bar[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_sfa);
+        tma_prefetch_desc(&tm_sfb);
+        tma_prefetch_desc(&tm_d);
+    }
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t sf_col0 = NUM_ACC * BN;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+            int slot = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;
+            bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && pair_id == 0;
+            int gs = 0, ga = 0;
+            uint32_t sf_issued = 0;
+            // scale cursor: (tile, group) sequence, kept one group ahead of A/B
+            int sf_t = pair_id, sf_j = 0;
+            for (int t = pair_id; t < num_tiles; t += num_pairs) {
+                PairTile tile;
+                get_pair_tile<BN>(p, t, rank, tile);
+                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                    if ((kb0 & 3) == 0) {
+                        while (sf_t < num_tiles && gs <= ga + 1) {
+                            const int sslot = gs % NSF;
+                            if (!mbar_wait(&sf_free_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                                goto prod_done;
+                            PairTile st;
+                            get_pair_tile<BN>(p, sf_t, rank, st);
+                            uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
+                            mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
+                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.a_row0, sf_j);
+                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0, sf_j);
+                            sf_issued |= 1u << sslot;
+                            ++gs;
+                            if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
+                        }
+                        ++ga;
+                    }
+                    if (!mbar_wait(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
+                    if (drop) {
+                        drop = false;  // diagnostic: leave this slot empty
+                    } else {
+                        // the leader expects both CTAs' bytes; each CTA's loads count there
+                        if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kStageBytes);
+                        const uint32_t fb = leader_full + slot * 8;
+                        auto load_kb = [&](int j) {
+                            const int kb = kb0 + j;
+                            const int stage = slot * G + j;
+                            tma_load_2d_pair(smem_a + stage * Cfg::kABytes, &tm_a, fb, kb * kBlockK, tile.a_row0);
+                            tma_load_2d_pair(smem_b + stage * Cfg::kBBytes, &tm_b, fb, kb * kBlockK, tile.b_row0);
+                        };
+                        if (nk == G) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) load_kb(j);
+                        } else {
+                            for (int j = 0; j < nk; ++j) load_kb(j);
+                        }
+                        issued |= 1u << slot;
+                    }
+                    if (++slot == R) { slot = 0; phase ^= 1; }
+                }
+            }
+        prod_done:
+            // the leader waits for the last fill of every slot (both CTAs' bytes count there)
+            if (leader)
+                for (int s = 0; s < R; ++s)
+                    if (issued & (1u << s))
+                        mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+            for (int j = 0; j < NSF; ++j)
+                if (sf_issued & (1u << j)) {
+                    const int g = gs - 1 - ((gs - 1 - j) % NSF + NSF) % NSF;
+                    mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader, one lane)
+        if (leader && lane == 0) {
+            int slot = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int g = 0;
+            const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
+            const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
+            constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, BN, 0, 0);
+            for (int t = pair_id; t < num_tiles; t += num_pairs) {
+                if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                    const int sslot = g % NSF;
+                    if ((kb0 & 3) == 0) {
+                        if (!mbar_wait(&sf_ready_bar[sslot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
+                            goto mma_done;
+                    }
+                    if (!mbar_wait(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                    tc_fence_after_sync();
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + sslot * Cfg::kSfCols;
+                    const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
+                    const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
+                    auto mma_kb = [&](int j) {
+                        const int kb = kb0 + j;
+                        const uint32_t sf = static_cast<uint32_t>(kb & 3);
+                        const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
+                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
+                        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kBBytes >> 4));
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            tc_mma_mxf8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
+                                             sfa_tmem + 4, (kb | k) != 0);
+                    };
+                    if (nk == G) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) mma_kb(j);
+                    } else {
+                        for (int j = 0; j < nk; ++j) mma_kb(j);
+                    }
+                    tc_commit_pair(&empty_bar[slot], 0x3);
+                    const int kb_last = kb0 + nk - 1;
+                    if ((kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1) {
+                        tc_commit_pair(&sf_free_bar[sslot], 0x3);
+                        ++g;
+                    }
+                    if (++slot == R) { slot = 0; phase ^= 1; }
+                }
+                tc_commit_pair(&tfull_bar[acc], 0x3);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+            }
+        mma_done:
+            tc_commit_pair(&drain_bar[0], 0x1);
+            mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == Cfg::kSfWarp) {
+        // ------------------------------------------------------------ scale-factor warp (both CTAs)
+        const uint32_t leader_peer = mapa_shared(smem_u32(sf_peer_bar), 0);
+        int g = 0;
+        bool copied = false;
+        for (int t = pair_id; t < num_tiles; t += num_pairs) {
+            for (int j = 0; j < groups_per_tile; ++j, ++g) {
+                const int slot = g % NSF;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
+                    goto sf_done;
+                uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
+                uint32_t *sfb_buf = sfa_buf + 128;
+                sf_transpose_for_cp(sfa_buf, lane);
+#pragma unroll
+                for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (!leader) {
+                    // tell the leader this CTA's words for the group are in place
+                    if (lane == 0) mbar_arrive_cluster(leader_peer + slot * 8);
+                } else {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
+                        goto sf_done;
+                    if (lane == 0) {
+                        tc_fence_after_sync();
+                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                        tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+#pragma unroll
+                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                            tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
+                                                      make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                        tc_commit_pair(&sf_ready_bar[slot], 0x1);
+                        copied = true;
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    sf_done:
+        if (leader && lane == 0 && copied) {
+            tc_commit_pair(&drain_bar[1], 0x1);
+            mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const uint32_t ew = warp - 2;
+        const uint32_t quad = warp & 3;
+        const uint32_t half = ew >> 2;
+        const uint32_t leader_tempty = mapa_shared(smem_u32(tempty_bar), 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t buf = 0;
+        uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
+        for (int t = pair_id; t < num_tiles; t += num_pairs) {
+            PairTile tile;
+            get_pair_tile<BN>(p, t, rank, tile);
+            const int row = tile.a_row0 + quad * 32 + lane;
+            const bool row_ok = row < p.rows;
+            uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
+            if constexpr (WITH_C) {
+#pragma unroll
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                    const int c = 2 * j + half;
+                    const int col0 = tile.n0 + c * Cfg::kEpiChunk;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+                        if (c < Cfg::kNumChunks && row_ok && col0 + 8 * h < p.n)
+                            cv = __ldg(reinterpret_cast<const uint4 *>(
+                                p.c + static_cast<int64_t>(row) * p.ldc + col0 + 8 * h));
+                        cpk[j][4 * h + 0] = cv.x;
+                        cpk[j][4 * h + 1] = cv.y;
+                        cpk[j][4 * h + 2] = cv.z;
+                        cpk[j][4 * h + 3] = cv.w;
+                    }
+                }
+            }
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
+            tc_fence_after_sync();
+            uint32_t out[Cfg::kChunksPerWarp][8];
+#pragma unroll
+            for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
+                uint32_t v[2][16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int c = 2 * (j0 + u) + half;
+                    if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
+                        tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (j0 + u >= Cfg::kChunksPerWarp) continue;
+                    reg_fence16(v[u]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float lo = __uint_as_float(v[u][2 * i]);
+                        float hi = __uint_as_float(v[u][2 * i + 1]);
+                        if constexpr (WITH_C) {
+                            lo += __uint_as_float(cpk[j0 + u][i] << 16);
+                            hi += __uint_as_float(cpk[j0 + u][i] & 0xFFFF0000u);
+                        }
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                        out[j0 + u][i] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+
+#pragma unroll
+            for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                const int c = 2 * j + half;
+                if (c >= Cfg::kNumChunks) continue;
+                const int col0 = tile.n0 + c * Cfg::kEpiChunk;
+                uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t off = lane * 32 + ((h ^ ((lane >> 2) & 1)) * 16);
+                    *reinterpret_cast<uint4 *>(sbuf + off) =
+                        make_uint4(out[j][4 * h], out[j][4 * h + 1], out[j][4 * h + 2], out[j][4 * h + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tm_d, sbuf, col0, tile.a_row0 + quad * 32);
+                    bulk_commit_group();
+                }
+                buf ^= 1;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    // neither CTA leaves while its peer may still signal its barriers or read its shared memory
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <int BN, bool WITH_C>
+cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
+                                 cudaStream_t stream) {
+    using Cfg = Bs2Config<BN>;
+    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dg_bs2_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
+        maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
+    return cudaGetLastError();
+}
+
+template <int BN, bool WITH_C>
+int max_active_pairs_impl() {
+    using Cfg = Bs2Config<BN>;
+    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C>, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int BN>
+void fill_bs2_info(KernelInfo *info) {
+    using Cfg = Bs2Config<BN>;
+    info->block_n = BN;
+    info->stages = Cfg::kStages;
+    info->smem_bytes = Cfg::kSmemBytes;
+    info->threads = Cfg::kThreads;
+}
+
+}  // namespace dg

@@ -2,6 +2,7 @@
 // (which live in the gemm_bs_inst_*.cu units).
 #include "gemm_bs.cuh"
 #include "gemm_promote.cuh"
+#include "gemm_bs2.cuh"
 
 namespace dg {
 
@@ -18,6 +19,37 @@ DG_BS_BLOCK_N_LIST(DG_EXTERN)
     extern template cudaError_t launch_bs_gemm_impl<BN, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
 DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #undef DG_EXTERN
+
+#define DG_BS2_LIST(X) X(128, false) X(128, true) X(192, false) X(224, false) X(256, false)
+#define DG_EXTERN2(BN, C)                                                                        \
+    extern template cudaError_t launch_bs2_gemm_impl<BN, C>(const TensorMaps &, const GemmParams &, \
+                                                            int, cudaStream_t);                      \
+    extern template int max_active_pairs_impl<BN, C>();
+DG_BS2_LIST(DG_EXTERN2)
+#undef DG_EXTERN2
+
+bool get_bs2_kernel_info(int block_n, bool with_c, KernelInfo *info) {
+#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) { fill_bs2_info<BN>(info); return true; }
+    DG_BS2_LIST(DG_CASE2)
+#undef DG_CASE2
+    return false;
+}
+
+cudaError_t launch_bs2_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+                            cudaStream_t stream) {
+    const bool with_c = p.c != nullptr;
+#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) return launch_bs2_gemm_impl<BN, C>(maps, p, grid, stream);
+    DG_BS2_LIST(DG_CASE2)
+#undef DG_CASE2
+    return cudaErrorInvalidValue;
+}
+
+int bs2_max_active_pairs(int block_n, bool with_c) {
+#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) return max_active_pairs_impl<BN, C>();
+    DG_BS2_LIST(DG_CASE2)
+#undef DG_CASE2
+    return 0;
+}
 
 bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info) {
     if (with_c) {

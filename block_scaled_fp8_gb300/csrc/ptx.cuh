@@ -56,6 +56,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 
+// As mbar_try_wait, with cluster-scope acquire: for barriers that the other CTA
+// of a cluster arrives on after its own writes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Per-CTA control block for bounded waits: when any wait runs out it raises
 // `abort` (shared memory) so every other role of the CTA stops waiting too,
 // and records the failure in the caller's status word.
@@ -65,13 +79,15 @@ struct WaitCtl {
     uint64_t timeout_ns;
 };
 
+template <bool CLUSTER = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar_addr, uint32_t parity, WaitCtl ctl,
                                             int32_t timeout_flag) {
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar_addr, parity)) return true;
+            if (CLUSTER ? mbar_try_wait_cluster(bar_addr, parity) : mbar_try_wait(bar_addr, parity))
+                return true;
         if (*ctl.abort) return false;
         if (global_timer_ns() - t0 > ctl.timeout_ns) {
             *ctl.abort = 1;
@@ -88,6 +104,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     return mbar_wait_slow(a, parity, ctl, timeout_flag);
+}
+
+// As mbar_wait, with cluster-scope acquire (arrivals come from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
+                                                  int32_t timeout_flag) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    return mbar_wait_slow<true>(a, parity, ctl, timeout_flag);
 }
 
 // ----------------------------------------------------------------- clusters
@@ -114,6 +138,19 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
+}
+
+// Address of the same shared-memory location in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in a peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
 }
 
 // All threads of all CTAs of the cluster (release/acquire ordering).
@@ -173,6 +210,17 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y)
                  : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (cluster address `bar_cluster`).
+__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src,
@@ -255,6 +303,55 @@ __device__ __forceinline__ void tc_commit_multicast(uint64_t *bar, uint16_t cta_
             smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+// ---- CTA-pair (cta_group::2) forms: the pair's two SMs act as one MMA unit.
+// Allocation is collective (one warp in each CTA); the leader issues the MMAs,
+// which read A rows 0-127 / B rows 0..N/2-1 from the leader's shared memory and
+// A rows 128-255 / B rows N/2..N-1 from the peer's (same offsets), and write
+// each CTA's 128 rows of D into its own TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Arrive on the mbarrier at this offset in every CTA of `cta_mask` when all
+// tcgen05 operations this thread issued so far have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copies each CTA's own shared-memory source into its own TMEM (issued by the leader).
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t src_desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+                 : "memory");
 }
 
 // D(tmem) (+)= A(smem) * B(smem)^T with UE8M0 block scales read from TMEM,

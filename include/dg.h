@@ -187,8 +187,10 @@ void dg_set_wait_timeout_ms(int ms);
  * launch skip its first operand load, so its consumer's bounded wait runs
  * out and DG_DEV_TIMEOUT is reported (used by the failure-detection test;
  * the flag clears itself after one launch).  DG_DEBUG_PRINT_CONFIGS prints
- * the chosen tile configuration of each GEMM to stderr. */
-enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2 };
+ * the chosen tile configuration of each GEMM to stderr.  DG_DEBUG_SINGLE_CTA
+ * runs dense GEMMs on single CTAs (128-row tiles) where CTA pairs (256-row
+ * tiles) would be chosen; results are bit-identical either way. */
+enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2, DG_DEBUG_SINGLE_CTA = 4 };
 void dg_set_debug_flags(uint32_t flags);
 
 /* Human-readable name of a dg_status value. */
@@ -196,7 +198,8 @@ const char *dg_status_string(int status);
 
 /* Tile configuration the last GEMM call on this thread launched:
  * out[0]=BLOCK_M, out[1]=BLOCK_N, out[2]=stages, out[3]=grid size,
- * out[4]=kernel kind (0 block-scaled, 1 FP32-promotion), out[5]=number of
+ * out[4]=kernel kind (0 block-scaled, 1 FP32-promotion, 2 block-scaled on
+ * CTA pairs), out[5]=number of
  * kernel launches of that call. */
 void dg_get_last_config(int out[6]);
 

@@ -1,0 +1,87 @@
+"""The CTA-pair kernel (256-row tiles, tcgen05 cta_group::2) against the oracle
+and, bit for bit, against the single-CTA kernel on the same inputs.
+
+Dense GEMMs with more than 128 rows run on CTA pairs; DG_DEBUG_SINGLE_CTA
+forces the single-CTA kernel, so the two paths can be compared directly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_gb300 import binding, inputs
+from tests._util import assert_close, bf16_bits, sb_rows, u8
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = "cuda"
+
+
+def _gemm(case, single_cta, c=None):
+    M, N, K = case.shape
+    sfa = binding.transform_sf(case.sfa.to(DEV), 1, M)
+    sfb = binding.transform_sf(case.sfb.to(DEV), 128, N)
+    d = torch.full((M, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.set_debug_flags(binding.DG_DEBUG_SINGLE_CTA if single_cta else 0)
+    try:
+        binding.dg_fp8_gemm_nt(case.a.to(DEV), sfa, case.b.to(DEV), sfb, d, c=c, status=status)
+        cfg = binding.last_config()
+    finally:
+        binding.set_debug_flags(0)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return d, cfg
+
+
+# ragged M (one pair half empty, a tail pair), ragged N (half a 128-block),
+# K not a multiple of 128 or of the 4-block scale group
+SHAPES = [(256, 256, 512), (257, 200, 640), (300, 520, 1024), (384, 72, 128),
+          (640, 1000, 336), (1000, 7168, 1536), (4096, 2112, 7168)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_pair_matches_single_cta_bitwise(M, N, K):
+    case = inputs.dense_case(M, N, K, seed=M * 3 + N + K, b_scale_exp_range=(-8, 4))
+    d_pair, cfg_pair = _gemm(case, single_cta=False)
+    d_one, cfg_one = _gemm(case, single_cta=True)
+    assert cfg_pair["kind"] == 2 and cfg_pair["block_m"] == 256
+    assert cfg_one["kind"] == 0 and cfg_one["block_m"] == 128
+    assert torch.equal(d_pair, d_one), f"{M}x{N}x{K}: pair and single-CTA results differ"
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 520, 1024), (1000, 264, 768)])
+def test_pair_with_c_full_compare(orc, M, N, K):
+    case = inputs.dense_case(M, N, K, seed=M + 11, with_c=True)
+    d, cfg = _gemm(case, single_cta=False, c=case.c.to(DEV))
+    assert cfg["kind"] == 2
+    ref = orc.gemm_nt(u8(case.a), case.sfa.double().numpy(), u8(case.b), sb_rows(case.sfb, N),
+                      c=bf16_bits(case.c))
+    assert_close(bf16_bits(d), ref, f"pair with C {M}x{N}x{K}")
+    d_one, _ = _gemm(case, single_cta=True, c=case.c.to(DEV))
+    assert torch.equal(d, d_one)
+
+
+def test_pair_integer_exact_bitwise(orc):
+    case = inputs.integer_exact_case(512, 640, 1024, seed=5)
+    d, cfg = _gemm(case, single_cta=False)
+    assert cfg["kind"] == 2
+    ref = orc.gemm_nt(u8(case.a), case.sfa.double().numpy(), u8(case.b), sb_rows(case.sfb, 640))
+    assert np.array_equal(bf16_bits(d), ref)
+
+
+def test_pair_full_compare_several_waves(orc):
+    """More pair tiles than co-resident pairs: every pair runs several tiles
+    (accumulator double-buffering and the scale ring wrap many times)."""
+    M, N, K = 2048, 4096, 640
+    case = inputs.dense_case(M, N, K, seed=17)
+    d, cfg = _gemm(case, single_cta=False)
+    assert cfg["kind"] == 2
+    tiles = (M // 256) * -(-N // cfg["block_n"])
+    assert tiles > cfg["grid"] // 2
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, M, 4000)
+    cols = rng.integers(0, N, 4000)
+    ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                              sb_rows(case.sfb, N), rows, cols)
+    assert_close(bf16_bits(d)[rows, cols], ref, "pair several waves")
