@@ -202,7 +202,12 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     // same score as choose_block_n, over the co-resident pairs
     int bn = 0;
     double best = -1.0;
-    for (int cand : {128, 192, 224, 256}) {
+    static const int forced_bn = [] {
+        const char *e = std::getenv("DG_PAIR_BLOCK_N");
+        return e ? std::atoi(e) : 0;
+    }();
+    for (int cand : {128, 192, 224, 240, 256}) {
+        if (forced_bn && cand != forced_bn) continue;
         KernelInfo ki;
         if (!get_bs2_kernel_info(cand, with_c, &ki)) continue;
         int pairs = cached_max_pairs(cand, with_c);

@@ -31,13 +31,26 @@ namespace dg {
 
 template <int BN>
 struct Bs2Config {
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN/2 rows of B per CTA, N <= 256");
+    // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; M=256 MMAs take N % 16 == 0, N <= 256
+    static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "BN/2 rows of B per CTA, N <= 256");
     static constexpr int kThreads = 352;
     static constexpr int kEpiWarps = 8;
     static constexpr int kSfWarp = 10;
     static constexpr int kSfbChunks = (BN + 127) / 128;
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;
-    static constexpr int kSfSlots = 4;
+    // Scale words pass through two rings: kSfSlots shared-memory slots (TMA
+    // destination, reordered in place) and kSfTmemSlots TMEM slots (what the
+    // MMA reads).  The producer issues the scale loads kSfLookahead groups
+    // ahead of the A/B group it is loading: the words queue behind the A/B
+    // tiles in the TMA unit, and the peer's hand-off to the leader takes about
+    // a microsecond, so both must start well before the MMAs need the group.
+    // A shared-memory slot frees when its copy into TMEM completes, which is
+    // more than kSfSlots - kSfLookahead groups behind the loads.  Four TMEM slots where two accumulators fit beside them; two
+    // where that makes room for a second accumulator (BN=240).
+    static constexpr int kSfSlots = 8;
+    static constexpr int kSfLookahead = kSfSlots - 3;
+    static constexpr int kSfTmemSlots =
+        (2 * BN + 4 * kSfCols <= 512 || 2 * BN + 2 * kSfCols > 512) ? 4 : 2;
     static constexpr int kABytes = kBlockM * kBlockK;           // this CTA's 128 rows of A
     static constexpr int kBBytes = (BN / 2) * kBlockK;          // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -56,9 +69,9 @@ struct Bs2Config {
     static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;
-    static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kNumAcc = (2 * BN + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
-    static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kNumAcc * BN + kSfTmemSlots * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kRing >= 2, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -99,7 +112,8 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     constexpr int R = Cfg::kRing;
     constexpr int G = Cfg::kGroupKb;
     constexpr int NUM_ACC = Cfg::kNumAcc;
-    constexpr int NSF = Cfg::kSfSlots;
+    constexpr int NSF = Cfg::kSfSlots;       // shared-memory scale slots
+    constexpr int NTS = Cfg::kSfTmemSlots;   // TMEM scale slots
     constexpr int MMA_M = 2 * kBlockM;
 
     extern __shared__ uint8_t smem_raw[];
@@ -116,9 +130,10 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] leader: both epilogues drained
     uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] both: own scale words landed
     uint64_t *sf_peer_bar = sf_full_bar + NSF;        // [NSF] leader: peer's words reordered
-    uint64_t *sf_ready_bar = sf_peer_bar + NSF;       // [NSF] leader: words copied to both TMEMs
-    uint64_t *sf_free_bar = sf_ready_bar + NSF;       // [NSF] both: MMAs done with the slot
-    uint64_t *drain_bar = sf_free_bar + NSF;          // [2]
+    uint64_t *sf_sfree_bar = sf_peer_bar + NSF;       // [NSF] both: words copied out of the slot
+    uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] leader: words in both TMEMs
+    uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] leader: MMAs done with the slot
+    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [2]
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -144,8 +159,11 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         for (int j = 0; j < NSF; ++j) {
             mbar_init(&sf_full_bar[j], 1);
             mbar_init(&sf_peer_bar[j], 1);
+            mbar_init(&sf_sfree_bar[j], 1);
+        }
+        for (int j = 0; j < NTS; ++j) {
             mbar_init(&sf_ready_bar[j], 1);
-            mbar_init(&sf_free_bar[j], 1);
+            mbar_init(&sf_tfree_bar[j], 1);
         }
         mbar_init(&drain_bar[0], 1);
         mbar_init(&drain_bar[1], 1);
@@ -172,46 +190,49 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     const uint32_t sf_col0 = NUM_ACC * BN;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer (both CTAs)
-        if (lane == 0) {
-            const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
-            int slot = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0;
-            bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && pair_id == 0;
-            int gs = 0, ga = 0;
-            uint32_t sf_issued = 0;
-            // scale cursor: (tile, group) sequence, kept one group ahead of A/B
-            int sf_t = pair_id, sf_j = 0;
-            for (int t = pair_id; t < num_tiles; t += num_pairs) {
-                PairTile tile;
-                get_pair_tile<BN>(p, t, rank, tile);
-                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
-                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                    if ((kb0 & 3) == 0) {
-                        while (sf_t < num_tiles && gs <= ga + 1) {
-                            const int sslot = gs % NSF;
-                            if (!mbar_wait(&sf_free_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                                goto prod_done;
-                            PairTile st;
-                            get_pair_tile<BN>(p, sf_t, rank, st);
+        // ------------------------------------------------------------ producer (both CTAs, whole warp)
+        const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+        int slot = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;
+        bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && pair_id == 0;
+        int gs = 0, ga = 0;
+        uint32_t sf_issued = 0;
+        // scale cursor over the same (tile, group) sequence, kSfLookahead groups ahead of A/B
+        int sf_t = pair_id, sf_j = 0;
+        for (int t = pair_id; t < num_tiles; t += num_pairs) {
+            PairTile tile;
+            get_pair_tile<BN>(p, t, rank, tile);
+            for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                if ((kb0 & 3) == 0) {
+                    while (sf_t < num_tiles && gs <= ga + Cfg::kSfLookahead) {
+                        const int sslot = gs % NSF;
+                        if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                            goto prod_done;
+                        PairTile st;
+                        get_pair_tile<BN>(p, sf_t, rank, st);
+                        if (elect_one()) {
                             uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
                             mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
                             tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.a_row0, sf_j);
                             tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0, sf_j);
-                            sf_issued |= 1u << sslot;
-                            ++gs;
-                            if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
                         }
-                        ++ga;
+                        __syncwarp();
+                        sf_issued |= 1u << sslot;
+                        ++gs;
+                        if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
                     }
-                    if (!mbar_wait(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
-                    if (drop) {
-                        drop = false;  // diagnostic: leave this slot empty
-                    } else {
+                    ++ga;
+                }
+                if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
+                if (drop) {
+                    drop = false;  // diagnostic: leave this slot empty
+                } else {
+                    const uint32_t fb = leader_full + slot * 8;
+                    if (elect_one()) {
                         // the leader expects both CTAs' bytes; each CTA's loads count there
                         if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kStageBytes);
-                        const uint32_t fb = leader_full + slot * 8;
                         auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
                             const int stage = slot * G + j;
@@ -224,26 +245,31 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                         } else {
                             for (int j = 0; j < nk; ++j) load_kb(j);
                         }
-                        issued |= 1u << slot;
                     }
-                    if (++slot == R) { slot = 0; phase ^= 1; }
+                    __syncwarp();
+                    issued |= 1u << slot;
                 }
+                if (++slot == R) { slot = 0; phase ^= 1; }
             }
-        prod_done:
+        }
+    prod_done:
+        if (lane == 0) {
             // the leader waits for the last fill of every slot (both CTAs' bytes count there)
             if (leader)
                 for (int s = 0; s < R; ++s)
                     if (issued & (1u << s))
                         mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+            // and every CTA for its last scale load into each slot
             for (int j = 0; j < NSF; ++j)
                 if (sf_issued & (1u << j)) {
                     const int g = gs - 1 - ((gs - 1 - j) % NSF + NSF) % NSF;
                     mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
                 }
         }
+        __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (leader, one lane)
-        if (leader && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader, whole warp)
+        if (leader) {
             int slot = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -253,54 +279,59 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
             const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
             constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, BN, 0, 0);
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
-                if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                if (!mbar_wait_cluster_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                     const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                    const int sslot = g % NSF;
+                    const int sslot = g % NTS;
                     if ((kb0 & 3) == 0) {
-                        if (!mbar_wait(&sf_ready_bar[sslot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
+                        if (!mbar_wait_warp(&sf_ready_bar[sslot], (g / NTS) & 1, ctl, DG_DEV_TIMEOUT))
                             goto mma_done;
                     }
-                    if (!mbar_wait(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+                    if (!mbar_wait_warp(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                     tc_fence_after_sync();
                     const uint32_t sfa_tmem = tmem_base + sf_col0 + sslot * Cfg::kSfCols;
                     const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
                     const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
-                    auto mma_kb = [&](int j) {
-                        const int kb = kb0 + j;
-                        const uint32_t sf = static_cast<uint32_t>(kb & 3);
-                        const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
-                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
-                        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kBBytes >> 4));
-#pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k)
-                            tc_mma_mxf8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
-                                             sfa_tmem + 4, (kb | k) != 0);
-                    };
-                    if (nk == G) {
-#pragma unroll
-                        for (int j = 0; j < G; ++j) mma_kb(j);
-                    } else {
-                        for (int j = 0; j < nk; ++j) mma_kb(j);
-                    }
-                    tc_commit_pair(&empty_bar[slot], 0x3);
                     const int kb_last = kb0 + nk - 1;
-                    if ((kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1) {
-                        tc_commit_pair(&sf_free_bar[sslot], 0x3);
-                        ++g;
+                    const bool group_end = (kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1;
+                    if (elect_one()) {
+                        auto mma_kb = [&](int j) {
+                            const int kb = kb0 + j;
+                            const uint32_t sf = static_cast<uint32_t>(kb & 3);
+                            const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
+                            const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
+                            const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kBBytes >> 4));
+#pragma unroll
+                            for (int k = 0; k < kBlockK / 32; ++k)
+                                tc_mma_mxf8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
+                                                 sfa_tmem + 4, (kb | k) != 0);
+                        };
+                        if (nk == G) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) mma_kb(j);
+                        } else {
+                            for (int j = 0; j < nk; ++j) mma_kb(j);
+                        }
+                        tc_commit_pair(&empty_bar[slot], 0x3);
+                        if (group_end) tc_commit_pair(&sf_tfree_bar[sslot], 0x1);
                     }
+                    __syncwarp();
+                    if (group_end) ++g;
                     if (++slot == R) { slot = 0; phase ^= 1; }
                 }
-                tc_commit_pair(&tfull_bar[acc], 0x3);
+                if (elect_one()) tc_commit_pair(&tfull_bar[acc], 0x3);
+                __syncwarp();
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
             }
         mma_done:
-            tc_commit_pair(&drain_bar[0], 0x1);
-            mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
+            if (elect_one()) {
+                tc_commit_pair(&drain_bar[0], 0x1);
+                mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp == Cfg::kSfWarp) {
         // ------------------------------------------------------------ scale-factor warp (both CTAs)
         const uint32_t leader_peer = mapa_shared(smem_u32(sf_peer_bar), 0);
@@ -309,8 +340,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             for (int j = 0; j < groups_per_tile; ++j, ++g) {
                 const int slot = g % NSF;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
-                    goto sf_done;
+                if (!mbar_wait_warp(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)) goto sf_done;
                 uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
                 uint32_t *sfb_buf = sfa_buf + 128;
                 sf_transpose_for_cp(sfa_buf, lane);
@@ -322,17 +352,21 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                     // tell the leader this CTA's words for the group are in place
                     if (lane == 0) mbar_arrive_cluster(leader_peer + slot * 8);
                 } else {
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
+                    const int tslot = g % NTS;
+                    if (!mbar_wait_cluster_warp(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
+                        goto sf_done;
+                    if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
                         goto sf_done;
                     if (lane == 0) {
                         tc_fence_after_sync();
-                        const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                        const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
                         tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
 #pragma unroll
                         for (int c = 0; c < Cfg::kSfbChunks; ++c)
                             tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
                                                       make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
-                        tc_commit_pair(&sf_ready_bar[slot], 0x1);
+                        tc_commit_pair(&sf_ready_bar[tslot], 0x1);
+                        tc_commit_pair(&sf_sfree_bar[slot], 0x3);   // both CTAs may refill the slot
                         copied = true;
                     }
                 }
@@ -340,7 +374,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
             }
         }
     sf_done:
-        if (leader && lane == 0 && copied) {
+        if (lane == 0 && leader && copied) {
             tc_commit_pair(&drain_bar[1], 0x1);
             mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
         }

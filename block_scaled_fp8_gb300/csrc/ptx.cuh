@@ -114,6 +114,31 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return mbar_wait_slow<true>(a, parity, ctl, timeout_flag);
 }
 
+// One lane of the converged warp (the lowest active lane).  The issuing
+// loops of the producer and MMA warps run on all 32 lanes, so their
+// warp-uniform operands (descriptors, coordinates, TMEM addresses) stay in
+// uniform registers, and only the issue itself is guarded by this election.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// Warp-uniform outcome of a bounded wait that every lane performs.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
+                                               int32_t timeout_flag) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, ctl, timeout_flag));
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
+                                                       int32_t timeout_flag) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar, parity, ctl, timeout_flag));
+}
+
 // ----------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
