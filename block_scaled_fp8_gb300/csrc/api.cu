@@ -162,23 +162,6 @@ int choose_cluster(int64_t num_n_blocks) {
     return c;
 }
 
-// L2 prefetch distance (K-blocks ahead of the loads) and which operands to
-// prefetch.  DG_PREFETCH_KB / DG_PREFETCH_MASK override the defaults.
-void choose_prefetch(GemmParams &p, int64_t m_blocks, int stages) {
-    static const int env_kb = [] {
-        const char *e = std::getenv("DG_PREFETCH_KB");
-        return e ? std::atoi(e) : -1;
-    }();
-    static const int env_mask = [] {
-        const char *e = std::getenv("DG_PREFETCH_MASK");
-        return e ? std::atoi(e) : -1;
-    }();
-    (void)m_blocks;
-    (void)stages;
-    p.prefetch_kb = env_kb >= 0 ? env_kb : 0;
-    p.prefetch_mask = env_mask >= 0 ? (env_mask & 3) : 0;
-}
-
 // Dense problems with more than one 128-row block run on CTA pairs (256-row
 // tiles, cta_group::2) unless DG_DEBUG_SINGLE_CTA is set.
 bool use_pair_kernel(const GemmParams &p) {
@@ -308,7 +291,6 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
     p.cluster = cluster;
     p.num_n_groups = static_cast<int>(cdiv64(p.num_n_blocks, cluster));
-    choose_prefetch(p, m_blocks_hint, info.stages);
     p.group_m = 8;
     p.d = static_cast<uint16_t *>(o.d);
     p.ldd = o.ldd;

@@ -26,8 +26,6 @@ struct GemmParams {
     int num_k_blocks;
     int cluster;         // CTAs per cluster along N (they share the A tile by TMA multicast)
     int num_n_groups;    // ceil(num_n_blocks / cluster): n-block groups, one per cluster tile
-    int prefetch_kb;     // K-blocks the producer prefetches into L2 ahead of its loads (0 = off)
-    int prefetch_mask;   // bit 0: prefetch A tiles, bit 1: prefetch B tiles
     int num_groups;
     int group_m;         // tile-order group size along M (L2 reuse)
     const int32_t *grouped_layout;  // contiguous

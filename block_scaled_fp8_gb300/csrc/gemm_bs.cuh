@@ -44,7 +44,14 @@ struct BsConfig {
     static constexpr int kSfWarp = 10;
     static constexpr int kSfbChunks = (BN + 127) / 128;        // 128-word tcgen05.cp chunks
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per scale slot
-    static constexpr int kSfSlots = 4;                          // scale groups in flight (smem + TMEM)
+    // Scale words pass through kSfSlots shared-memory slots (TMA destination,
+    // reordered in place) and kSfTmemSlots TMEM slots (what the MMA reads).  The
+    // producer loads them kSfLookahead groups ahead of its A/B group: they queue
+    // behind the A/B tiles in the TMA unit, and the copy into TMEM queues behind
+    // the issued MMAs, so both must start well before the MMAs need the group.
+    static constexpr int kSfSlots = 8;
+    static constexpr int kSfLookahead = kSfSlots - 3;
+    static constexpr int kSfTmemSlots = 4;
     static constexpr int kABytes = kBlockM * kBlockK;           // 16 KB
     static constexpr int kBBytes = BN * kBlockK;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -63,16 +70,16 @@ struct BsConfig {
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
     // K-blocks per ring slot: the stages of a slot share one full and one empty
-    // barrier, so the MMA issuer waits and commits once per kGroupKb K-blocks
-    // (each wait or commit costs the issuing thread 70-200 cycles).  The largest
+    // barrier, so the MMA warp waits and commits once per kGroupKb K-blocks
+    // (each wait or commit costs the issuing warp about 100 cycles).  The largest
     // of 4, 2, 1 that still leaves 4 slots in the ring (the load latency needs
     // that depth); it divides 4, so slots never straddle a scale group.
     static constexpr int kGroupKb = kStagesCap >= 16 ? 4 : (kStagesCap >= 8 ? 2 : 1);
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;             // barrier slots
-    static constexpr int kNumAcc = (2 * BN + kSfSlots * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kNumAcc = (2 * BN + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
-    static_assert(kNumAcc * BN + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kNumAcc * BN + kSfTmemSlots * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kRing >= 2, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -121,33 +128,6 @@ struct GroupCursor {
     }
 };
 
-// Walks the (tile, K-block) sequence of one CTA in scheduler order; the
-// producer runs it ahead of its loads to prefetch A/B tiles into L2.
-template <int BN>
-struct KbCursor {
-    const GemmParams *p;
-    const int *prefix;
-    int t, kb, num_tiles, num_clusters, rank, psf_k;
-    bool valid;
-    Tile tile;
-    __device__ __forceinline__ void start(const GemmParams &params, const int *pre, int cluster_id,
-                                          int nclusters, int r, int ntiles, int psf) {
-        p = &params; prefix = pre; num_clusters = nclusters; rank = r; num_tiles = ntiles;
-        psf_k = psf;
-        t = cluster_id - nclusters;
-        next_tile();
-    }
-    __device__ __forceinline__ void next_tile() {
-        kb = 0;
-        valid = false;
-        for (t += num_clusters; t < num_tiles; t += num_clusters)
-            if (get_tile<BN>(*p, prefix, t, rank, psf_k, tile, false)) { valid = true; return; }
-    }
-    __device__ __forceinline__ void next() {
-        if (++kb == p->num_k_blocks) next_tile();
-    }
-};
-
 template <int BN, bool WITH_C>
 __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     dg_bs_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -158,7 +138,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     using Cfg = BsConfig<BN>;
     constexpr int S = Cfg::kStages;
     constexpr int NUM_ACC = Cfg::kNumAcc;
-    constexpr int NSF = Cfg::kSfSlots;
+    constexpr int NSF = Cfg::kSfSlots;       // shared-memory scale slots
+    constexpr int NTS = Cfg::kSfTmemSlots;   // TMEM scale slots
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -175,9 +156,10 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     uint64_t *tfull_bar = bars + 2 * R;               // [NUM_ACC] accumulator complete
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] accumulator drained
     uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] scale words landed in smem
-    uint64_t *sf_ready_bar = sf_full_bar + NSF;       // [NSF] scale words copied to TMEM
-    uint64_t *sf_free_bar = sf_ready_bar + NSF;       // [NSF] MMAs done with the scale slot
-    uint64_t *drain_bar = sf_free_bar + NSF;          // [2]  MMA issuer, scale warp
+    uint64_t *sf_sfree_bar = sf_full_bar + NSF;       // [NSF] scale words copied out of the slot
+    uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] scale words in TMEM
+    uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] MMAs done with the TMEM slot
+    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [2]  MMA warp, scale warp
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
@@ -204,8 +186,11 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         }
         for (int j = 0; j < NSF; ++j) {
             mbar_init(&sf_full_bar[j], 1);
+            mbar_init(&sf_sfree_bar[j], 1);
+        }
+        for (int j = 0; j < NTS; ++j) {
             mbar_init(&sf_ready_bar[j], 1);
-            mbar_init(&sf_free_bar[j], 1);
+            mbar_init(&sf_tfree_bar[j], 1);
         }
         mbar_init(&drain_bar[0], 1);
         mbar_init(&drain_bar[1], 1);
@@ -234,58 +219,47 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const int groups_per_tile = psf_k;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int slot = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0;
-            bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
-            GroupCursor<BN> sfc;
-            sfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
-            int gs = 0;          // scale groups issued
-            int ga = 0;          // A/B groups started
-            uint32_t sf_issued = 0;
-            // L2 prefetch cursor, p.prefetch_kb K-blocks ahead of the loads
-            KbCursor<BN> pfc;
-            pfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
-            auto prefetch_one = [&]() {
-                if (!pfc.valid) return;
-                if (p.prefetch_mask & 1)
-                    tma_prefetch_l2_2d(&tm_a, pfc.kb * kBlockK,
-                                       pfc.tile.a_row0 + rank * (kBlockM / csize));
-                if (p.prefetch_mask & 2)
-                    tma_prefetch_l2_2d(&tm_b, pfc.kb * kBlockK, pfc.tile.b_row0);
-                pfc.next();
-            };
-            if (p.prefetch_mask != 0)
-                for (int i = 0; i < p.prefetch_kb; ++i) prefetch_one();
-            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-                Tile tile;
-                if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, true)) continue;
-                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
-                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                    if ((kb0 & 3) == 0) {
-                        // keep the scale words one group ahead of the A/B stream
-                        while (sfc.valid && gs <= ga + 1) {
-                            const int sslot = gs % NSF;
-                            if (!mbar_wait(&sf_free_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                                goto prod_done;
+        // ------------------------------------------------------------ producer (whole warp)
+        int slot = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;
+        bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
+        GroupCursor<BN> sfc;
+        sfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+        int gs = 0;          // scale groups issued
+        int ga = 0;          // A/B groups started
+        uint32_t sf_issued = 0;
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+            Tile tile;
+            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, lane == 0)) continue;
+            for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                if ((kb0 & 3) == 0) {
+                    // keep the scale words kSfLookahead groups ahead of the A/B stream
+                    while (sfc.valid && gs <= ga + Cfg::kSfLookahead) {
+                        const int sslot = gs % NSF;
+                        if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                            goto prod_done;
+                        if (elect_one()) {
                             uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
                             mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
                             tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], sfc.tile.sfa_x,
                                         sfc.tile.sfa_y0 + sfc.j);
                             tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot],
                                         sfc.tile.n0, sfc.tile.sfb_y0 + sfc.j);
-                            sf_issued |= 1u << sslot;
-                            ++gs;
-                            sfc.next();
                         }
-                        ++ga;
+                        __syncwarp();
+                        sf_issued |= 1u << sslot;
+                        ++gs;
+                        sfc.next();
                     }
-                    if (!mbar_wait(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
-                    if (drop) {
-                        drop = false;  // diagnostic: leave this slot empty
-                    } else {
+                    ++ga;
+                }
+                if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
+                if (drop) {
+                    drop = false;  // diagnostic: leave this slot empty
+                } else {
+                    if (elect_one()) {
                         mbar_arrive_expect_tx(&full_bar[slot], nk * Cfg::kStageBytes);
                         auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
@@ -302,7 +276,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                             }
                             tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[slot],
                                         kb * kBlockK, tile.b_row0);
-                            if (p.prefetch_mask != 0 && p.prefetch_kb > 0) prefetch_one();
                         };
                         if (nk == G) {
 #pragma unroll
@@ -310,12 +283,15 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         } else {
                             for (int j = 0; j < nk; ++j) load_kb(j);
                         }
-                        issued |= 1u << slot;
                     }
-                    if (++slot == R) { slot = 0; phase ^= 1; }
+                    __syncwarp();
+                    issued |= 1u << slot;
                 }
+                if (++slot == R) { slot = 0; phase ^= 1; }
             }
-        prod_done:
+        }
+    prod_done:
+        if (lane == 0) {
             // never leave the CTA with loads in flight: wait for the last fill of every buffer
             for (int s = 0; s < R; ++s)
                 if (issued & (1u << s))
@@ -327,38 +303,41 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
                 }
         }
+        __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (one lane)
-        if (lane == 0) {
-            int slot = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            int g = 0;  // scale groups consumed
-            const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
-            const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
-            constexpr uint32_t idesc_base = make_idesc_mxf8(kBlockM, BN, 0, 0);
-            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-                Tile tile;
-                if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
-                if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+        // ------------------------------------------------------------ MMA issuer (whole warp)
+        int slot = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int g = 0;  // scale groups consumed
+        const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
+        const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
+        constexpr uint32_t idesc_base = make_idesc_mxf8(kBlockM, BN, 0, 0);
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+            Tile tile;
+            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
+            if (!mbar_wait_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
+                const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                const int tslot = g % NTS;
+                if ((kb0 & 3) == 0) {
+                    // scale words of this 4-K-block group are in TMEM slot `tslot`
+                    if (!mbar_wait_warp(&sf_ready_bar[tslot], (g / NTS) & 1, ctl, DG_DEV_TIMEOUT))
+                        goto mma_done;
+                }
+                if (!mbar_wait_warp(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
-                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                    const int sslot = g % NSF;
-                    if ((kb0 & 3) == 0) {
-                        // scale words of this 4-K-block group are in TMEM slot `sslot`
-                        if (!mbar_wait(&sf_ready_bar[sslot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
-                            goto mma_done;
-                    }
-                    if (!mbar_wait(&full_bar[slot], phase, ctl, DG_DEV_TIMEOUT)) goto mma_done;
-                    tc_fence_after_sync();
-                    const uint32_t sfa_tmem = tmem_base + sf_col0 + sslot * Cfg::kSfCols;
-                    // descriptors of this slot's first stage; a stage further is a fixed
-                    // address step (>> 4), and the scale byte of K-block kb is kb % 4
-                    const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
-                    const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
+                const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
+                // descriptors of this slot's first stage; a stage further is a fixed
+                // address step (>> 4), and the scale byte of K-block kb is kb % 4
+                const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
+                const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
+                const int kb_last = kb0 + nk - 1;
+                const bool group_end = (kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1;
+                if (elect_one()) {
                     auto mma_kb = [&](int j) {
                         const int kb = kb0 + j;
                         const uint32_t sf = static_cast<uint32_t>(kb & 3);
@@ -378,19 +357,20 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     }
                     if (csize == 1) tc_commit(&empty_bar[slot]);
                     else tc_commit_multicast(&empty_bar[slot], cmask);
-                    const int kb_last = kb0 + nk - 1;
-                    if ((kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1) {
-                        // last K-block of the scale group: its slot is free once these MMAs finish
-                        tc_commit(&sf_free_bar[sslot]);
-                        ++g;
-                    }
-                    if (++slot == R) { slot = 0; phase ^= 1; }
+                    // last K-block of the scale group: its TMEM slot is free once these MMAs finish
+                    if (group_end) tc_commit(&sf_tfree_bar[tslot]);
                 }
-                tc_commit(&tfull_bar[acc]);
-                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+                __syncwarp();
+                if (group_end) ++g;
+                if (++slot == R) { slot = 0; phase ^= 1; }
             }
-        mma_done:
-            // all MMAs this thread issued must finish before TMEM is freed
+            if (elect_one()) tc_commit(&tfull_bar[acc]);
+            __syncwarp();
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+        }
+    mma_done:
+        // all MMAs this warp issued must finish before TMEM is freed
+        if (elect_one()) {
             tc_commit(&drain_bar[0]);
             mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
         }
@@ -398,13 +378,14 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     } else if (warp == Cfg::kSfWarp) {
         // ------------------------------------------------------------ scale-factor warp
         int g = 0;
+        bool copied = false;
         for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
             if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
             for (int j = 0; j < groups_per_tile; ++j, ++g) {
                 const int slot = g % NSF;
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)))
-                    goto sf_done;
+                const int tslot = g % NTS;
+                if (!mbar_wait_warp(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)) goto sf_done;
                 uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
                 uint32_t *sfb_buf = sfa_buf + 128;
                 sf_transpose_for_cp(sfa_buf, lane);
@@ -412,23 +393,26 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                 for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
+                // the MMAs of the TMEM slot's previous group have completed
+                if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                    goto sf_done;
                 if (lane == 0) {
-                    // the slot's previous group was released (sf_free) before its words were
-                    // reloaded, so its MMAs have completed
                     tc_fence_after_sync();
-                    const uint32_t sfa_tmem = tmem_base + sf_col0 + slot * Cfg::kSfCols;
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
                     tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
 #pragma unroll
                     for (int c = 0; c < Cfg::kSfbChunks; ++c)
                         tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c,
                                              make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
-                    tc_commit(&sf_ready_bar[slot]);
+                    tc_commit(&sf_ready_bar[tslot]);
+                    tc_commit(&sf_sfree_bar[slot]);   // the producer may refill the slot
+                    copied = true;
                 }
                 __syncwarp();
             }
         }
     sf_done:
-        if (lane == 0) {
+        if (lane == 0 && copied) {
             tc_commit(&drain_bar[1]);
             mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
         }

@@ -229,14 +229,6 @@ __device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUte
         : "memory");
 }
 
-// Pulls a box into L2 ahead of its use (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cluster address `bar_cluster`).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
