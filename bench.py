@@ -130,6 +130,121 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --------------------------------------------------------------------- other workloads
+
+def _time_launches(fn, flush, reps, stream):
+    """Median device time (ms) of fn() over reps launches, each behind an L2
+    flush, bracketed by CUDA events on the launching stream."""
+    import torch
+    ts = []
+    for r in range(reps):
+        flush.fill_(r)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def measure_other_workloads(dev, flush, reps, stream):
+    """The other workloads of the method, each timed alone (not part of the
+    step): C-accumulate dense GEMM, the two contiguous grouped MoE shapes and
+    the masked grouped decode shape.  Inputs are drawn and quantised on the
+    GPU (same recipe as the parity tests, another random stream)."""
+    import torch
+
+    from block_scaled_fp8_gb300 import binding, inputs
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = []
+
+    def record(name, fn, fl, by, extra):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ms = _time_launches(fn, flush, reps, stream)
+        cfg = binding.last_config()
+        out.append({"workload": name, "us": round(ms * 1e3, 2),
+                    "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                    "gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                    "block_m": cfg["block_m"], "block_n": cfg["block_n"], **extra})
+
+    # dense with C accumulate, B block-scale exponents spread over 2^-8..2^4
+    m, n, k = 4096, 7168, 2048
+    c_ = inputs.dense_case(m, n, k, seed=2, with_c=True, b_scale_exp_range=(-8, 4), device=dev)
+    sfa = binding.transform_sf(c_.sfa, 1, m)
+    sfb = binding.transform_sf(c_.sfb, 128, n)
+    d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    record(f"dense NT + C {m}x{n}x{k}",
+           lambda: binding.dg_fp8_gemm_nt(c_.a, sfa, c_.b, sfb, d, c=c_.c, status=status),
+           flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {})
+    del c_, sfa, sfb, d
+
+    # contiguous grouped: 8 experts, M_e ~ U[128, 4096] padded to 128
+    for (n, k) in ((4096, 7168), (7168, 2048)):
+        cc = inputs.contiguous_case(8, n, k, seed=3, device=dev)
+        mt = cc.a.shape[0]
+        sfa = binding.transform_sf(cc.sfa, 1, mt)
+        sfb = binding.transform_sf(cc.sfb, 128, n)
+        d = torch.empty(mt, n, dtype=torch.bfloat16, device=dev)
+        valid = sum(cc.m_per_expert)
+        used = sum(1 for v in cc.m_per_expert if v)
+        record(f"m-grouped contiguous 8 experts N={n} K={k}",
+               lambda: binding.dg_m_grouped_fp8_gemm_nt_contiguous(cc.a, sfa, cc.b, sfb, d,
+                                                                   cc.grouped_layout,
+                                                                   status=status),
+               flops(valid, n, k), valid * k + used * n * k + 2 * valid * n,
+               {"valid_rows": valid, "rows": mt})
+        del cc, sfa, sfb, d
+
+    # masked grouped decode: 32 experts, max_m 256
+    n, k, e, max_m = 4096, 7168, 32, 256
+    mc = inputs.masked_case(e, max_m, n, k, seed=4, device=dev)
+    sfa = binding.transform_sf(mc.sfa, 1, max_m)
+    sfb = binding.transform_sf(mc.sfb, 128, n)
+    d = torch.empty(e, max_m, n, dtype=torch.bfloat16, device=dev)
+    valid = int(mc.masked_m.sum())
+    used = int((mc.masked_m > 0).sum())
+    record(f"m-grouped masked {e} experts max_m={max_m} N={n} K={k}",
+           lambda: binding.dg_m_grouped_fp8_gemm_nt_masked(mc.a, sfa, mc.b, sfb, d, mc.masked_m,
+                                                           mc.expected_m, status=status),
+           flops(valid, n, k), valid * k + used * n * k + 2 * valid * n,
+           {"valid_rows": valid, "bound": "hbm"})
+    del mc, sfa, sfb, d
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the other workloads")
+    return out
+
+
+def measure_library_fp8_peak(dev, stream):
+    """Context only: a library FP8 matmul (torch._scaled_mm, per-tensor scales)
+    at 8192^3, the best of 10 back-to-back runs."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+    except Exception as exc:  # the library may not offer an FP8 GEMM here
+        return f"unavailable: {type(exc).__name__}"
+
+
 # --------------------------------------------------------------------- ours
 
 def run_ours(args, rank, world, local_rank):
@@ -260,8 +375,16 @@ def run_ours(args, rank, world, local_rank):
 
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_TFLOPS / NOMINAL_BF16_TFLOPS
-    gemm_total_ms = sum(gemm_ms)
-    achieved = step_flops / (gemm_total_ms * 1e-3) / 1e12
+    # The dominant kernel is the CTA-pair kernel of the three M=4096 GEMMs
+    # (tensor-bound); the three M=128 GEMMs run the single-CTA kernel (HBM-bound).
+    big = [i for i, p in enumerate(probs) if p["shape"][0] > 128]
+    skinny = [i for i, p in enumerate(probs) if p["shape"][0] <= 128]
+    big_ms = sum(gemm_ms[i] for i in big)
+    achieved = sum(flops(*probs[i]["shape"]) for i in big) / (big_ms * 1e-3) / 1e12
+    skinny_ms = sum(gemm_ms[i] for i in skinny)
+    skinny_gbs = sum(gemm_bytes(*probs[i]["shape"]) for i in skinny) / (skinny_ms * 1e-3) / 1e9
+    other = measure_other_workloads(dev, flush, max(5, args.steps // 4), stream) if rank == 0 else []
+    lib_fp8 = measure_library_fp8_peak(dev, stream) if rank == 0 else None
     per_gemm = []
     for p, ms, cfg in zip(probs, gemm_ms, bn_used):
         m, n, k = p["shape"]
@@ -270,6 +393,10 @@ def run_ours(args, rank, world, local_rank):
                          "gbs": round(gemm_bytes(m, n, k) / (ms * 1e-3) / 1e9, 1),
                          "block_n": cfg["block_n"], "grid": cfg["grid"]})
     traffic = load_traffic()
+    big_traffic = skinny_traffic = None
+    if traffic is not None:
+        big_traffic = traffic.get("dg_bs2_gemm_kernel")
+        skinny_traffic = traffic.get("dg_bs_gemm_kernel")
 
     result = None
     if rank == 0:
@@ -289,9 +416,18 @@ def run_ours(args, rank, world, local_rank):
                          "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                          "frac": round(achieved / fp8_peak, 4),
                          "peak_note": f"fp8 = {peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio), of {peaks['source']}",
-                         "kernel": "dg_bs_gemm_kernel (sum over the six GEMMs of the step)",
-                         "traffic": None if traffic is None else traffic.get("bytes_per_step")},
+                         "kernel": "dg_bs2_gemm_kernel (CTA pairs): the three M=4096 GEMMs, "
+                                   "flops / summed launch time",
+                         "traffic": big_traffic},
+            "roofline_skinny": {"bound": "hbm", "achieved": round(skinny_gbs, 1),
+                                "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
+                                "frac": round(skinny_gbs / peaks["hbm_gbs"], 4),
+                                "kernel": "dg_bs_gemm_kernel: the three M=128 GEMMs, algorithmic "
+                                          "bytes / summed launch time, of " + peaks["source"],
+                                "traffic": skinny_traffic},
             "per_gemm": per_gemm,
+            "other_workloads": other,
+            "library_fp8_matmul_8192_tflops": lib_fp8,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

@@ -98,10 +98,15 @@ constexpr int kMaxBlockNWithC = 160;
 // never used: with few M blocks, narrow BLOCK_N is what fills the SMs (the
 // non-power-of-two block idea of PaperTrace §4.3).
 int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c) {
+    static const int forced_bn = [] {
+        const char *e = std::getenv("DG_BLOCK_N");
+        return e ? std::atoi(e) : 0;
+    }();
     double best = -1.0;
     int best_bn = 128;
     for (int bn : kBsBlockN) {
         if (with_c && bn > kMaxBlockNWithC) continue;
+        if (forced_bn && bn != forced_bn) continue;
         const int64_t nb = cdiv64(n, bn);
         const int64_t tiles = m_blocks * nb;
         const int64_t waves = cdiv64(tiles, num_sms);

@@ -29,8 +29,8 @@ def cdiv(a: int, b: int) -> int:
     return (a + b - 1) // b
 
 
-def generator(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def generator(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
@@ -70,7 +70,7 @@ def quantize_128x128(w: torch.Tensor):
 
 def random_finite_e4m3(shape, g: torch.Generator) -> torch.Tensor:
     """Uniformly random E4M3fn codes, NaN codes (0x7f, 0xff) excluded."""
-    codes = torch.randint(0, 254, shape, generator=g, dtype=torch.int32)
+    codes = torch.randint(0, 254, shape, generator=g, dtype=torch.int32, device=g.device)
     codes = codes + (codes >= 0x7f).int()          # skip 0x7f; 0xff is never reached
     return codes.to(torch.uint8).view(torch.float8_e4m3fn)
 
@@ -91,24 +91,27 @@ class DenseCase:
 
 
 def dense_case(M: int, N: int, K: int, seed: int = 0, with_c: bool = False,
-               b_scale_exp_range: tuple[int, int] | None = None) -> DenseCase:
+               b_scale_exp_range: tuple[int, int] | None = None, device="cpu") -> DenseCase:
     """Dense NT problem: A, B from N(0,1) quantised per 1x128 / 128x128.
 
     b_scale_exp_range=(lo, hi) replaces every B block scale by 2^u with u a
     uniform integer in [lo, hi] (the C-accumulate workload's spread of weight
-    scale exponents over 2^-8..2^4)."""
-    g = generator(seed)
-    x = torch.randn(M, K, generator=g, dtype=torch.float32)
-    w = torch.randn(N, K, generator=g, dtype=torch.float32)
+    scale exponents over 2^-8..2^4).  device="cuda" draws and quantises on the
+    GPU (a different random stream, same recipe): for workload-sized timing
+    inputs whose values no test compares."""
+    g = generator(seed, device)
+    x = torch.randn(M, K, generator=g, dtype=torch.float32, device=device)
+    w = torch.randn(N, K, generator=g, dtype=torch.float32, device=device)
     a, sfa = quantize_1x128(x)
     del x
     b, sfb = quantize_128x128(w)
     del w
     if b_scale_exp_range is not None:
         lo, hi = b_scale_exp_range
-        u = torch.randint(lo, hi + 1, sfb.shape, generator=g, dtype=torch.int64)
-        sfb = torch.ldexp(torch.ones(sfb.shape, dtype=torch.float64), u).float()
-    c = torch.randn(M, N, generator=g, dtype=torch.float32).to(torch.bfloat16) if with_c else None
+        u = torch.randint(lo, hi + 1, sfb.shape, generator=g, dtype=torch.int64, device=device)
+        sfb = torch.ldexp(torch.ones(sfb.shape, dtype=torch.float64, device=device), u).float()
+    c = (torch.randn(M, N, generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+         if with_c else None)
     return DenseCase(a, sfa, b, sfb, c, {"M": M, "N": N, "K": K, "seed": seed})
 
 
@@ -144,28 +147,30 @@ class ContiguousCase:
 
 def contiguous_case(num_groups: int, N: int, K: int, seed: int = 0, m_lo: int = 128,
                     m_hi: int = 4096, align: int = 128,
-                    m_per_expert: list[int] | None = None) -> ContiguousCase:
-    g = generator(seed)
+                    m_per_expert: list[int] | None = None, device="cpu") -> ContiguousCase:
+    g = generator(seed, device)
     if m_per_expert is None:
-        m_per_expert = [int(v) for v in torch.randint(m_lo, m_hi + 1, (num_groups,), generator=g)]
+        m_per_expert = [int(v) for v in torch.randint(m_lo, m_hi + 1, (num_groups,), generator=g,
+                                                      device=device)]
     padded = [cdiv(m, align) * align for m in m_per_expert]
     M_total = sum(padded)
     sf_k = cdiv(K, GRAN)
-    a = torch.zeros(M_total, K, dtype=torch.float8_e4m3fn)
-    sfa = torch.ones(M_total, sf_k, dtype=torch.float32)
-    layout = torch.full((M_total,), -1, dtype=torch.int32)
+    a = torch.zeros(M_total, K, dtype=torch.float8_e4m3fn, device=device)
+    sfa = torch.ones(M_total, sf_k, dtype=torch.float32, device=device)
+    layout = torch.full((M_total,), -1, dtype=torch.int32, device=device)
     row = 0
     for e, (m, mp) in enumerate(zip(m_per_expert, padded)):
         if m:
-            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32))
+            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32, device=device))
             a[row:row + m] = q
             sfa[row:row + m] = s
             layout[row:row + m] = e
         row += mp
-    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn)
-    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32)
+    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn, device=device)
+    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32, device=device)
     for e in range(num_groups):
-        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32))
+        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32,
+                                                    device=device))
     return ContiguousCase(a, sfa, b, sfb, layout, m_per_expert,
                           {"E": num_groups, "N": N, "K": K, "M_total": M_total, "seed": seed})
 
@@ -183,28 +188,30 @@ class MaskedCase:
 
 
 def masked_case(num_groups: int, max_m: int, N: int, K: int, seed: int = 0,
-                masked_m: list[int] | None = None) -> MaskedCase:
+                masked_m: list[int] | None = None, device="cpu") -> MaskedCase:
     """Valid rows per expert uniform in [0, max_m]; rows past masked_m[e] hold
     random finite codes and random scales (they must not affect anything)."""
-    g = generator(seed)
+    g = generator(seed, device)
     if masked_m is None:
-        mm = torch.randint(0, max_m + 1, (num_groups,), generator=g, dtype=torch.int32)
+        mm = torch.randint(0, max_m + 1, (num_groups,), generator=g, dtype=torch.int32, device=device)
     else:
-        mm = torch.tensor(masked_m, dtype=torch.int32)
+        mm = torch.tensor(masked_m, dtype=torch.int32, device=device)
     sf_k = cdiv(K, GRAN)
     a = random_finite_e4m3((num_groups, max_m, K), g)
-    sfa = torch.ldexp(torch.ones(num_groups, max_m, sf_k, dtype=torch.float64),
-                      torch.randint(-10, 4, (num_groups, max_m, sf_k), generator=g)).float()
+    sfa = torch.ldexp(torch.ones(num_groups, max_m, sf_k, dtype=torch.float64, device=device),
+                      torch.randint(-10, 4, (num_groups, max_m, sf_k), generator=g,
+                                    device=device)).float()
     for e in range(num_groups):
         m = int(mm[e])
         if m:
-            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32))
+            q, s = quantize_1x128(torch.randn(m, K, generator=g, dtype=torch.float32, device=device))
             a[e, :m] = q
             sfa[e, :m] = s
-    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn)
-    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32)
+    b = torch.empty(num_groups, N, K, dtype=torch.float8_e4m3fn, device=device)
+    sfb = torch.empty(num_groups, cdiv(N, GRAN), sf_k, dtype=torch.float32, device=device)
     for e in range(num_groups):
-        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32))
+        b[e], sfb[e] = quantize_128x128(torch.randn(N, K, generator=g, dtype=torch.float32,
+                                                    device=device))
     expected_m = max(1, math.ceil(float(mm.float().mean())))
     return MaskedCase(a, sfa, b, sfb, mm, expected_m,
                       {"E": num_groups, "max_m": max_m, "N": N, "K": K, "seed": seed})
