@@ -64,7 +64,7 @@ cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams
 int bs_max_active_clusters(int block_n, bool with_c, int cluster);
 
 // CTA-pair (cta_group::2) block-scaled kernel family, dense layout: 256 x BLOCK_N
-// tiles, BLOCK_N in {128, 192, 224, 240, 256} (128 only with C).
+// tiles, BLOCK_N in {128, 192, 224, 240, 256} (up to 240 with C).
 bool get_bs2_kernel_info(int block_n, bool with_c, KernelInfo *info);
 cudaError_t launch_bs2_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream);

@@ -389,69 +389,40 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         uint32_t acc_phase = 0;
         uint32_t buf = 0;
         uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
-        for (int t = pair_id; t < num_tiles; t += num_pairs) {
-            PairTile tile;
-            get_pair_tile<BN>(p, t, rank, tile);
-            const int row = tile.a_row0 + quad * 32 + lane;
-            const bool row_ok = row < p.rows;
-            uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
+        // C (bf16) of one chunk of this thread's row; zero outside [rows, n)
+        auto load_c = [&](const PairTile &tl, int j, uint32_t (&dst)[8]) {
+            const int c = 2 * j + half;
+            const int row = tl.a_row0 + quad * 32 + lane;
+            const int col0 = tl.n0 + c * Cfg::kEpiChunk;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+                if (c < Cfg::kNumChunks && row < p.rows && col0 + 8 * h < p.n)
+                    cv = __ldg(reinterpret_cast<const uint4 *>(p.c + static_cast<int64_t>(row) * p.ldc +
+                                                               col0 + 8 * h));
+                dst[4 * h + 0] = cv.x;
+                dst[4 * h + 1] = cv.y;
+                dst[4 * h + 2] = cv.z;
+                dst[4 * h + 3] = cv.w;
+            }
+        };
+        // With C, each chunk's registers are refilled with the next tile's C as soon
+        // as this tile's chunk is stored, so the C loads run a whole tile ahead.
+        uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
+        PairTile tile;
+        if (pair_id < num_tiles) {
+            get_pair_tile<BN>(p, pair_id, rank, tile);
             if constexpr (WITH_C) {
 #pragma unroll
-                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
-                    const int c = 2 * j + half;
-                    const int col0 = tile.n0 + c * Cfg::kEpiChunk;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 cv = make_uint4(0u, 0u, 0u, 0u);
-                        if (c < Cfg::kNumChunks && row_ok && col0 + 8 * h < p.n)
-                            cv = __ldg(reinterpret_cast<const uint4 *>(
-                                p.c + static_cast<int64_t>(row) * p.ldc + col0 + 8 * h));
-                        cpk[j][4 * h + 0] = cv.x;
-                        cpk[j][4 * h + 1] = cv.y;
-                        cpk[j][4 * h + 2] = cv.z;
-                        cpk[j][4 * h + 3] = cv.w;
-                    }
-                }
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
             }
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
-            tc_fence_after_sync();
-            uint32_t out[Cfg::kChunksPerWarp][8];
-#pragma unroll
-            for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
-                uint32_t v[2][16];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int c = 2 * (j0 + u) + half;
-                    if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
-                        tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (j0 + u >= Cfg::kChunksPerWarp) continue;
-                    reg_fence16(v[u]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float lo = __uint_as_float(v[u][2 * i]);
-                        float hi = __uint_as_float(v[u][2 * i + 1]);
-                        if constexpr (WITH_C) {
-                            lo += __uint_as_float(cpk[j0 + u][i] << 16);
-                            hi += __uint_as_float(cpk[j0 + u][i] & 0xFFFF0000u);
-                        }
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                        out[j0 + u][i] = *reinterpret_cast<uint32_t *>(&b2);
-                    }
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
-            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
-
-#pragma unroll
-            for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
-                const int c = 2 * j + half;
-                if (c >= Cfg::kNumChunks) continue;
+        }
+        for (int t = pair_id; t < num_tiles; t += num_pairs) {
+            const bool has_next = t + num_pairs < num_tiles;
+            PairTile next_tile = tile;
+            if (has_next) get_pair_tile<BN>(p, t + num_pairs, rank, next_tile);
+            // bf16 chunk (16 columns of this thread's row) -> swizzled staging -> TMA store
+            auto store_chunk = [&](const uint32_t (&o)[8], int c) {
                 const int col0 = tile.n0 + c * Cfg::kEpiChunk;
                 uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
                 if (lane == 0) bulk_wait_group_read<1>();
@@ -459,8 +430,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t off = lane * 32 + ((h ^ ((lane >> 2) & 1)) * 16);
-                    *reinterpret_cast<uint4 *>(sbuf + off) =
-                        make_uint4(out[j][4 * h], out[j][4 * h + 1], out[j][4 * h + 2], out[j][4 * h + 3]);
+                    *reinterpret_cast<uint4 *>(sbuf + off) = make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -469,7 +439,81 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                     bulk_commit_group();
                 }
                 buf ^= 1;
+            };
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
+            tc_fence_after_sync();
+            if constexpr (WITH_C) {
+                // C is held as bf16 (prefetched above), so the FP32 accumulator stays in
+                // TMEM until each chunk is converted and stored; the other accumulator
+                // keeps the MMAs busy meanwhile
+#pragma unroll
+                for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
+                    uint32_t v[2][16];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = 2 * (j0 + u) + half;
+                        if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
+                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int j = j0 + u;
+                        const int c = 2 * j + half;
+                        if (j >= Cfg::kChunksPerWarp || c >= Cfg::kNumChunks) continue;
+                        reg_fence16(v[u]);
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float lo = __uint_as_float(v[u][2 * i]) + __uint_as_float(cpk[j][i] << 16);
+                            const float hi = __uint_as_float(v[u][2 * i + 1]) + __uint_as_float(cpk[j][i] & 0xFFFF0000u);
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                            o[i] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        store_chunk(o, c);
+                        if (has_next) load_c(next_tile, j, cpk[j]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+            } else {
+                // the whole row segment to registers, release the accumulator, then store
+                uint32_t out[Cfg::kChunksPerWarp][8];
+#pragma unroll
+                for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
+                    uint32_t v[2][16];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = 2 * (j0 + u) + half;
+                        if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
+                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (j0 + u >= Cfg::kChunksPerWarp) continue;
+                        reg_fence16(v[u]);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[u][2 * i]),
+                                                                      __uint_as_float(v[u][2 * i + 1]));
+                            out[j0 + u][i] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+#pragma unroll
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                    const int c = 2 * j + half;
+                    if (c < Cfg::kNumChunks) store_chunk(out[j], c);
+                }
             }
+            tile = next_tile;
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -20,7 +20,9 @@ DG_BS_BLOCK_N_LIST(DG_EXTERN)
 DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #undef DG_EXTERN
 
-#define DG_BS2_LIST(X) X(128, false) X(128, true) X(192, false) X(224, false) X(240, false) X(256, false)
+#define DG_BS2_LIST(X) \
+    X(128, false) X(128, true) X(192, false) X(192, true) X(224, false) X(224, true) X(240, false) \
+    X(240, true) X(256, false)
 #define DG_EXTERN2(BN, C)                                                                        \
     extern template cudaError_t launch_bs2_gemm_impl<BN, C>(const TensorMaps &, const GemmParams &, \
                                                             int, cudaStream_t);                      \
