@@ -88,6 +88,25 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, cons
     return r == CUDA_SUCCESS;
 }
 
+// K-blocked 3-D view of a K-contiguous FP8 operand [rows][ld]: x = K within a
+// 128-K block, y = row, z = K-block (stride 128 bytes).  A box {128, box_rows,
+// depth} loads `depth` consecutive K-blocks as consecutive 128B-swizzled
+// [box_rows][128] slabs, i.e. the stages of one ring slot.  Valid only when K
+// is a multiple of 128 (x never runs past K inside a block).
+bool encode_kblocked_3d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t ld_bytes,
+                        uint64_t k_blocks, uint32_t box_rows, uint32_t depth) {
+    EncodeTiledFn enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBlockK), rows, k_blocks};
+    cuuint64_t strides[2] = {ld_bytes, static_cast<cuuint64_t>(kBlockK)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, depth};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Block-N values compiled into the block-scaled kernel family.
 constexpr int kBsBlockN[] = {16, 32, 48, 64, 96, 128, 160, 176, 192, 224, 256};
 constexpr int kMaxBlockNWithC = 160;
@@ -217,10 +236,18 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
-    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                    kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
-                    bn / 2, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    // K a multiple of 128: one 3-D load per operand fills a ring slot
+    p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
+    if (p.ab_3d) {
+        const uint64_t kblocks = static_cast<uint64_t>(k / kBlockK);
+        ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, kBlockM, info.group_kb);
+        ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, bn / 2, info.group_kb);
+    } else {
+        ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
+                        kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
+                        bn / 2, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
     ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
                     align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE);
@@ -278,11 +305,19 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
-    // each CTA of a cluster loads (and multicasts) kBlockM / cluster rows of A
-    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                    kBlockM / cluster, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    // K a multiple of 128 and no A multicast: one 3-D load per operand fills a ring slot
+    p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1 && cluster == 1) ? 1 : 0;
+    if (p.ab_3d) {
+        const uint64_t kblocks = static_cast<uint64_t>(k / kBlockK);
+        ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, kBlockM, info.group_kb);
+        ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, bn, info.group_kb);
+    } else {
+        // each CTA of a cluster loads (and multicasts) kBlockM / cluster rows of A
+        ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
+                        kBlockM / cluster, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    }
     ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
                     align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE);

@@ -37,6 +37,7 @@ struct GemmParams {
     int32_t *status;
     uint64_t timeout_ns;
     uint32_t debug_flags;
+    int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
     // FP32-promotion kernel only
     const float *sfa_f32;   // [rows][sf_k]
     const float *sfb_f32;   // [ceil(n/128)][sf_k]
@@ -53,6 +54,7 @@ struct KernelInfo {
     int stages;
     int smem_bytes;
     int threads;
+    int group_kb;   // K-blocks per ring slot (the depth of a 3-D A/B load)
 };
 
 // Block-scaled (UE8M0) tcgen05 kernel family: returns false if block_n is not

@@ -259,7 +259,17 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                 if (drop) {
                     drop = false;  // diagnostic: leave this slot empty
                 } else {
-                    if (elect_one()) {
+                    if (p.ab_3d) {
+                        // one load per operand fills the slot's G stages; K-blocks past the
+                        // end of K are out of bounds (zero-filled) and still count their bytes
+                        if (elect_one()) {
+                            mbar_arrive_expect_tx(&full_bar[slot], G * Cfg::kStageBytes);
+                            tma_load_3d(smem_a + slot * G * Cfg::kABytes, &tm_a, &full_bar[slot], 0,
+                                        tile.a_row0, kb0);
+                            tma_load_3d(smem_b + slot * G * Cfg::kBBytes, &tm_b, &full_bar[slot], 0,
+                                        tile.b_row0, kb0);
+                        }
+                    } else if (elect_one()) {
                         mbar_arrive_expect_tx(&full_bar[slot], nk * Cfg::kStageBytes);
                         auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
@@ -602,6 +612,7 @@ void fill_bs_info(KernelInfo *info) {
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
+    info->group_kb = Cfg::kGroupKb;
 }
 
 }  // namespace dg

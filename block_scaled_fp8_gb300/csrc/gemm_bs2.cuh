@@ -230,7 +230,15 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                     drop = false;  // diagnostic: leave this slot empty
                 } else {
                     const uint32_t fb = leader_full + slot * 8;
-                    if (elect_one()) {
+                    if (p.ab_3d) {
+                        // one load per operand fills the slot's G stages; K-blocks past the
+                        // end of K are out of bounds (zero-filled) and still count their bytes
+                        if (elect_one()) {
+                            if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * G * Cfg::kStageBytes);
+                            tma_load_3d_pair(smem_a + slot * G * Cfg::kABytes, &tm_a, fb, 0, tile.a_row0, kb0);
+                            tma_load_3d_pair(smem_b + slot * G * Cfg::kBBytes, &tm_b, fb, 0, tile.b_row0, kb0);
+                        }
+                    } else if (elect_one()) {
                         // the leader expects both CTAs' bytes; each CTA's loads count there
                         if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kStageBytes);
                         auto load_kb = [&](int j) {
@@ -571,6 +579,7 @@ void fill_bs2_info(KernelInfo *info) {
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
+    info->group_kb = Cfg::kGroupKb;
 }
 
 }  // namespace dg

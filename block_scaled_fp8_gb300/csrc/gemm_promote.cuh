@@ -297,6 +297,7 @@ void fill_promote_info(KernelInfo *info) {
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
+    info->group_kb = 1;
 }
 
 }  // namespace dg

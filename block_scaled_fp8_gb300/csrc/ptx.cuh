@@ -240,6 +240,29 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// 3-D tiled load: box {x extent, y extent, z extent} lands as z slabs of y rows.
+// With the K-blocked operand view (x = K within a 128-K block, y = row, z =
+// K-block) one load fills the consecutive stages of a ring slot.
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// As tma_load_3d, completing on an mbarrier given by its cluster address
+// (the leader CTA's barrier in a CTA pair).
+__device__ __forceinline__ void tma_load_3d_pair(void *smem_dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src,
                                              int32_t x, int32_t y) {
     asm volatile(
