@@ -192,21 +192,27 @@ bool use_pair_kernel(const GemmParams &p) {
     return !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA) && p.mode == kModeDense && p.rows > kBlockM;
 }
 
-int cached_max_pairs(int bn, bool with_c) {
+int cached_max_pairs(int bn, bool with_c, int mp) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][257];
+    static int cache[kMaxDevices][2][2][257];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn > 256) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][bn];
-    if (v == 0) v = bs2_max_active_pairs(bn, with_c);
+    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp);
     return v;
 }
 
-dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStream_t stream) {
-    const bool with_c = p.c != nullptr;
+int usable_pairs(int bn, bool with_c, int mp, int num_sms) {
+    int pairs = cached_max_pairs(bn, with_c, mp);
+    if (pairs * 2 > num_sms) pairs = num_sms / 2;
+    return pairs;
+}
+
+// BLOCK_N of the 256-row pair kernel: the score of choose_block_n over the
+// co-resident pairs (DG_PAIR_BLOCK_N forces one).
+int choose_pair_block_n(const GemmParams &p, bool with_c, int num_sms) {
     const int64_t m_pairs = cdiv64(p.rows, 2 * kBlockM);
-    // same score as choose_block_n, over the co-resident pairs
     int bn = 0;
     double best = -1.0;
     static const int forced_bn = [] {
@@ -216,10 +222,9 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     for (int cand : {128, 192, 224, 240, 256}) {
         if (forced_bn && cand != forced_bn) continue;
         KernelInfo ki;
-        if (!get_bs2_kernel_info(cand, with_c, &ki)) continue;
-        int pairs = cached_max_pairs(cand, with_c);
+        if (!get_bs2_kernel_info(cand, with_c, 256, &ki)) continue;
+        const int pairs = usable_pairs(cand, with_c, 256, num_sms);
         if (pairs <= 0) continue;
-        if (pairs * 2 > num_sms) pairs = num_sms / 2;
         const int64_t nb = cdiv64(p.n, cand);
         const int64_t tiles = m_pairs * nb;
         const int64_t waves = cdiv64(tiles, pairs);
@@ -228,11 +233,43 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
                              (cand / (cand + 64.0));
         if (score > best + 1e-9) { best = score; bn = cand; }
     }
-    if (bn == 0) return DG_ERR_UNSUPPORTED;
+    return bn;
+}
+
+// Skinny dense problems (one 128-row block, no C): the single-CTA kernel with
+// BLOCK_N bn1, or the 128-row pair kernel, whose CTAs load 64 rows of A each.
+// With one row block every CTA re-reads the same A tile, and a CTA's loads are
+// capped at about 60 bytes per cycle, so the time of a K-block is modelled as
+// max(bytes a CTA loads / 60, MMA cycles) times the waves of tiles.  Returns
+// the pair kernel's BLOCK_N, or 0 to keep the single-CTA kernel.
+int choose_skinny_pair_block_n(const GemmParams &p, int bn1, int num_sms) {
+    auto cost = [](int64_t waves, double bytes, double mma) {
+        return static_cast<double>(waves) * (bytes / 60.0 > mma ? bytes / 60.0 : mma);
+    };
+    const double mma1 = 2.0 * bn1 > 200.0 ? 2.0 * bn1 : 200.0;
+    const double cost1 = cost(cdiv64(cdiv64(p.n, bn1), num_sms), kBlockM * kBlockK + bn1 * kBlockK, mma1);
+    int best_bn = 0;
+    double best = cost1 * 0.95;   // switch only for a clear gain
+    for (int cand : {32, 64, 96, 128}) {
+        const int pairs = usable_pairs(cand, false, 128, num_sms);
+        if (pairs <= 0) continue;
+        const double mma2 = cand > 200 ? cand : 200.0;
+        const double c = cost(cdiv64(cdiv64(p.n, cand), pairs), kBlockM / 2 * kBlockK + cand / 2 * kBlockK, mma2);
+        if (c < best) { best = c; best_bn = cand; }
+    }
+    return best_bn;
+}
+
+// One launch of the pair kernel with mp rows per pair tile and BLOCK_N bn.
+dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int num_sms,
+                      cudaStream_t stream) {
+    const bool with_c = p.c != nullptr;
     KernelInfo info;
-    get_bs2_kernel_info(bn, with_c, &info);
-    int pairs = cached_max_pairs(bn, with_c);
-    if (pairs * 2 > num_sms) pairs = num_sms / 2;
+    if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info)) return DG_ERR_UNSUPPORTED;
+    const int pairs = usable_pairs(bn, with_c, mp, num_sms);
+    if (pairs <= 0) return DG_ERR_UNSUPPORTED;
+    const int64_t m_units = cdiv64(p.rows, mp);
+    const uint32_t a_rows = static_cast<uint32_t>(mp / 2);   // rows of A each CTA loads
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
@@ -240,16 +277,16 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
     if (p.ab_3d) {
         const uint64_t kblocks = static_cast<uint64_t>(k / kBlockK);
-        ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, kBlockM, info.group_kb);
+        ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, a_rows, info.group_kb);
         ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, bn / 2, info.group_kb);
     } else {
         ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                        kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                        a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
                         bn / 2, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
-                    align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    align4(o.sfa_mn) * 4, a_rows, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE);
     ok &= encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfb, o.sfb_mn, o.sfb_slices,
                     align4(o.sfb_mn) * 4, bn, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -257,7 +294,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                     32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
-    p.num_m_blocks = static_cast<int>(m_pairs);     // the pair kernel counts 256-row blocks
+    p.num_m_blocks = static_cast<int>(m_units);     // the pair kernel counts mp-row units
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
     p.cluster = 2;
@@ -269,27 +306,33 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int num_sms, cudaStrea
     uint32_t dbg = g_debug_flags.load();
     if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
     p.debug_flags = dbg;
-    const int64_t tiles = m_pairs * p.num_n_blocks;
+    const int64_t tiles = m_units * p.num_n_blocks;
     const int64_t used = tiles < pairs ? tiles : pairs;
     const int grid = static_cast<int>(2 * used);
     if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
-        std::fprintf(stderr, "[dg] pair rows=%d n=%d k=%d -> BLOCK_M=256 BLOCK_N=%d stages=%d smem=%d grid=%d\n",
-                     p.rows, p.n, k, bn, info.stages, info.smem_bytes, grid);
-    g_last_config[0] = 2 * kBlockM;
+        std::fprintf(stderr, "[dg] pair rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d grid=%d\n",
+                     p.rows, p.n, k, mp, bn, info.stages, info.smem_bytes, grid);
+    g_last_config[0] = mp;
     g_last_config[1] = bn;
     g_last_config[2] = info.stages;
     g_last_config[3] = grid;
     g_last_config[4] = 2;
     g_last_config[5] = 1;
-    cudaError_t e = launch_bs2_gemm(bn, maps, p, grid, stream);
+    cudaError_t e = launch_bs2_gemm(bn, mp, maps, p, grid, stream);
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
 dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_blocks_hint,
                               int64_t max_tiles_per_n_block, int num_sms, cudaStream_t stream) {
-    if (use_pair_kernel(p)) return launch_pair(p, o, num_sms, stream);
+    if (use_pair_kernel(p))
+        return launch_pair(p, o, 256, choose_pair_block_n(p, p.c != nullptr, num_sms), num_sms, stream);
     const bool with_c = p.c != nullptr;
     const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
+    if (p.mode == kModeDense && !with_c && p.rows <= kBlockM &&
+        !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA)) {
+        const int bn2 = choose_skinny_pair_block_n(p, bn, num_sms);
+        if (bn2 > 0) return launch_pair(p, o, 128, bn2, num_sms, stream);
+    }
     KernelInfo info;
     if (!get_bs_kernel_info(bn, with_c, &info)) return DG_ERR_UNSUPPORTED;
     int cluster = choose_cluster(cdiv64(p.n, bn));

@@ -65,12 +65,13 @@ cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams
 // Largest number of co-resident clusters of `cluster` CTAs for that kernel (0 on error).
 int bs_max_active_clusters(int block_n, bool with_c, int cluster);
 
-// CTA-pair (cta_group::2) block-scaled kernel family, dense layout: 256 x BLOCK_N
-// tiles, BLOCK_N in {128, 192, 224, 240, 256} (up to 240 with C).
-bool get_bs2_kernel_info(int block_n, bool with_c, KernelInfo *info);
-cudaError_t launch_bs2_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+// CTA-pair (cta_group::2) block-scaled kernel family, dense layout.  mp = rows
+// of a pair tile: 256 (BLOCK_N in {128, 192, 224, 240, 256}, up to 240 with C)
+// or 128 (BLOCK_N in {32, 64, 96, 128}, no C).
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info);
+cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream);
-int bs2_max_active_pairs(int block_n, bool with_c);
+int bs2_max_active_pairs(int block_n, bool with_c, int mp);
 
 // FP32-scale promotion kernel family.
 bool get_promote_kernel_info(int block_n, KernelInfo *info);

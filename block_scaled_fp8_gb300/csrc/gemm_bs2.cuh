@@ -29,15 +29,26 @@
 
 namespace dg {
 
-template <int BN>
+// MP = rows of a pair tile: 256 (each CTA 128 rows; D in TMEM lanes 0-127, BN
+// columns) or 128 (each CTA 64 rows; TMEM lanes 0-63 hold D columns [0, BN/2)
+// and lanes 64-127 columns [BN/2, BN) of the same 64 rows, so an accumulator is
+// BN/2 columns wide).
+template <int BN, int MP = 256>
 struct Bs2Config {
-    // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; M=256 MMAs take N % 16 == 0, N <= 256
-    static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "BN/2 rows of B per CTA, N <= 256");
+    // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
+    // with MP=128 each half of N is whole 16-column epilogue chunks
+    static_assert(MP == 256 || MP == 128, "pair tile rows");
+    static_assert(MP == 256 ? (BN % 16 == 0 && BN >= 64) : (BN % 32 == 0 && BN >= 32), "tile columns");
+    static_assert(BN <= 256, "N <= 256");
     static constexpr int kThreads = 352;
     static constexpr int kEpiWarps = 8;
     static constexpr int kSfWarp = 10;
-    static constexpr int kSfbChunks = (BN + 127) / 128;
-    static constexpr int kSfCols = 4 + 4 * kSfbChunks;
+    static constexpr int kARows = MP / 2;                        // rows of A (and D) per CTA
+    static constexpr int kAccCols = MP == 256 ? BN : BN / 2;     // TMEM columns of one accumulator
+    // B scale words: MP=256 copies each 128-column chunk to all four lane quadrants;
+    // MP=128 copies the two halves of N to quadrants {0,1} and {2,3} (one 64-row copy)
+    static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
+    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4);
     // Scale words pass through two rings: kSfSlots shared-memory slots (TMA
     // destination, reordered in place) and kSfTmemSlots TMEM slots (what the
     // MMA reads).  The producer issues the scale loads kSfLookahead groups
@@ -50,16 +61,16 @@ struct Bs2Config {
     static constexpr int kSfSlots = 8;
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots =
-        (2 * BN + 4 * kSfCols <= 512 || 2 * BN + 2 * kSfCols > 512) ? 4 : 2;
-    static constexpr int kABytes = kBlockM * kBlockK;           // this CTA's 128 rows of A
+        (2 * kAccCols + 4 * kSfCols <= 512 || 2 * kAccCols + 2 * kSfCols > 512) ? 4 : 2;
+    static constexpr int kABytes = kARows * kBlockK;            // this CTA's rows of A
     static constexpr int kBBytes = (BN / 2) * kBlockK;          // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = 512 * kSfbChunks;
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
-    static constexpr int kSfTxBytes = kSfaBytes + BN * 4;
+    static constexpr int kSfTxBytes = kARows * 4 + BN * 4;
     static constexpr int kEpiChunk = 16;
-    static constexpr int kNumChunks = BN / kEpiChunk;
+    static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
     static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;
     static constexpr int kSmemLimit = 232448;
@@ -69,14 +80,32 @@ struct Bs2Config {
     static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;
-    static constexpr int kNumAcc = (2 * BN + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
+    static constexpr int kNumAcc = (2 * kAccCols + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
-    static_assert(kNumAcc * BN + kSfTmemSlots * kSfCols <= kTmemCols, "TMEM budget");
+    static_assert(kNumAcc * kAccCols + kSfTmemSlots * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kRing >= 2, "pipeline too shallow");
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
 };
+
+// MP=128 B scales: the words of D columns [0, half) and [half, 2 half) (as TMA
+// lands them, column j at word j) become rows 0-31 and 32-63 of the 64x128b copy
+// source, row r of a half holding its words r, r+32, r+64, r+96.  One warp, in
+// place (all reads before the writes; a half has at most 128 words, so every
+// read stays inside the 256-word buffer).
+__device__ __forceinline__ void sf_transpose_halves_for_cp(uint32_t *buf, int half, uint32_t lane) {
+    uint32_t v[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) v[h][i] = buf[h * half + ((i ^ (lane >> 3)) & 3) * 32 + lane];
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) buf[(32 * h + lane) * 4 + ((i ^ (lane >> 3)) & 3)] = v[h][i];
+}
 
 struct PairTile {
     int a_row0;   // this CTA's first row of A and D
@@ -85,7 +114,7 @@ struct PairTile {
 };
 
 // Pair tile t -> (m-pair, n-block), grouped along M for L2 reuse.
-template <int BN>
+template <int BN, int MP>
 __device__ __forceinline__ void get_pair_tile(const GemmParams &p, int t, int rank, PairTile &tile) {
     const int per_group = p.group_m * p.num_n_blocks;
     const int g = t / per_group;
@@ -95,26 +124,27 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, int t, int ra
     const int r = t - g * per_group;
     const int mp = first + r % gsize;
     const int nb = r / gsize;
-    tile.a_row0 = mp * 2 * kBlockM + rank * kBlockM;
+    tile.a_row0 = mp * MP + rank * (MP / 2);
     tile.n0 = nb * BN;
     tile.b_row0 = tile.n0 + rank * (BN / 2);
 }
 
-template <int BN, bool WITH_C>
-__global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2, 1, 1)
+template <int BN, bool WITH_C, int MP>
+__global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_sfa,
                        const __grid_constant__ CUtensorMap tm_sfb,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
-    using Cfg = Bs2Config<BN>;
+    using Cfg = Bs2Config<BN, MP>;
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
     constexpr int G = Cfg::kGroupKb;
     constexpr int NUM_ACC = Cfg::kNumAcc;
     constexpr int NSF = Cfg::kSfSlots;       // shared-memory scale slots
     constexpr int NTS = Cfg::kSfTmemSlots;   // TMEM scale slots
-    constexpr int MMA_M = 2 * kBlockM;
+    constexpr int MMA_M = MP;
+    constexpr int ACC = Cfg::kAccCols;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -187,7 +217,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
-    const uint32_t sf_col0 = NUM_ACC * BN;
+    const uint32_t sf_col0 = NUM_ACC * ACC;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs, whole warp)
@@ -202,7 +232,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         int sf_t = pair_id, sf_j = 0;
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             PairTile tile;
-            get_pair_tile<BN>(p, t, rank, tile);
+            get_pair_tile<BN, MP>(p, t, rank, tile);
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                 if ((kb0 & 3) == 0) {
@@ -211,7 +241,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                         if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
                             goto prod_done;
                         PairTile st;
-                        get_pair_tile<BN>(p, sf_t, rank, st);
+                        get_pair_tile<BN, MP>(p, sf_t, rank, st);
                         if (elect_one()) {
                             uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
                             mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
@@ -289,7 +319,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
                 if (!mbar_wait_cluster_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * ACC;
                 for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                     const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                     const int sslot = g % NTS;
@@ -352,13 +382,17 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                 uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
                 uint32_t *sfb_buf = sfa_buf + 128;
                 sf_transpose_for_cp(sfa_buf, lane);
+                if constexpr (MP == 256) {
 #pragma unroll
-                for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
+                } else {
+                    sf_transpose_halves_for_cp(sfb_buf, BN / 2, lane);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (!leader) {
                     // tell the leader this CTA's words for the group are in place
-                    if (lane == 0) mbar_arrive_cluster(leader_peer + slot * 8);
+                    if (lane == 0) mbar_arrive_remote(leader_peer + slot * 8);
                 } else {
                     const int tslot = g % NTS;
                     if (!mbar_wait_cluster_warp(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
@@ -369,10 +403,14 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                         tc_fence_after_sync();
                         const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
                         tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+                        if constexpr (MP == 256) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
-                            tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
-                                                      make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                            for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                                tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
+                                                          make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                        } else {
+                            tc_cp_64x128b_warpx2_01_23_pair(sfa_tmem + 4, make_desc_sf_32x128b(smem_u32(sfb_buf)));
+                        }
                         tc_commit_pair(&sf_ready_bar[tslot], 0x1);
                         tc_commit_pair(&sf_sfree_bar[slot], 0x3);   // both CTAs may refill the slot
                         copied = true;
@@ -390,8 +428,11 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const uint32_t ew = warp - 2;
-        const uint32_t quad = warp & 3;
-        const uint32_t half = ew >> 2;
+        const uint32_t quad = warp & 3;       // TMEM lane quadrant this warp may access
+        const uint32_t half = ew >> 2;        // which interleaved half of the quadrant's column chunks
+        // the quadrant's 32 rows (offset in this CTA's rows) and D-column offset of its TMEM columns
+        const int row_off = MP == 256 ? static_cast<int>(quad) * 32 : static_cast<int>(quad & 1) * 32;
+        const int col_off = MP == 256 ? 0 : static_cast<int>(quad >> 1) * (BN / 2);
         const uint32_t leader_tempty = mapa_shared(smem_u32(tempty_bar), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -400,8 +441,8 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         // C (bf16) of one chunk of this thread's row; zero outside [rows, n)
         auto load_c = [&](const PairTile &tl, int j, uint32_t (&dst)[8]) {
             const int c = 2 * j + half;
-            const int row = tl.a_row0 + quad * 32 + lane;
-            const int col0 = tl.n0 + c * Cfg::kEpiChunk;
+            const int row = tl.a_row0 + row_off + lane;
+            const int col0 = tl.n0 + col_off + c * Cfg::kEpiChunk;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint4 cv = make_uint4(0u, 0u, 0u, 0u);
@@ -419,7 +460,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
         PairTile tile;
         if (pair_id < num_tiles) {
-            get_pair_tile<BN>(p, pair_id, rank, tile);
+            get_pair_tile<BN, MP>(p, pair_id, rank, tile);
             if constexpr (WITH_C) {
 #pragma unroll
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
@@ -428,10 +469,10 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             const bool has_next = t + num_pairs < num_tiles;
             PairTile next_tile = tile;
-            if (has_next) get_pair_tile<BN>(p, t + num_pairs, rank, next_tile);
+            if (has_next) get_pair_tile<BN, MP>(p, t + num_pairs, rank, next_tile);
             // bf16 chunk (16 columns of this thread's row) -> swizzled staging -> TMA store
             auto store_chunk = [&](const uint32_t (&o)[8], int c) {
-                const int col0 = tile.n0 + c * Cfg::kEpiChunk;
+                const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
                 uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
@@ -443,7 +484,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tm_d, sbuf, col0, tile.a_row0 + quad * 32);
+                    tma_store_2d(&tm_d, sbuf, col0, tile.a_row0 + row_off);
                     bulk_commit_group();
                 }
                 buf ^= 1;
@@ -461,7 +502,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                     for (int u = 0; u < 2; ++u) {
                         const int c = 2 * (j0 + u) + half;
                         if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
-                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v[u]);
                     }
                     tmem_ld_wait();
 #pragma unroll
@@ -484,7 +525,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
+                if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
             } else {
                 // the whole row segment to registers, release the accumulator, then store
@@ -496,7 +537,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                     for (int u = 0; u < 2; ++u) {
                         const int c = 2 * (j0 + u) + half;
                         if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
-                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * BN + c * Cfg::kEpiChunk, v[u]);
+                            tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v[u]);
                     }
                     tmem_ld_wait();
 #pragma unroll
@@ -513,7 +554,7 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_tempty + acc * 8);
+                if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
 #pragma unroll
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
@@ -537,23 +578,23 @@ __global__ void __launch_bounds__(Bs2Config<BN>::kThreads, 1) __cluster_dims__(2
     }
 }
 
-template <int BN, bool WITH_C>
+template <int BN, bool WITH_C, int MP>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
-    using Cfg = Bs2Config<BN>;
-    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C>,
+    using Cfg = Bs2Config<BN, MP>;
+    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dg_bs2_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
+    dg_bs2_gemm_kernel<BN, WITH_C, MP><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
         maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
     return cudaGetLastError();
 }
 
-template <int BN, bool WITH_C>
+template <int BN, bool WITH_C, int MP>
 int max_active_pairs_impl() {
-    using Cfg = Bs2Config<BN>;
-    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C>,
+    using Cfg = Bs2Config<BN, MP>;
+    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -568,13 +609,13 @@ int max_active_pairs_impl() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C, MP>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 
-template <int BN>
+template <int BN, int MP>
 void fill_bs2_info(KernelInfo *info) {
-    using Cfg = Bs2Config<BN>;
+    using Cfg = Bs2Config<BN, MP>;
     info->block_n = BN;
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;

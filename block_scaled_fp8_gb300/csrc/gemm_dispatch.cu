@@ -20,34 +20,38 @@ DG_BS_BLOCK_N_LIST(DG_EXTERN)
 DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #undef DG_EXTERN
 
-#define DG_BS2_LIST(X) \
-    X(128, false) X(128, true) X(192, false) X(192, true) X(224, false) X(224, true) X(240, false) \
-    X(240, true) X(256, false)
-#define DG_EXTERN2(BN, C)                                                                        \
-    extern template cudaError_t launch_bs2_gemm_impl<BN, C>(const TensorMaps &, const GemmParams &, \
-                                                            int, cudaStream_t);                      \
-    extern template int max_active_pairs_impl<BN, C>();
+#define DG_BS2_LIST(X)                                                                             \
+    X(128, false, 256) X(128, true, 256) X(192, false, 256) X(192, true, 256) X(224, false, 256)      \
+    X(224, true, 256) X(240, false, 256) X(240, true, 256) X(256, false, 256) X(32, false, 128)       \
+    X(64, false, 128) X(96, false, 128) X(128, false, 128)
+#define DG_EXTERN2(BN, C, MP)                                                                      \
+    extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP>(const TensorMaps &, const GemmParams &, \
+                                                                int, cudaStream_t);                      \
+    extern template int max_active_pairs_impl<BN, C, MP>();
 DG_BS2_LIST(DG_EXTERN2)
 #undef DG_EXTERN2
 
-bool get_bs2_kernel_info(int block_n, bool with_c, KernelInfo *info) {
-#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) { fill_bs2_info<BN>(info); return true; }
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info) {
+#define DG_CASE2(BN, C, MP) \
+    if (block_n == BN && with_c == C && mp == MP) { fill_bs2_info<BN, MP>(info); return true; }
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return false;
 }
 
-cudaError_t launch_bs2_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
+cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream) {
     const bool with_c = p.c != nullptr;
-#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) return launch_bs2_gemm_impl<BN, C>(maps, p, grid, stream);
+#define DG_CASE2(BN, C, MP) \
+    if (block_n == BN && with_c == C && mp == MP) return launch_bs2_gemm_impl<BN, C, MP>(maps, p, grid, stream);
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return cudaErrorInvalidValue;
 }
 
-int bs2_max_active_pairs(int block_n, bool with_c) {
-#define DG_CASE2(BN, C) if (block_n == BN && with_c == C) return max_active_pairs_impl<BN, C>();
+int bs2_max_active_pairs(int block_n, bool with_c, int mp) {
+#define DG_CASE2(BN, C, MP) \
+    if (block_n == BN && with_c == C && mp == MP) return max_active_pairs_impl<BN, C, MP>();
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return 0;

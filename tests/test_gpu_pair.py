@@ -85,3 +85,27 @@ def test_pair_full_compare_several_waves(orc):
     ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
                               sb_rows(case.sfb, N), rows, cols)
     assert_close(bf16_bits(d)[rows, cols], ref, "pair several waves")
+
+
+# ------------------------------------------------------------------ 128-row pairs (skinny M)
+
+@pytest.mark.parametrize("M,N,K", [(128, 2112, 1024), (100, 7168, 640), (1, 2112, 384), (64, 7168, 2048),
+                                   (128, 7168, 336)])
+def test_skinny_pair_matches_single_cta_and_oracle(orc, M, N, K):
+    """M <= 128 runs on 128-row pairs (64 rows of A per CTA; D columns split
+    across TMEM lane halves) when the load model prefers them; the result is
+    bit-identical to the single-CTA kernel and matches the oracle."""
+    case = inputs.dense_case(M, N, K, seed=M + N + K, b_scale_exp_range=(-8, 4))
+    d_pair, cfg = _gemm(case, single_cta=False)
+    d_one, cfg_one = _gemm(case, single_cta=True)
+    assert cfg["kind"] == 2 and cfg["block_m"] == 128, cfg
+    assert cfg_one["kind"] == 0
+    assert torch.equal(d_pair, d_one), f"{M}x{N}x{K}: 128-row pair and single-CTA results differ"
+    rng = np.random.default_rng(M + K)
+    rows = rng.integers(0, M, 3000)
+    cols = rng.integers(0, N, 3000)
+    rows[:4] = [0, 0, M - 1, M - 1]
+    cols[:4] = [0, N - 1, 0, N - 1]
+    ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                              sb_rows(case.sfb, N), rows, cols)
+    assert_close(bf16_bits(d_pair)[rows, cols], ref, f"skinny pair {M}x{N}x{K}")
