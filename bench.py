@@ -422,8 +422,8 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic()
     big_traffic = skinny_traffic = None
     if traffic is not None:
-        big_traffic = traffic.get("dg_bs2_gemm_kernel")
-        skinny_traffic = traffic.get("dg_bs_gemm_kernel")
+        big_traffic = traffic.get("m4096_mean_bytes_per_launch")
+        skinny_traffic = traffic.get("m128_mean_bytes_per_launch")
 
     result = None
     if rank == 0:
@@ -454,8 +454,9 @@ def run_ours(args, rank, world, local_rank):
             "roofline_skinny": {"bound": "hbm", "achieved": round(skinny_gbs, 1),
                                 "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
                                 "frac": round(skinny_gbs / peaks["hbm_gbs"], 4),
-                                "kernel": "dg_bs_gemm_kernel: the three M=128 GEMMs, algorithmic "
-                                          "bytes / summed launch time, of " + peaks["source"],
+                                "kernel": "the three M=128 GEMMs (dg_bs2_gemm_kernel on 128-row CTA pairs "
+                                          "where the load model prefers them, else dg_bs_gemm_kernel): "
+                                          "algorithmic bytes / summed launch time, of " + peaks["source"],
                                 "traffic": skinny_traffic},
             "per_gemm": per_gemm,
             "other_workloads": other,
