@@ -251,6 +251,25 @@ def measure_library_fp8_peak(dev, stream):
         return f"unavailable: {type(exc).__name__}"
 
 
+# --------------------------------------------------------------------- ranks
+
+def reduce_job_times(local_ms, world, device):
+    """Maximum over ranks of each per-rank time in `local_ms` (a list, ms); every
+    rank receives the same list."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(local_ms, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_tflops(flops_per_step, steps, world, total_ms):
+    """Whole-job throughput: each of `world` ranks runs `steps` steps of its own
+    replica of the workload in at most `total_ms`."""
+    return flops_per_step * steps * world / (total_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------- ours
 
 def run_ours(args, rank, world, local_rank):
@@ -393,12 +412,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
 
     # ---------------- reductions over ranks (max time)
-    t = torch.tensor([local_ms, e2e_ms, local_t_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_total_ms, total_t_ms = float(t[0]), float(t[1]), float(t[2])
-    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
-    e2e_value = step_flops * e2e_steps * world / (e2e_total_ms * 1e-3) / 1e12
+    total_ms, e2e_total_ms, total_t_ms = reduce_job_times([local_ms, e2e_ms, local_t_ms], world, dev)
+    value = job_tflops(step_flops, args.steps, world, total_ms)
+    e2e_value = job_tflops(step_flops, e2e_steps, world, e2e_total_ms)
 
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_TFLOPS / NOMINAL_BF16_TFLOPS
@@ -440,7 +456,7 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": f"replicas x{world}"},
             "pct_of_nominal_fp8_peak": round(100.0 * value / NOMINAL_FP8_TFLOPS, 2),
             "with_transform": {
-                "value": round(step_flops * args.steps * world / (total_t_ms * 1e-3) / 1e12, 2),
+                "value": round(job_tflops(step_flops, args.steps, world, total_t_ms), 2),
                 "ms_per_step": round(total_t_ms / args.steps, 4),
                 "step": "dg_transform_sf of each activation's FP32 scales + dg_fp8_gemm_nt "
                         "(12 launches per step, one CUDA graph)"},
