@@ -186,10 +186,19 @@ int choose_cluster(int64_t num_n_blocks) {
     return c;
 }
 
-// Dense problems with more than one 128-row block run on CTA pairs (256-row
-// tiles, cta_group::2) unless DG_DEBUG_SINGLE_CTA is set.
-bool use_pair_kernel(const GemmParams &p) {
-    return !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA) && p.mode == kModeDense && p.rows > kBlockM;
+// 256-row CTA pairs (cta_group::2) unless DG_DEBUG_SINGLE_CTA is set: dense
+// problems with more than one 128-row block; contiguous layouts of at most
+// kMaxPairPrefix m-pairs (and fewer than 2^15 experts); masked layouts of at
+// most kMaxPairPrefix experts that expect more than 256 rows per expert.  The
+// masked decode (a few dozen rows per expert) is bound by reading each
+// expert's B once from HBM, which the single-CTA kernel does as well (its two
+// 128-row blocks of an expert share B through L2) at less cost per tile.
+bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
+    if (g_debug_flags.load() & DG_DEBUG_SINGLE_CTA) return false;
+    if (p.mode == kModeDense) return p.rows > kBlockM;
+    if (p.mode == kModeContiguous)
+        return cdiv64(p.rows, 2 * kBlockM) <= kMaxPairPrefix && p.num_groups < 32768;
+    return p.rows > kBlockM && p.num_groups <= kMaxPairPrefix && m_blocks_hint > 2LL * p.num_groups;
 }
 
 int cached_max_pairs(int bn, bool with_c, int mp) {
@@ -210,9 +219,9 @@ int usable_pairs(int bn, bool with_c, int mp, int num_sms) {
 }
 
 // BLOCK_N of the 256-row pair kernel: the score of choose_block_n over the
-// co-resident pairs (DG_PAIR_BLOCK_N forces one).
-int choose_pair_block_n(const GemmParams &p, bool with_c, int num_sms) {
-    const int64_t m_pairs = cdiv64(p.rows, 2 * kBlockM);
+// co-resident pairs (DG_PAIR_BLOCK_N forces one); m_pairs is the expected
+// number of 256-row units.
+int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int num_sms) {
     int bn = 0;
     double best = -1.0;
     static const int forced_bn = [] {
@@ -260,15 +269,15 @@ int choose_skinny_pair_block_n(const GemmParams &p, int bn1, int num_sms) {
     return best_bn;
 }
 
-// One launch of the pair kernel with mp rows per pair tile and BLOCK_N bn.
-dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int num_sms,
-                      cudaStream_t stream) {
+// One launch of the pair kernel with mp rows per pair tile and BLOCK_N bn;
+// max_units bounds the number of mp-row units (the grid size).
+dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_t max_units,
+                      int num_sms, cudaStream_t stream) {
     const bool with_c = p.c != nullptr;
     KernelInfo info;
     if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info)) return DG_ERR_UNSUPPORTED;
     const int pairs = usable_pairs(bn, with_c, mp, num_sms);
     if (pairs <= 0) return DG_ERR_UNSUPPORTED;
-    const int64_t m_units = cdiv64(p.rows, mp);
     const uint32_t a_rows = static_cast<uint32_t>(mp / 2);   // rows of A each CTA loads
     TensorMaps maps;
     const int k = p.k;
@@ -294,7 +303,8 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int nu
     ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                     32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
-    p.num_m_blocks = static_cast<int>(m_units);     // the pair kernel counts mp-row units
+    // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused)
+    if (p.mode != kModeMasked) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
     p.cluster = 2;
@@ -306,7 +316,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int nu
     uint32_t dbg = g_debug_flags.load();
     if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
     p.debug_flags = dbg;
-    const int64_t tiles = m_units * p.num_n_blocks;
+    const int64_t tiles = max_units * p.num_n_blocks;
     const int64_t used = tiles < pairs ? tiles : pairs;
     const int grid = static_cast<int>(2 * used);
     if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
@@ -324,14 +334,19 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int nu
 
 dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_blocks_hint,
                               int64_t max_tiles_per_n_block, int num_sms, cudaStream_t stream) {
-    if (use_pair_kernel(p))
-        return launch_pair(p, o, 256, choose_pair_block_n(p, p.c != nullptr, num_sms), num_sms, stream);
+    if (use_pair_kernel(p, m_blocks_hint)) {
+        // dense: 256-row m-pairs; grouped: about half the 128-row blocks (at most all of them)
+        const int64_t units_hint = p.mode == kModeDense ? cdiv64(p.rows, 2 * kBlockM) : cdiv64(m_blocks_hint, 2);
+        const int64_t max_units = p.mode == kModeDense ? units_hint : max_tiles_per_n_block;
+        return launch_pair(p, o, 256, choose_pair_block_n(p, p.c != nullptr, units_hint, num_sms), max_units,
+                           num_sms, stream);
+    }
     const bool with_c = p.c != nullptr;
     const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
     if (p.mode == kModeDense && !with_c && p.rows <= kBlockM &&
         !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA)) {
         const int bn2 = choose_skinny_pair_block_n(p, bn, num_sms);
-        if (bn2 > 0) return launch_pair(p, o, 128, bn2, num_sms, stream);
+        if (bn2 > 0) return launch_pair(p, o, 128, bn2, cdiv64(p.rows, 128), num_sms, stream);
     }
     KernelInfo info;
     if (!get_bs_kernel_info(bn, with_c, &info)) return DG_ERR_UNSUPPORTED;

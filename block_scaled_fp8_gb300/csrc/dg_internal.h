@@ -13,6 +13,8 @@ constexpr int kBlockM = 128;   // rows per tile (one UMMA M=128, TMEM lanes)
 constexpr int kBlockK = 128;   // K per pipeline stage (= scale granularity)
 constexpr int kGran = 128;     // scale granularity along K (and N for FP32 B scales)
 constexpr int kMaxGroupsMasked = 1024;
+// Grouped layouts on CTA pairs: at most this many m-pairs (contiguous) or experts (masked).
+constexpr int kMaxPairPrefix = 512;
 
 enum GemmMode : int { kModeDense = 0, kModeContiguous = 1, kModeMasked = 2 };
 

@@ -74,7 +74,8 @@ struct Bs2Config {
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
     static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;
     static constexpr int kSmemLimit = 232448;
-    static constexpr int kFixedBytes = 1024 + kStagingBytes + kSfSlots * kSfSlotBytes + 512;
+    static constexpr int kPrefixBytes = (2 * kMaxPairPrefix + 1) * 4;  // grouped-layout unit prefix + info
+    static constexpr int kFixedBytes = 1024 + kStagingBytes + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
     static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
@@ -108,25 +109,159 @@ __device__ __forceinline__ void sf_transpose_halves_for_cp(uint32_t *buf, int ha
 }
 
 struct PairTile {
-    int a_row0;   // this CTA's first row of A and D
-    int n0;       // first output column of the tile
-    int b_row0;   // this CTA's first row of B (its half of the tile's columns)
+    int a_row0;      // this CTA's first row in the 2-D view of A (and D)
+    int sfa_x;       // MN index of that row in the packed SFA view
+    int sfa_y0;      // row of the packed SFA view for K-slice 0
+    int n0;          // first output column of the tile
+    int b_row0;      // this CTA's first row of B ([E*N, K] view): its half of the tile's columns
+    int sfb_y0;      // row of the packed SFB view for K-slice 0
+    int valid_rows;  // rows of this CTA's MP/2 that are stored (0: none)
 };
 
-// Pair tile t -> (m-pair, n-block), grouped along M for L2 reuse.
+// Pair units.  A unit is the row range of one pair tile; the tiles are the
+// units crossed with the n-blocks.
+//   dense:      unit u = rows [MP u, MP u + MP).
+//   contiguous: (MP = 256) m-pair j = rows [256j, 256j + 256): two 128-row
+//               blocks, each of one expert or padding.  Both blocks of one
+//               expert: one unit.  Otherwise one unit per block that has an
+//               expert: the pair still computes 256 rows, but only the CTA
+//               holding that block stores.
+//   masked:     (MP = 256) expert e gets ceil(masked_m[e] / 256) units of 256
+//               of its rows; rows at or past masked_m[e] are not stored.
+// For the grouped layouts prefix[i] = units before m-pair (expert) i, built
+// once per CTA in shared memory; total units = prefix[count].  info[i] keeps
+// what the tile lookup needs without touching global memory: the two blocks'
+// experts (contiguous, 16 bits each) or the clamped masked_m (masked).
+
+// Experts of the two blocks of m-pair j (contiguous layout); -1 for padding,
+// past the end, or an out-of-range id (reported).
+__device__ __forceinline__ void pair_block_experts(const GemmParams &p, int j, int &e0, int &e1) {
+    const int r0 = 2 * j * kBlockM, r1 = r0 + kBlockM;
+    e0 = __ldg(p.grouped_layout + r0);
+    e1 = r1 < p.rows ? __ldg(p.grouped_layout + r1) : -1;
+    if (e0 >= p.num_groups) {
+        if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+        e0 = -1;
+    }
+    if (e1 >= p.num_groups) {
+        if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+        e1 = -1;
+    }
+}
+
+__device__ __forceinline__ int clamp_masked_m(const GemmParams &p, int e) {
+    int mm = __ldg(p.masked_m + e);
+    if (mm < 0 || mm > p.rows) {
+        if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+        mm = mm < 0 ? 0 : p.rows;
+    }
+    return mm;
+}
+
+// Builds prefix[0..count] and info[0..count) (count = m-pairs or experts)
+// with the whole CTA: unit counts in parallel, then one warp scans them.  Ends
+// with __syncthreads.
+__device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *prefix, int *info) {
+    const int count = p.mode == kModeMasked ? p.num_groups : p.num_m_blocks;
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+        int units;
+        if (p.mode == kModeMasked) {
+            const int mm = clamp_masked_m(p, i);
+            info[i] = mm;
+            units = (mm + 2 * kBlockM - 1) / (2 * kBlockM);
+        } else {
+            int e0, e1;
+            pair_block_experts(p, i, e0, e1);
+            info[i] = (e0 & 0xFFFF) | (e1 << 16);
+            units = (e0 >= 0 && e0 == e1) ? 1 : (e0 >= 0) + (e1 >= 0);
+        }
+        prefix[i + 1] = units;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (count + 31) / 32;
+        const int lo = lane * per, hi = lo + per < count ? lo + per : count;
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += prefix[i + 1];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        if (lane == 0) prefix[0] = 0;
+        for (int i = lo; i < hi; ++i) {
+            run += prefix[i + 1];
+            prefix[i + 1] = run;
+        }
+    }
+    __syncthreads();
+}
+
+// Largest i with prefix[i] <= u (prefix is non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int prefix_find(const int *prefix, int count, int u) {
+    int lo = 0, hi = count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int pair_units(const GemmParams &p, const int *prefix) {
+    if (p.mode == kModeDense) return p.num_m_blocks;
+    return prefix[p.mode == kModeMasked ? p.num_groups : p.num_m_blocks];
+}
+
+// Pair tile t (< units * n-blocks) for cluster rank `rank`; units are grouped
+// along M in runs of group_m so that pairs running at the same time share B.
 template <int BN, int MP>
-__device__ __forceinline__ void get_pair_tile(const GemmParams &p, int t, int rank, PairTile &tile) {
+__device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *prefix, const int *info,
+                                              int num_units, int psf_k, int t, int rank, PairTile &tile) {
     const int per_group = p.group_m * p.num_n_blocks;
     const int g = t / per_group;
     const int first = g * p.group_m;
-    const int rem = p.num_m_blocks - first;
+    const int rem = num_units - first;
     const int gsize = rem < p.group_m ? rem : p.group_m;
     const int r = t - g * per_group;
-    const int mp = first + r % gsize;
+    const int u = first + r % gsize;
     const int nb = r / gsize;
-    tile.a_row0 = mp * MP + rank * (MP / 2);
     tile.n0 = nb * BN;
-    tile.b_row0 = tile.n0 + rank * (BN / 2);
+    int group = 0;
+    if (MP == 128 || p.mode == kModeDense) {
+        tile.a_row0 = u * MP + rank * (MP / 2);
+        tile.sfa_x = tile.a_row0;
+        tile.sfa_y0 = 0;
+        tile.valid_rows = MP / 2;
+    } else if (p.mode == kModeContiguous) {
+        const int j = prefix_find(prefix, p.num_m_blocks, u);
+        const int e0 = static_cast<int16_t>(info[j] & 0xFFFF), e1 = info[j] >> 16;
+        tile.a_row0 = j * 2 * kBlockM + rank * kBlockM;
+        tile.sfa_x = tile.a_row0;
+        tile.sfa_y0 = 0;
+        if (e0 >= 0 && e0 == e1) {
+            group = e0;
+            tile.valid_rows = kBlockM;
+        } else {
+            // the unit's block: the first valid one, or the second if this is the pair's second unit
+            const int h = (e0 >= 0 && u > prefix[j]) || e0 < 0 ? 1 : 0;
+            group = h == 0 ? e0 : e1;
+            tile.valid_rows = rank == h ? kBlockM : 0;
+        }
+    } else {
+        const int e = prefix_find(prefix, p.num_groups, u);
+        const int local0 = (u - prefix[e]) * 2 * kBlockM + rank * kBlockM;
+        const int v = info[e] - local0;
+        group = e;
+        tile.a_row0 = e * p.rows + local0;
+        tile.sfa_x = local0;
+        tile.sfa_y0 = e * psf_k;
+        tile.valid_rows = v <= 0 ? 0 : (v < kBlockM ? v : kBlockM);
+    }
+    tile.b_row0 = group * p.n + tile.n0 + rank * (BN / 2);
+    tile.sfb_y0 = group * psf_k;
 }
 
 template <int BN, bool WITH_C, int MP>
@@ -166,6 +301,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     uint64_t *drain_bar = sf_tfree_bar + NTS;         // [2]
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *prefix = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + 512);  // grouped layouts
+    int *pinfo = prefix + kMaxPairPrefix + 1;
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -174,8 +311,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     const bool leader = rank == 0;
     const int pair_id = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
-    const int num_tiles = p.num_m_blocks * p.num_n_blocks;  // num_m_blocks counts 256-row pairs
     const int groups_per_tile = (p.num_k_blocks + 3) >> 2;
+    const int psf_k = groups_per_tile;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
@@ -207,6 +344,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         tma_prefetch_desc(&tm_sfb);
         tma_prefetch_desc(&tm_d);
     }
+    if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo);  // ends with __syncthreads
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     if (warp == 1) {
@@ -218,6 +356,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t sf_col0 = NUM_ACC * ACC;
+    const int num_units = pair_units(p, prefix);
+    const int num_tiles = num_units * p.num_n_blocks;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs, whole warp)
@@ -232,7 +372,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         int sf_t = pair_id, sf_j = 0;
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             PairTile tile;
-            get_pair_tile<BN, MP>(p, t, rank, tile);
+            get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tile);
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                 if ((kb0 & 3) == 0) {
@@ -241,12 +381,13 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
                             goto prod_done;
                         PairTile st;
-                        get_pair_tile<BN, MP>(p, sf_t, rank, st);
+                        get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, sf_t, rank, st);
                         if (elect_one()) {
                             uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
                             mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
-                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.a_row0, sf_j);
-                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0, sf_j);
+                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.sfa_x, st.sfa_y0 + sf_j);
+                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0,
+                                        st.sfb_y0 + sf_j);
                         }
                         __syncwarp();
                         sf_issued |= 1u << sslot;
@@ -460,7 +601,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
         PairTile tile;
         if (pair_id < num_tiles) {
-            get_pair_tile<BN, MP>(p, pair_id, rank, tile);
+            get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
             if constexpr (WITH_C) {
 #pragma unroll
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
@@ -469,10 +610,26 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             const bool has_next = t + num_pairs < num_tiles;
             PairTile next_tile = tile;
-            if (has_next) get_pair_tile<BN, MP>(p, t + num_pairs, rank, next_tile);
+            if (has_next) get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t + num_pairs, rank, next_tile);
             // bf16 chunk (16 columns of this thread's row) -> swizzled staging -> TMA store
+            // valid_rows: all (MP/2) -> TMA store (clipped at the tensor's edge); 0 -> this
+            // CTA's rows belong to no unit of the tile; otherwise (masked edge) direct stores
+            // of the valid rows only
             auto store_chunk = [&](const uint32_t (&o)[8], int c) {
                 const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
+                if (tile.valid_rows == 0 || col0 >= p.n) return;
+                if (tile.valid_rows < MP / 2) {
+                    const int local_row = row_off + static_cast<int>(lane);
+                    if (local_row < tile.valid_rows) {
+                        uint16_t *drow = p.d + static_cast<int64_t>(tile.a_row0 + local_row) * p.ldd + col0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (col0 + 8 * h < p.n)
+                                *reinterpret_cast<uint4 *>(drow + 8 * h) =
+                                    make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+                    }
+                    return;
+                }
                 uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();

@@ -87,6 +87,91 @@ def test_pair_full_compare_several_waves(orc):
     assert_close(bf16_bits(d)[rows, cols], ref, "pair several waves")
 
 
+
+# ------------------------------------------------------------------ grouped layouts on pairs
+
+def _contiguous(case, single_cta):
+    M_total = case.a.shape[0]
+    E, N, K = case.b.shape
+    sfa = binding.transform_sf(case.sfa.to(DEV), 1, M_total)
+    sfb = binding.transform_sf(case.sfb.to(DEV), 128, N)
+    d = torch.full((M_total, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.set_debug_flags(binding.DG_DEBUG_SINGLE_CTA if single_cta else 0)
+    try:
+        binding.dg_m_grouped_fp8_gemm_nt_contiguous(case.a.to(DEV), sfa, case.b.to(DEV), sfb, d,
+                                                    case.grouped_layout.to(DEV), status=status)
+        cfg = binding.last_config()
+    finally:
+        binding.set_debug_flags(0)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return d, cfg
+
+
+@pytest.mark.parametrize("m_per_expert", [[5, 130, 0, 128, 300, 1], [256, 384, 129], [1, 1, 1, 1, 1]])
+def test_contiguous_pair_matches_single_cta_and_oracle(orc, m_per_expert):
+    """Expert segments (padded to 128 rows) of odd and even block counts, so
+    256-row pairs both share an expert and straddle two."""
+    E, N, K = len(m_per_expert), 264, 512
+    case = inputs.contiguous_case(E, N, K, seed=sum(m_per_expert), m_per_expert=m_per_expert)
+    d_pair, cfg = _contiguous(case, single_cta=False)
+    d_one, cfg_one = _contiguous(case, single_cta=True)
+    assert cfg["kind"] == 2 and cfg_one["kind"] == 0
+    layout = case.grouped_layout.numpy()
+    valid = layout >= 0
+    assert torch.equal(d_pair[torch.from_numpy(valid).to(DEV)], d_one[torch.from_numpy(valid).to(DEV)])
+    ref = orc.m_grouped_contiguous(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                                   sb_rows(case.sfb, N), layout)
+    assert_close(bf16_bits(d_pair)[valid], ref[valid], f"contiguous pairs {m_per_expert}")
+    # 128-row blocks that start with padding are left untouched by both
+    for mb in range(len(layout) // 128):
+        if layout[mb * 128] < 0:
+            assert bool((d_pair[mb * 128:(mb + 1) * 128] == 3.0).all())
+
+
+def _masked(case, single_cta, expected_m=None):
+    E, max_m, K = case.a.shape
+    N = case.b.shape[1]
+    sfa = binding.transform_sf(case.sfa.to(DEV), 1, max_m)
+    sfb = binding.transform_sf(case.sfb.to(DEV), 128, N)
+    d = torch.full((E, max_m, N), 5.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.set_debug_flags(binding.DG_DEBUG_SINGLE_CTA if single_cta else 0)
+    try:
+        binding.dg_m_grouped_fp8_gemm_nt_masked(case.a.to(DEV), sfa, case.b.to(DEV), sfb, d,
+                                                case.masked_m.to(DEV), expected_m or case.expected_m,
+                                                status=status)
+        cfg = binding.last_config()
+    finally:
+        binding.set_debug_flags(0)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return d, cfg
+
+
+@pytest.mark.parametrize("max_m", [384, 520, 300])
+def test_masked_pair_matches_single_cta_and_oracle(orc, max_m):
+    """Masked layouts that expect more than 256 rows per expert run on pairs.
+    Valid-row counts on both sides of 128 and 256 (a half-filled pair, a pair
+    whose peer rows end inside its block); rows past masked_m keep their
+    canary value."""
+    mm = [m for m in [0, 1, 100, 128, 129, 200, 255, 256, 300, 384, 511, 520] if m <= max_m]
+    N, K = 136, 384
+    case = inputs.masked_case(len(mm), max_m, N, K, seed=max_m, masked_m=mm)
+    d_pair, cfg = _masked(case, single_cta=False, expected_m=max_m)
+    d_one, cfg_one = _masked(case, single_cta=True, expected_m=max_m)
+    assert cfg["kind"] == 2 and cfg_one["kind"] == 0
+    ref = orc.m_grouped_masked(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                               sb_rows(case.sfb, N), case.masked_m.numpy())
+    got = bf16_bits(d_pair)
+    for e, m in enumerate(mm):
+        assert torch.equal(d_pair[e, :m], d_one[e, :m]), f"expert {e}: pair and single-CTA differ"
+        if m:
+            assert_close(got[e, :m], ref[e, :m], f"masked pairs expert {e}")
+        assert bool((d_pair[e, m:] == 5.0).all()), f"expert {e} wrote rows past masked_m"
+
+
 # ------------------------------------------------------------------ 128-row pairs (skinny M)
 
 @pytest.mark.parametrize("M,N,K", [(128, 2112, 1024), (100, 7168, 640), (1, 2112, 384), (64, 7168, 2048),
