@@ -1,24 +1,26 @@
-// Block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2), dense layout.
+// Block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2): dense, contiguous
+// grouped and masked grouped layouts.
 //
 // Same method as the single-CTA kernel (gemm_bs.cuh; "02 · DeepGEMM 技术解析"
 // §2-§4, "DeepSeek V4 源码剖析 第13章" §13.3): per output tile the block-scaled
 // MMA accumulates sa*sb*(A_kb @ B_kb^T) over all K-blocks in FP32 TMEM.  Here a
-// cluster of two CTAs on two SMs computes one 256 x BN tile with M=256 MMAs
-// issued by the leader CTA:
-//   - each CTA loads its own 128 rows of A and half of the tile's B columns
-//     (BN/2 rows of B) per 128-K stage, so a stage holds 16 KB + 64*BN bytes
-//     instead of 16 KB + 128*BN and the ring is half again as deep; the pair's
-//     loads complete on the leader's barrier;
-//   - the MMA reads A rows 0-127 and B rows 0..BN/2-1 from the leader's shared
-//     memory, A rows 128-255 and B rows BN/2..BN-1 from the peer's, and writes
-//     each CTA's 128 rows of D into that CTA's TMEM;
-//   - each CTA's TMEM holds the A scales of its own rows and the B scales of all
-//     BN columns (lane n%32, column n/32, as in the single-CTA layout);
-//     tcgen05.cp.cta_group::2 copies each CTA's reordered words into its own TMEM;
+// cluster of two CTAs on two SMs computes one MP x BN tile with M=MP MMAs
+// issued by the leader CTA (MP = 256, or 128 for skinny problems):
+//   - each CTA loads its own MP/2 rows of A and half of the tile's B columns
+//     (BN/2 rows of B) per 128-K stage; the pair's loads complete on the
+//     leader's barrier.  An SM's TMA ingest is capped near 60 bytes per cycle,
+//     so halving the B bytes each SM loads is what the pair buys;
+//   - the MMA reads the leader's A rows and B rows 0..BN/2-1 from the leader's
+//     shared memory, the peer's A rows and B rows BN/2..BN-1 from the peer's,
+//     and writes each CTA's rows of D into that CTA's TMEM;
+//   - each CTA's TMEM holds the A scales of its own rows and the B scales of
+//     all BN columns (lane n%32, column n/32; for MP=128 per half of N, see
+//     Bs2Config); tcgen05.cp.cta_group::2 copies each CTA's reordered words
+//     into its own TMEM;
 //   - commits reach both CTAs (multicast), and the peer's epilogue and scale
 //     warps signal the leader's barriers through their cluster addresses.
-// Ring slots group kGroupKb K-blocks under one barrier pair to keep the single
-// issuing thread's per-K-block work below the tensor time.
+// Ring slots group kGroupKb K-blocks under one barrier pair to keep the MMA
+// warp's per-K-block work below the tensor time.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,11 +55,13 @@ struct Bs2Config {
     // destination, reordered in place) and kSfTmemSlots TMEM slots (what the
     // MMA reads).  The producer issues the scale loads kSfLookahead groups
     // ahead of the A/B group it is loading: the words queue behind the A/B
-    // tiles in the TMA unit, and the peer's hand-off to the leader takes about
-    // a microsecond, so both must start well before the MMAs need the group.
-    // A shared-memory slot frees when its copy into TMEM completes, which is
-    // more than kSfSlots - kSfLookahead groups behind the loads.  Four TMEM slots where two accumulators fit beside them; two
-    // where that makes room for a second accumulator (BN=240).
+    // tiles in the TMA unit, the peer hands its reordered words to the leader,
+    // and the copy into TMEM queues behind the issued MMAs, so all of it must
+    // start well before the MMAs need the group.  A shared-memory slot frees
+    // when its copy into TMEM completes, which is more than kSfSlots -
+    // kSfLookahead groups behind the loads.  Four TMEM slots where two
+    // accumulators fit beside them; two where that makes room for a second
+    // accumulator (BN=240).
     static constexpr int kSfSlots = 8;
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots =

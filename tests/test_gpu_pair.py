@@ -1,8 +1,10 @@
-"""The CTA-pair kernel (256-row tiles, tcgen05 cta_group::2) against the oracle
+"""The CTA-pair kernels (tcgen05 cta_group::2; 256- and 128-row tiles) against the oracle
 and, bit for bit, against the single-CTA kernel on the same inputs.
 
-Dense GEMMs with more than 128 rows run on CTA pairs; DG_DEBUG_SINGLE_CTA
-forces the single-CTA kernel, so the two paths can be compared directly.
+Dense GEMMs with more than 128 rows, contiguous grouped GEMMs and masked ones
+with many rows per expert run on 256-row pairs, skinny dense GEMMs on 128-row
+pairs; DG_DEBUG_SINGLE_CTA forces the single-CTA kernel, so the two paths can
+be compared directly.
 """
 import numpy as np
 import pytest
@@ -85,7 +87,6 @@ def test_pair_full_compare_several_waves(orc):
     ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
                               sb_rows(case.sfb, N), rows, cols)
     assert_close(bf16_bits(d)[rows, cols], ref, "pair several waves")
-
 
 
 # ------------------------------------------------------------------ grouped layouts on pairs
