@@ -175,26 +175,18 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const int num_clusters = gridDim.x / csize;
     const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], csize);   // every CTA of the cluster frees the slot
+    if (warp == 0) {
+        // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
+        // initialise them, each fencing its own inits.  Every CTA of a cluster frees
+        // an empty slot; both epilogue halves drain an accumulator.
+        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 2;
+        for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
+            uint32_t count = 1;
+            if (i >= R && i < 2 * R) count = csize;
+            if (i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC) count = Cfg::kEpiWarps;
+            mbar_init(&bars[i], count);
         }
-        for (int a = 0; a < NUM_ACC; ++a) {
-            mbar_init(&tfull_bar[a], 1);
-            mbar_init(&tempty_bar[a], Cfg::kEpiWarps);
-        }
-        for (int j = 0; j < NSF; ++j) {
-            mbar_init(&sf_full_bar[j], 1);
-            mbar_init(&sf_sfree_bar[j], 1);
-        }
-        for (int j = 0; j < NTS; ++j) {
-            mbar_init(&sf_ready_bar[j], 1);
-            mbar_init(&sf_tfree_bar[j], 1);
-        }
-        mbar_init(&drain_bar[0], 1);
-        mbar_init(&drain_bar[1], 1);
-        *abort_flag = 0;
+        if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -229,30 +221,33 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         int gs = 0;          // scale groups issued
         int ga = 0;          // A/B groups started
         uint32_t sf_issued = 0;
+        // issues the scale words of group gs; false if the CTA is aborting
+        auto issue_sf = [&]() -> bool {
+            const int sslot = gs % NSF;
+            if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT)) return false;
+            if (elect_one()) {
+                uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
+                mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
+                tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], sfc.tile.sfa_x, sfc.tile.sfa_y0 + sfc.j);
+                tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], sfc.tile.n0,
+                            sfc.tile.sfb_y0 + sfc.j);
+            }
+            __syncwarp();
+            sf_issued |= 1u << sslot;
+            ++gs;
+            sfc.next();
+            return true;
+        };
         for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
             if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, lane == 0)) continue;
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                 if ((kb0 & 3) == 0) {
-                    // keep the scale words kSfLookahead groups ahead of the A/B stream
-                    while (sfc.valid && gs <= ga + Cfg::kSfLookahead) {
-                        const int sslot = gs % NSF;
-                        if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                            goto prod_done;
-                        if (elect_one()) {
-                            uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
-                            mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
-                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], sfc.tile.sfa_x,
-                                        sfc.tile.sfa_y0 + sfc.j);
-                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot],
-                                        sfc.tile.n0, sfc.tile.sfb_y0 + sfc.j);
-                        }
-                        __syncwarp();
-                        sf_issued |= 1u << sslot;
-                        ++gs;
-                        sfc.next();
-                    }
+                    // the group's own scale words, where the lookahead has not issued them
+                    // (the first group): ahead of its A/B tiles
+                    while (sfc.valid && gs <= ga)
+                        if (!issue_sf()) goto prod_done;
                     ++ga;
                 }
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
@@ -298,6 +293,10 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     issued |= 1u << slot;
                 }
                 if (++slot == R) { slot = 0; phase ^= 1; }
+                // then up to two more scale groups per slot until they run kSfLookahead
+                // groups ahead: the first A/B tiles go out without waiting behind them
+                for (int i = 0; i < 2 && sfc.valid && gs <= ga - 1 + Cfg::kSfLookahead; ++i)
+                    if (!issue_sf()) goto prod_done;
             }
         }
     prod_done:

@@ -318,27 +318,15 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     const int groups_per_tile = (p.num_k_blocks + 3) >> 2;
     const int psf_k = groups_per_tile;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+    if (warp == 0) {
+        // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
+        // initialise them, each fencing its own inits
+        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 3 * NSF + 2 * NTS + 2;
+        for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
+            const bool is_tempty = i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC;
+            mbar_init(&bars[i], is_tempty ? 2 * Cfg::kEpiWarps : 1);
         }
-        for (int a = 0; a < NUM_ACC; ++a) {
-            mbar_init(&tfull_bar[a], 1);
-            mbar_init(&tempty_bar[a], 2 * Cfg::kEpiWarps);
-        }
-        for (int j = 0; j < NSF; ++j) {
-            mbar_init(&sf_full_bar[j], 1);
-            mbar_init(&sf_peer_bar[j], 1);
-            mbar_init(&sf_sfree_bar[j], 1);
-        }
-        for (int j = 0; j < NTS; ++j) {
-            mbar_init(&sf_ready_bar[j], 1);
-            mbar_init(&sf_tfree_bar[j], 1);
-        }
-        mbar_init(&drain_bar[0], 1);
-        mbar_init(&drain_bar[1], 1);
-        *abort_flag = 0;
+        if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -374,30 +362,34 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         uint32_t sf_issued = 0;
         // scale cursor over the same (tile, group) sequence, kSfLookahead groups ahead of A/B
         int sf_t = pair_id, sf_j = 0;
+        // issues the scale words of group gs; false if the CTA is aborting
+        auto issue_sf = [&]() -> bool {
+            const int sslot = gs % NSF;
+            if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT)) return false;
+            PairTile st;
+            get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, sf_t, rank, st);
+            if (elect_one()) {
+                uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
+                mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
+                tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.sfa_x, st.sfa_y0 + sf_j);
+                tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0, st.sfb_y0 + sf_j);
+            }
+            __syncwarp();
+            sf_issued |= 1u << sslot;
+            ++gs;
+            if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
+            return true;
+        };
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             PairTile tile;
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tile);
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                 if ((kb0 & 3) == 0) {
-                    while (sf_t < num_tiles && gs <= ga + Cfg::kSfLookahead) {
-                        const int sslot = gs % NSF;
-                        if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                            goto prod_done;
-                        PairTile st;
-                        get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, sf_t, rank, st);
-                        if (elect_one()) {
-                            uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
-                            mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
-                            tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.sfa_x, st.sfa_y0 + sf_j);
-                            tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0,
-                                        st.sfb_y0 + sf_j);
-                        }
-                        __syncwarp();
-                        sf_issued |= 1u << sslot;
-                        ++gs;
-                        if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
-                    }
+                    // the group's own scale words, where the lookahead has not issued them
+                    // (the first group): ahead of its A/B tiles
+                    while (sf_t < num_tiles && gs <= ga)
+                        if (!issue_sf()) goto prod_done;
                     ++ga;
                 }
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
@@ -433,6 +425,10 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     issued |= 1u << slot;
                 }
                 if (++slot == R) { slot = 0; phase ^= 1; }
+                // then up to two more scale groups per slot until they run kSfLookahead
+                // groups ahead: the first A/B tiles go out without waiting behind them
+                for (int i = 0; i < 2 && sf_t < num_tiles && gs <= ga - 1 + Cfg::kSfLookahead; ++i)
+                    if (!issue_sf()) goto prod_done;
             }
         }
     prod_done:
