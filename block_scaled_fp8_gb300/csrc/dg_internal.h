@@ -40,6 +40,12 @@ struct GemmParams {
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
+    // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the pair
+    // kernel's scale warps read them with cp.async
+    const uint32_t *sfa_words;
+    const uint32_t *sfb_words;
+    int sfa_ld, sfb_ld;
+    int sfa_slices, sfb_slices;
     // FP32-promotion kernel only
     const float *sfa_f32;   // [rows][sf_k]
     const float *sfb_f32;   // [ceil(n/128)][sf_k]

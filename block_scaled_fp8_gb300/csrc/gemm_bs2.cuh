@@ -51,17 +51,15 @@ struct Bs2Config {
     // MP=128 copies the two halves of N to quadrants {0,1} and {2,3} (one 64-row copy)
     static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
     static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4);
-    // Scale words pass through two rings: kSfSlots shared-memory slots (TMA
+    // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
     // destination, reordered in place) and kSfTmemSlots TMEM slots (what the
-    // MMA reads).  The producer issues the scale loads kSfLookahead groups
-    // ahead of the A/B group it is loading: the words queue behind the A/B
-    // tiles in the TMA unit, the peer hands its reordered words to the leader,
-    // and the copy into TMEM queues behind the issued MMAs, so all of it must
-    // start well before the MMAs need the group.  A shared-memory slot frees
-    // when its copy into TMEM completes, which is more than kSfSlots -
-    // kSfLookahead groups behind the loads.  Four TMEM slots where two
-    // accumulators fit beside them; two where that makes room for a second
-    // accumulator (BN=240).
+    // MMA reads).  The scale warp loads a group kSfLookahead groups before it
+    // copies it to TMEM: the load takes a global-memory latency, the peer
+    // hands its reordered words to the leader, and the copy into TMEM queues
+    // behind the issued MMAs.  A shared-memory slot frees when its copy into
+    // TMEM completes, which is kSfSlots - kSfLookahead groups before the slot
+    // is loaded again.  Four TMEM slots where two accumulators fit beside
+    // them; two where that makes room for a second accumulator (BN=240).
     static constexpr int kSfSlots = 8;
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots =
@@ -72,7 +70,6 @@ struct Bs2Config {
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = 512 * kSfbChunks;
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
-    static constexpr int kSfTxBytes = kARows * 4 + BN * 4;
     static constexpr int kEpiChunk = 16;
     static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
@@ -93,24 +90,6 @@ struct Bs2Config {
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
 };
-
-// MP=128 B scales: the words of D columns [0, half) and [half, 2 half) (as TMA
-// lands them, column j at word j) become rows 0-31 and 32-63 of the 64x128b copy
-// source, row r of a half holding its words r, r+32, r+64, r+96.  One warp, in
-// place (all reads before the writes; a half has at most 128 words, so every
-// read stays inside the 256-word buffer).
-__device__ __forceinline__ void sf_transpose_halves_for_cp(uint32_t *buf, int half, uint32_t lane) {
-    uint32_t v[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) v[h][i] = buf[h * half + ((i ^ (lane >> 3)) & 3) * 32 + lane];
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (uint32_t i = 0; i < 4; ++i) buf[(32 * h + lane) * 4 + ((i ^ (lane >> 3)) & 3)] = v[h][i];
-}
 
 struct PairTile {
     int a_row0;      // this CTA's first row in the 2-D view of A (and D)
@@ -272,8 +251,6 @@ template <int BN, bool WITH_C, int MP>
 __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
-                       const __grid_constant__ CUtensorMap tm_sfa,
-                       const __grid_constant__ CUtensorMap tm_sfb,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
     using Cfg = Bs2Config<BN, MP>;
     constexpr int S = Cfg::kStages;
@@ -297,8 +274,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     uint64_t *empty_bar = full_bar + R;               // [R] both: MMAs done with the slot
     uint64_t *tfull_bar = empty_bar + R;              // [NUM_ACC] both: accumulator complete
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] leader: both epilogues drained
-    uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] both: own scale words landed
-    uint64_t *sf_peer_bar = sf_full_bar + NSF;        // [NSF] leader: peer's words reordered
+    uint64_t *sf_peer_bar = tempty_bar + NUM_ACC;     // [NSF] leader: peer's words reordered
     uint64_t *sf_sfree_bar = sf_peer_bar + NSF;       // [NSF] both: words copied out of the slot
     uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] leader: words in both TMEMs
     uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] leader: MMAs done with the slot
@@ -321,7 +297,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     if (warp == 0) {
         // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
         // initialise them, each fencing its own inits
-        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 3 * NSF + 2 * NTS + 2;
+        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 2;
         for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
             const bool is_tempty = i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC;
             mbar_init(&bars[i], is_tempty ? 2 * Cfg::kEpiWarps : 1);
@@ -332,8 +308,6 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
-        tma_prefetch_desc(&tm_sfa);
-        tma_prefetch_desc(&tm_sfb);
         tma_prefetch_desc(&tm_d);
     }
     if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo);  // ends with __syncthreads
@@ -358,40 +332,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && pair_id == 0;
-        int gs = 0, ga = 0;
-        uint32_t sf_issued = 0;
-        // scale cursor over the same (tile, group) sequence, kSfLookahead groups ahead of A/B
-        int sf_t = pair_id, sf_j = 0;
-        // issues the scale words of group gs; false if the CTA is aborting
-        auto issue_sf = [&]() -> bool {
-            const int sslot = gs % NSF;
-            if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT)) return false;
-            PairTile st;
-            get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, sf_t, rank, st);
-            if (elect_one()) {
-                uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
-                mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
-                tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], st.sfa_x, st.sfa_y0 + sf_j);
-                tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], st.n0, st.sfb_y0 + sf_j);
-            }
-            __syncwarp();
-            sf_issued |= 1u << sslot;
-            ++gs;
-            if (++sf_j == groups_per_tile) { sf_j = 0; sf_t += num_pairs; }
-            return true;
-        };
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             PairTile tile;
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tile);
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                if ((kb0 & 3) == 0) {
-                    // the group's own scale words, where the lookahead has not issued them
-                    // (the first group): ahead of its A/B tiles
-                    while (sf_t < num_tiles && gs <= ga)
-                        if (!issue_sf()) goto prod_done;
-                    ++ga;
-                }
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                 if (drop) {
                     drop = false;  // diagnostic: leave this slot empty
@@ -425,26 +370,14 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     issued |= 1u << slot;
                 }
                 if (++slot == R) { slot = 0; phase ^= 1; }
-                // then up to two more scale groups per slot until they run kSfLookahead
-                // groups ahead: the first A/B tiles go out without waiting behind them
-                for (int i = 0; i < 2 && sf_t < num_tiles && gs <= ga - 1 + Cfg::kSfLookahead; ++i)
-                    if (!issue_sf()) goto prod_done;
             }
         }
     prod_done:
-        if (lane == 0) {
-            // the leader waits for the last fill of every slot (both CTAs' bytes count there)
-            if (leader)
-                for (int s = 0; s < R; ++s)
-                    if (issued & (1u << s))
-                        mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
-            // and every CTA for its last scale load into each slot
-            for (int j = 0; j < NSF; ++j)
-                if (sf_issued & (1u << j)) {
-                    const int g = gs - 1 - ((gs - 1 - j) % NSF + NSF) % NSF;
-                    mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
-                }
-        }
+        // the leader waits for the last fill of every slot (both CTAs' bytes count there)
+        if (lane == 0 && leader)
+            for (int s = 0; s < R; ++s)
+                if (issued & (1u << s))
+                    mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader, whole warp)
@@ -513,24 +446,82 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         }
     } else if (warp == Cfg::kSfWarp) {
         // ------------------------------------------------------------ scale-factor warp (both CTAs)
+        // This CTA's words of a group (its A rows, all BN columns of B) land in a
+        // slot by cp.async, up to kSfLookahead groups ahead of the group being
+        // copied to TMEM: plain loads keep the TMA unit to the operand tiles and
+        // the producer's loop to A and B.  Each 4-byte copy puts its word where
+        // tcgen05.cp wants it (source row r holds words r, r+32, r+64, r+96 of a
+        // 128-word chunk; for MP=128 the two halves of N are rows 0-31 and
+        // 32-63), so the words need no reordering.  A word past the packed row
+        // length reads nothing and lands as zero.
         const uint32_t leader_peer = mapa_shared(smem_u32(sf_peer_bar), 0);
+        int lt = pair_id, lj = 0;   // tile and group of the next load
+        int gl = 0;                 // groups whose loads are issued
+        int st_t = -1;              // tile whose coordinates st holds
+        PairTile st;
+        // issues the loads of group gl, or an empty commit group past the last one;
+        // false if the CTA is aborting
+        auto load_group = [&]() -> bool {
+            if (lt < num_tiles) {
+                const int slot = gl % NSF;
+                // the slot's previous words have been copied to TMEM
+                if (gl >= NSF &&
+                    !mbar_wait_warp(&sf_sfree_bar[slot], ((gl / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                    return false;
+                if (st_t != lt) {
+                    get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, lt, rank, st);
+                    st_t = lt;
+                }
+                const uint32_t dst0 = smem_u32(smem_sf + slot * Cfg::kSfSlotBytes);
+                // word x of packed row y of one scale tensor -> word w of the slot
+                auto copy_word = [&](const uint32_t *base, int ld, int slices, int x, int y, uint32_t w) {
+                    const bool in = x < ld && y < slices;
+                    cp_async_4(dst0 + 4u * w, in ? base + static_cast<int64_t>(y) * ld + x : base, in ? 4u : 0u);
+                };
+                const int ya = st.sfa_y0 + lj, yb = st.sfb_y0 + lj;
+#pragma unroll
+                for (int q = 0; q < Cfg::kARows / 32; ++q)
+                    copy_word(p.sfa_words, p.sfa_ld, p.sfa_slices, st.sfa_x + 32 * q + static_cast<int>(lane), ya,
+                              4 * lane + q);
+                if constexpr (MP == 256) {
+#pragma unroll
+                    for (int c = 0; c < Cfg::kSfbChunks; ++c)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
+                                      st.n0 + 128 * c + 32 * q + static_cast<int>(lane), yb,
+                                      128 + 128 * c + 4 * lane + q);
+                } else {
+                    constexpr int kHalf = BN / 2;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int q = 0; q < (kHalf + 31) / 32; ++q)
+                            if (32 * q + static_cast<int>(lane) < kHalf)
+                                copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
+                                          st.n0 + h * kHalf + 32 * q + static_cast<int>(lane), yb,
+                                          128 + 4 * (32 * h + lane) + q);
+                }
+                if (++lj == groups_per_tile) { lj = 0; lt += num_pairs; }
+            }
+            cp_async_commit();
+            ++gl;
+            return true;
+        };
         int g = 0;
         bool copied = false;
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             for (int j = 0; j < groups_per_tile; ++j, ++g) {
                 const int slot = g % NSF;
-                if (!mbar_wait_warp(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)) goto sf_done;
+                // up to two more groups, kSfLookahead ahead at most; the first group
+                // starts at once
+                for (int i = 0; i < 2 && gl <= g + Cfg::kSfLookahead; ++i)
+                    if (!load_group()) goto sf_done;
+                cp_async_wait_dyn(gl - g - 1);                // this lane's words of group g
+                fence_proxy_async_smem();                     // visible to tcgen05.cp
+                __syncwarp();
                 uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
                 uint32_t *sfb_buf = sfa_buf + 128;
-                sf_transpose_for_cp(sfa_buf, lane);
-                if constexpr (MP == 256) {
-#pragma unroll
-                    for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
-                } else {
-                    sf_transpose_halves_for_cp(sfb_buf, BN / 2, lane);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (!leader) {
                     // tell the leader this CTA's words for the group are in place
                     if (lane == 0) mbar_arrive_remote(leader_peer + slot * 8);
@@ -561,6 +552,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             }
         }
     sf_done:
+        cp_async_wait<0>();
         if (lane == 0 && leader && copied) {
             tc_commit_pair(&drain_bar[1], 0x1);
             mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
@@ -744,7 +736,7 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     dg_bs2_gemm_kernel<BN, WITH_C, MP><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-        maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
+        maps.a, maps.b, maps.d, p);
     return cudaGetLastError();
 }
 
