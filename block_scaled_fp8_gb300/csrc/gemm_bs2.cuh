@@ -42,9 +42,10 @@ struct Bs2Config {
     static_assert(MP == 256 || MP == 128, "pair tile rows");
     static_assert(MP == 256 ? (BN % 16 == 0 && BN >= 64) : (BN % 32 == 0 && BN >= 32), "tile columns");
     static_assert(BN <= 256, "N <= 256");
-    static constexpr int kThreads = 352;
+    static constexpr int kThreads = 384;
     static constexpr int kEpiWarps = 8;
-    static constexpr int kSfWarp = 10;
+    static constexpr int kSfWarp = 10;                           // first scale warp
+    static constexpr int kSfWarps = 2;                           // they take alternate groups
     static constexpr int kARows = MP / 2;                        // rows of A (and D) per CTA
     static constexpr int kAccCols = MP == 256 ? BN : BN / 2;     // TMEM columns of one accumulator
     // B scale words: MP=256 copies each 128-column chunk to all four lane quadrants;
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     uint64_t *sf_sfree_bar = sf_peer_bar + NSF;       // [NSF] both: words copied out of the slot
     uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] leader: words in both TMEMs
     uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] leader: MMAs done with the slot
-    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [2]
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
+    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [1 + kSfWarps] MMA warp, scale warps
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1 + Cfg::kSfWarps);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + 512);  // grouped layouts
     int *pinfo = prefix + kMaxPairPrefix + 1;
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     if (warp == 0) {
         // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
         // initialise them, each fencing its own inits
-        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 2;
+        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 1 + Cfg::kSfWarps;
         for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
             const bool is_tempty = i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC;
             mbar_init(&bars[i], is_tempty ? 2 * Cfg::kEpiWarps : 1);
@@ -444,8 +445,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             }
             __syncwarp();
         }
-    } else if (warp == Cfg::kSfWarp) {
-        // ------------------------------------------------------------ scale-factor warp (both CTAs)
+    } else if (warp >= Cfg::kSfWarp) {
+        // ------------------------------------------------------------ scale-factor warps (both CTAs)
+        // kSfWarps warps take the (tile, 4-K-block group) sequence in turns, so
+        // the waits and tcgen05 issues of one group overlap those of the next.
+        // A warp reuses only its own slots (kSfSlots is a multiple of kSfWarps).
         // This CTA's words of a group (its A rows, all BN columns of B) land in a
         // slot by cp.async, up to kSfLookahead groups ahead of the group being
         // copied to TMEM: plain loads keep the TMA unit to the operand tiles and
@@ -454,15 +458,22 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         // 128-word chunk; for MP=128 the two halves of N are rows 0-31 and
         // 32-63), so the words need no reordering.  A word past the packed row
         // length reads nothing and lands as zero.
+        constexpr int NW = Cfg::kSfWarps;
+        static_assert(NSF % NW == 0, "scale slots per warp");
+        const int sw = static_cast<int>(warp) - Cfg::kSfWarp;
         const uint32_t leader_peer = mapa_shared(smem_u32(sf_peer_bar), 0);
-        int lt = pair_id, lj = 0;   // tile and group of the next load
-        int gl = 0;                 // groups whose loads are issued
+        // this pair's groups: tiles pair_id, pair_id + num_pairs, ... times groups_per_tile
+        const int num_groups_here =
+            pair_id < num_tiles ? (num_tiles - pair_id + num_pairs - 1) / num_pairs * groups_per_tile : 0;
+        int lt = pair_id, lj = sw;  // tile and group of the next load
+        while (lj >= groups_per_tile) { lj -= groups_per_tile; lt += num_pairs; }
+        int gl = sw;                // next group to load (this warp's: sw, sw + NW, ...)
         int st_t = -1;              // tile whose coordinates st holds
         PairTile st;
         // issues the loads of group gl, or an empty commit group past the last one;
         // false if the CTA is aborting
         auto load_group = [&]() -> bool {
-            if (lt < num_tiles) {
+            if (gl < num_groups_here) {
                 const int slot = gl % NSF;
                 // the slot's previous words have been copied to TMEM
                 if (gl >= NSF &&
@@ -502,60 +513,58 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                           st.n0 + h * kHalf + 32 * q + static_cast<int>(lane), yb,
                                           128 + 4 * (32 * h + lane) + q);
                 }
-                if (++lj == groups_per_tile) { lj = 0; lt += num_pairs; }
+                lj += NW;
+                while (lj >= groups_per_tile) { lj -= groups_per_tile; lt += num_pairs; }
             }
             cp_async_commit();
-            ++gl;
+            gl += NW;
             return true;
         };
-        int g = 0;
         bool copied = false;
-        for (int t = pair_id; t < num_tiles; t += num_pairs) {
-            for (int j = 0; j < groups_per_tile; ++j, ++g) {
-                const int slot = g % NSF;
-                // up to two more groups, kSfLookahead ahead at most; the first group
-                // starts at once
-                for (int i = 0; i < 2 && gl <= g + Cfg::kSfLookahead; ++i)
-                    if (!load_group()) goto sf_done;
-                cp_async_wait_dyn(gl - g - 1);                // this lane's words of group g
-                fence_proxy_async_smem();                     // visible to tcgen05.cp
-                __syncwarp();
-                uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
-                uint32_t *sfb_buf = sfa_buf + 128;
-                if (!leader) {
-                    // tell the leader this CTA's words for the group are in place
-                    if (lane == 0) mbar_arrive_remote(leader_peer + slot * 8);
-                } else {
-                    const int tslot = g % NTS;
-                    if (!mbar_wait_cluster_warp(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
-                        goto sf_done;
-                    if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                        goto sf_done;
-                    if (lane == 0) {
-                        tc_fence_after_sync();
-                        const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
-                        tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
-                        if constexpr (MP == 256) {
+        for (int g = sw; g < num_groups_here; g += NW) {
+            const int slot = g % NSF;
+            // up to two more of this warp's groups, kSfLookahead ahead at most;
+            // the first group starts at once
+            for (int i = 0; i < 2 && gl <= g + Cfg::kSfLookahead; ++i)
+                if (!load_group()) goto sf_done;
+            cp_async_wait_dyn((gl - g) / NW - 1);         // this lane's words of group g
+            fence_proxy_async_smem();                     // visible to tcgen05.cp
+            __syncwarp();
+            uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
+            uint32_t *sfb_buf = sfa_buf + 128;
+            if (!leader) {
+                // tell the leader this CTA's words for the group are in place
+                if (lane == 0) mbar_arrive_remote(leader_peer + slot * 8);
+            } else {
+                const int tslot = g % NTS;
+                if (!mbar_wait_cluster_warp(&sf_peer_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT))
+                    goto sf_done;
+                if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                    goto sf_done;
+                if (lane == 0) {
+                    tc_fence_after_sync();
+                    const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
+                    tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+                    if constexpr (MP == 256) {
 #pragma unroll
-                            for (int c = 0; c < Cfg::kSfbChunks; ++c)
-                                tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
-                                                          make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
-                        } else {
-                            tc_cp_64x128b_warpx2_01_23_pair(sfa_tmem + 4, make_desc_sf_32x128b(smem_u32(sfb_buf)));
-                        }
-                        tc_commit_pair(&sf_ready_bar[tslot], 0x1);
-                        tc_commit_pair(&sf_sfree_bar[slot], 0x3);   // both CTAs may refill the slot
-                        copied = true;
+                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                            tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
+                                                      make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                    } else {
+                        tc_cp_64x128b_warpx2_01_23_pair(sfa_tmem + 4, make_desc_sf_32x128b(smem_u32(sfb_buf)));
                     }
+                    tc_commit_pair(&sf_ready_bar[tslot], 0x1);
+                    tc_commit_pair(&sf_sfree_bar[slot], 0x3);   // both CTAs may refill the slot
+                    copied = true;
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
     sf_done:
         cp_async_wait<0>();
         if (lane == 0 && leader && copied) {
-            tc_commit_pair(&drain_bar[1], 0x1);
-            mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
+            tc_commit_pair(&drain_bar[1 + sw], 0x1);
+            mbar_wait(&drain_bar[1 + sw], 0, ctl, DG_DEV_TIMEOUT);
         }
         __syncwarp();
     } else {
