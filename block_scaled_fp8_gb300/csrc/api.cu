@@ -269,6 +269,16 @@ int choose_skinny_pair_block_n(const GemmParams &p, int bn1, int num_sms) {
     return best_bn;
 }
 
+// The packed scale words are read by the kernels' scale warps (cp.async), not by TMA.
+void set_scale_words(GemmParams &p, const BsOperands &o) {
+    p.sfa_words = static_cast<const uint32_t *>(o.sfa);
+    p.sfb_words = static_cast<const uint32_t *>(o.sfb);
+    p.sfa_ld = static_cast<int>(align4(o.sfa_mn));
+    p.sfb_ld = static_cast<int>(align4(o.sfb_mn));
+    p.sfa_slices = static_cast<int>(o.sfa_slices);
+    p.sfb_slices = static_cast<int>(o.sfb_slices);
+}
+
 // One launch of the pair kernel with mp rows per pair tile and BLOCK_N bn;
 // max_units bounds the number of mp-row units (the grid size).
 dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_t max_units,
@@ -297,13 +307,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                     32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
-    // the scale words are read by the kernel's scale warps (cp.async), not by TMA
-    p.sfa_words = static_cast<const uint32_t *>(o.sfa);
-    p.sfb_words = static_cast<const uint32_t *>(o.sfb);
-    p.sfa_ld = static_cast<int>(align4(o.sfa_mn));
-    p.sfb_ld = static_cast<int>(align4(o.sfb_mn));
-    p.sfa_slices = static_cast<int>(o.sfa_slices);
-    p.sfb_slices = static_cast<int>(o.sfb_slices);
+    set_scale_words(p, o);
     // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused)
     if (p.mode != kModeMasked) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
@@ -377,15 +381,10 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
         ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
-    ok &= encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfa, o.sfa_mn, o.sfa_slices,
-                    align4(o.sfa_mn) * 4, kBlockM, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
-    ok &= encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, o.sfb, o.sfb_mn, o.sfb_slices,
-                    align4(o.sfb_mn) * 4, bn, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
     ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                     32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
+    set_scale_words(p, o);
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
     p.cluster = cluster;

@@ -40,8 +40,8 @@ struct GemmParams {
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
-    // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the pair
-    // kernel's scale warps read them with cp.async
+    // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the
+    // block-scaled kernels' scale warps read them with cp.async
     const uint32_t *sfa_words;
     const uint32_t *sfb_words;
     int sfa_ld, sfb_ld;
@@ -53,7 +53,7 @@ struct GemmParams {
 };
 
 struct TensorMaps {
-    CUtensorMap a, b, sfa, sfb, d;
+    CUtensorMap a, b, d;
 };
 
 // Per-instantiation launch information.

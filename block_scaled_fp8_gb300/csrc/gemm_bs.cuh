@@ -39,16 +39,17 @@ namespace dg {
 template <int BN>
 struct BsConfig {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128 is 16..256, step 16");
-    static constexpr int kThreads = 352;
+    static constexpr int kThreads = 384;
     static constexpr int kEpiWarps = 8;
-    static constexpr int kSfWarp = 10;
+    static constexpr int kSfWarp = 10;                          // first scale warp
+    static constexpr int kSfWarps = 2;                          // they take alternate groups
     static constexpr int kSfbChunks = (BN + 127) / 128;        // 128-word tcgen05.cp chunks
     static constexpr int kSfCols = 4 + 4 * kSfbChunks;          // TMEM columns per scale slot
-    // Scale words pass through kSfSlots shared-memory slots (TMA destination,
-    // reordered in place) and kSfTmemSlots TMEM slots (what the MMA reads).  The
-    // producer loads them kSfLookahead groups ahead of its A/B group: they queue
-    // behind the A/B tiles in the TMA unit, and the copy into TMEM queues behind
-    // the issued MMAs, so both must start well before the MMAs need the group.
+    // Scale words pass through kSfSlots shared-memory slots (cp.async destination,
+    // already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what the MMA
+    // reads).  The scale warps load a group up to kSfLookahead groups before
+    // they copy it to TMEM: the load takes a global-memory latency and the copy
+    // into TMEM queues behind the issued MMAs.
     static constexpr int kSfSlots = 8;
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots = 4;
@@ -58,7 +59,6 @@ struct BsConfig {
     static constexpr int kSfaBytes = 512;                       // 128 words
     static constexpr int kSfbBytes = 512 * kSfbChunks;
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
-    static constexpr int kSfTxBytes = kSfaBytes + BN * 4;
     static constexpr int kEpiChunk = 16;                        // columns per epilogue chunk
     static constexpr int kNumChunks = BN / kEpiChunk;
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
@@ -84,25 +84,15 @@ struct BsConfig {
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
+    // full, empty, tfull, tempty, sfree, sf_ready, sf_tfree, drain; then the TMEM
+    // holder and abort flag (16 bytes), all inside the 512-byte barrier region
+    static constexpr int kNumBars = 2 * kRing + 2 * kNumAcc + kSfSlots + 2 * kSfTmemSlots + 1 + kSfWarps;
+    static_assert(kNumBars * 8 + 16 <= 512, "barrier region");
 };
 
-// Reorder 128 scale words (row i at word i, as TMA lands them from the
-// MN-major tensor) into the 32x128b tcgen05.cp source layout: 16-byte row r
-// holds the words of MN rows r, r+32, r+64, r+96.  After the copy, TMEM lane
-// r (in each 32-lane sub-partition) column j holds the word of row 32*j + r,
-// which is where the block-scaled MMA reads the scale of row (or column)
-// 32*j + r.  One warp; in place.  The XOR spreads the accesses over the banks.
-__device__ __forceinline__ void sf_transpose_for_cp(uint32_t *buf, uint32_t lane) {
-    uint32_t v[4];
-#pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) v[i] = buf[((i ^ (lane >> 3)) & 3) * 32 + lane];
-    __syncwarp();
-#pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) buf[lane * 4 + ((i ^ (lane >> 3)) & 3)] = v[i];
-}
-
-// Walks the (tile, 4-K-block group) sequence of one cluster in scheduler order;
-// the producer runs it ahead of the A/B stream to prefetch scale words.
+// Walks the (tile, 4-K-block group) sequence of one cluster in scheduler order,
+// skipping tiles with nothing to compute; the scale warps run one to load and one
+// to copy.
 template <int BN>
 struct GroupCursor {
     const GemmParams *p;
@@ -132,8 +122,6 @@ template <int BN, bool WITH_C>
 __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     dg_bs_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                       const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ CUtensorMap tm_sfa,
-                      const __grid_constant__ CUtensorMap tm_sfb,
                       const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
     using Cfg = BsConfig<BN>;
     constexpr int S = Cfg::kStages;
@@ -155,12 +143,11 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     uint64_t *empty_bar = bars + R;                   // [R]   a slot's stages consumed by the MMAs
     uint64_t *tfull_bar = bars + 2 * R;               // [NUM_ACC] accumulator complete
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] accumulator drained
-    uint64_t *sf_full_bar = tempty_bar + NUM_ACC;     // [NSF] scale words landed in smem
-    uint64_t *sf_sfree_bar = sf_full_bar + NSF;       // [NSF] scale words copied out of the slot
+    uint64_t *sf_sfree_bar = tempty_bar + NUM_ACC;    // [NSF] scale words copied out of the slot
     uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] scale words in TMEM
     uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] MMAs done with the TMEM slot
-    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [2]  MMA warp, scale warp
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 2);
+    uint64_t *drain_bar = sf_tfree_bar + NTS;         // [1 + kSfWarps]  MMA warp, scale warps
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1 + Cfg::kSfWarps);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
 
@@ -179,12 +166,13 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
         // initialise them, each fencing its own inits.  Every CTA of a cluster frees
         // an empty slot; both epilogue halves drain an accumulator.
-        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 2;
-        for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
+        const int num_bars = static_cast<int>(drain_bar + 1 + Cfg::kSfWarps - bars);  // <= Cfg::kNumBars
+        for (int i = static_cast<int>(lane); i < num_bars; i += 32) {
+            uint64_t *b = bars + i;
             uint32_t count = 1;
-            if (i >= R && i < 2 * R) count = csize;
-            if (i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC) count = Cfg::kEpiWarps;
-            mbar_init(&bars[i], count);
+            if (b >= empty_bar && b < empty_bar + R) count = csize;
+            if (b >= tempty_bar && b < tempty_bar + NUM_ACC) count = Cfg::kEpiWarps;
+            mbar_init(b, count);
         }
         if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
@@ -192,8 +180,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
-        tma_prefetch_desc(&tm_sfa);
-        tma_prefetch_desc(&tm_sfb);
         tma_prefetch_desc(&tm_d);
     }
     if (warp == 1) {
@@ -208,7 +194,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t sf_col0 = NUM_ACC * BN;
     const int num_tiles = total_tiles(p, prefix);
-    const int groups_per_tile = psf_k;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (whole warp)
@@ -216,40 +201,11 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
-        GroupCursor<BN> sfc;
-        sfc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
-        int gs = 0;          // scale groups issued
-        int ga = 0;          // A/B groups started
-        uint32_t sf_issued = 0;
-        // issues the scale words of group gs; false if the CTA is aborting
-        auto issue_sf = [&]() -> bool {
-            const int sslot = gs % NSF;
-            if (!mbar_wait_warp(&sf_sfree_bar[sslot], ((gs / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT)) return false;
-            if (elect_one()) {
-                uint8_t *sbuf = smem_sf + sslot * Cfg::kSfSlotBytes;
-                mbar_arrive_expect_tx(&sf_full_bar[sslot], Cfg::kSfTxBytes);
-                tma_load_2d(sbuf, &tm_sfa, &sf_full_bar[sslot], sfc.tile.sfa_x, sfc.tile.sfa_y0 + sfc.j);
-                tma_load_2d(sbuf + Cfg::kSfaBytes, &tm_sfb, &sf_full_bar[sslot], sfc.tile.n0,
-                            sfc.tile.sfb_y0 + sfc.j);
-            }
-            __syncwarp();
-            sf_issued |= 1u << sslot;
-            ++gs;
-            sfc.next();
-            return true;
-        };
         for (int t = cluster_id; t < num_tiles; t += num_clusters) {
             Tile tile;
             if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, lane == 0)) continue;
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
-                if ((kb0 & 3) == 0) {
-                    // the group's own scale words, where the lookahead has not issued them
-                    // (the first group): ahead of its A/B tiles
-                    while (sfc.valid && gs <= ga)
-                        if (!issue_sf()) goto prod_done;
-                    ++ga;
-                }
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                 if (drop) {
                     drop = false;  // diagnostic: leave this slot empty
@@ -293,10 +249,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     issued |= 1u << slot;
                 }
                 if (++slot == R) { slot = 0; phase ^= 1; }
-                // then up to two more scale groups per slot until they run kSfLookahead
-                // groups ahead: the first A/B tiles go out without waiting behind them
-                for (int i = 0; i < 2 && sfc.valid && gs <= ga - 1 + Cfg::kSfLookahead; ++i)
-                    if (!issue_sf()) goto prod_done;
             }
         }
     prod_done:
@@ -305,12 +257,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             for (int s = 0; s < R; ++s)
                 if (issued & (1u << s))
                     mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
-            for (int j = 0; j < NSF; ++j)
-                if (sf_issued & (1u << j)) {
-                    // last use of slot j was group g = the largest g < gs with g % NSF == j
-                    const int g = gs - 1 - ((gs - 1 - j) % NSF + NSF) % NSF;
-                    mbar_wait(&sf_full_bar[j], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT);
-                }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -384,46 +330,90 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
             mbar_wait(&drain_bar[0], 0, ctl, DG_DEV_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp == Cfg::kSfWarp) {
-        // ------------------------------------------------------------ scale-factor warp
-        int g = 0;
-        bool copied = false;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-            Tile tile;
-            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
-            for (int j = 0; j < groups_per_tile; ++j, ++g) {
-                const int slot = g % NSF;
-                const int tslot = g % NTS;
-                if (!mbar_wait_warp(&sf_full_bar[slot], (g / NSF) & 1, ctl, DG_DEV_TIMEOUT)) goto sf_done;
-                uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
-                uint32_t *sfb_buf = sfa_buf + 128;
-                sf_transpose_for_cp(sfa_buf, lane);
+    } else if (warp >= Cfg::kSfWarp) {
+        // ------------------------------------------------------------ scale-factor warps
+        // kSfWarps warps take the (tile, 4-K-block group) sequence in turns, so
+        // the waits and tcgen05 issues of one group overlap those of the next; a
+        // warp reuses only its own slots.  A group's words land in its slot by
+        // cp.async, up to kSfLookahead groups ahead of the group being copied to
+        // TMEM, each 4-byte copy at the position tcgen05.cp reads it from (source
+        // row r holds words r, r+32, r+64, r+96 of a 128-word chunk).  A word
+        // past the packed row length reads nothing and lands as zero.
+        constexpr int NW = Cfg::kSfWarps;
+        static_assert(NSF % NW == 0, "scale slots per warp");
+        const int sw = static_cast<int>(warp) - Cfg::kSfWarp;
+        GroupCursor<BN> lc, gc;   // next group to load, next group to copy
+        lc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+        gc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+        for (int i = 0; i < sw; ++i) { lc.next(); gc.next(); }
+        int gl = sw;              // index of lc's group
+        // issues the loads of group gl, or an empty commit group past the last one;
+        // false if the CTA is aborting
+        auto load_group = [&]() -> bool {
+            if (lc.valid) {
+                const int slot = gl % NSF;
+                // the slot's previous words have been copied to TMEM
+                if (gl >= NSF &&
+                    !mbar_wait_warp(&sf_sfree_bar[slot], ((gl / NSF) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                    return false;
+                const uint32_t dst0 = smem_u32(smem_sf + slot * Cfg::kSfSlotBytes);
+                auto copy_word = [&](const uint32_t *base, int ld, int slices, int x, int y, uint32_t w) {
+                    const bool in = x < ld && y < slices;
+                    cp_async_4(dst0 + 4u * w, in ? base + static_cast<int64_t>(y) * ld + x : base, in ? 4u : 0u);
+                };
+                const int ya = lc.tile.sfa_y0 + lc.j, yb = lc.tile.sfb_y0 + lc.j;
 #pragma unroll
-                for (int c = 0; c < Cfg::kSfbChunks; ++c) sf_transpose_for_cp(sfb_buf + c * 128, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                // the MMAs of the TMEM slot's previous group have completed
-                if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
-                    goto sf_done;
-                if (lane == 0) {
-                    tc_fence_after_sync();
-                    const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
-                    tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+                for (int q = 0; q < 4; ++q)
+                    copy_word(p.sfa_words, p.sfa_ld, p.sfa_slices, lc.tile.sfa_x + 32 * q + static_cast<int>(lane),
+                              ya, 4 * lane + q);
 #pragma unroll
-                    for (int c = 0; c < Cfg::kSfbChunks; ++c)
-                        tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c,
-                                             make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
-                    tc_commit(&sf_ready_bar[tslot]);
-                    tc_commit(&sf_sfree_bar[slot]);   // the producer may refill the slot
-                    copied = true;
-                }
-                __syncwarp();
+                for (int c = 0; c < Cfg::kSfbChunks; ++c)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
+                                  lc.tile.n0 + 128 * c + 32 * q + static_cast<int>(lane), yb,
+                                  128 + 128 * c + 4 * lane + q);
+                for (int i = 0; i < NW; ++i) lc.next();
             }
+            cp_async_commit();
+            gl += NW;
+            return true;
+        };
+        bool copied = false;
+        for (int g = sw; gc.valid; g += NW) {
+            const int slot = g % NSF;
+            const int tslot = g % NTS;
+            // up to two more of this warp's groups, kSfLookahead ahead at most; the
+            // first group starts at once
+            for (int i = 0; i < 2 && gl <= g + Cfg::kSfLookahead; ++i)
+                if (!load_group()) goto sf_done;
+            cp_async_wait_dyn((gl - g) / NW - 1);         // this lane's words of group g
+            fence_proxy_async_smem();                     // visible to tcgen05.cp
+            __syncwarp();
+            uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
+            uint32_t *sfb_buf = sfa_buf + 128;
+            // the MMAs of the TMEM slot's previous group have completed
+            if (!mbar_wait_warp(&sf_tfree_bar[tslot], ((g / NTS) & 1) ^ 1, ctl, DG_DEV_TIMEOUT))
+                goto sf_done;
+            if (lane == 0) {
+                tc_fence_after_sync();
+                const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
+                tc_cp_32x128b_warpx4(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+#pragma unroll
+                for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                    tc_cp_32x128b_warpx4(sfa_tmem + 4 + 4 * c, make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
+                tc_commit(&sf_ready_bar[tslot]);
+                tc_commit(&sf_sfree_bar[slot]);   // the slot may be loaded again
+                copied = true;
+            }
+            __syncwarp();
+            for (int i = 0; i < NW; ++i) gc.next();
         }
     sf_done:
+        cp_async_wait<0>();
         if (lane == 0 && copied) {
-            tc_commit(&drain_bar[1]);
-            mbar_wait(&drain_bar[1], 0, ctl, DG_DEV_TIMEOUT);
+            tc_commit(&drain_bar[1 + sw]);
+            mbar_wait(&drain_bar[1 + sw], 0, ctl, DG_DEV_TIMEOUT);
         }
         __syncwarp();
     } else {
@@ -562,7 +552,7 @@ cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int
     if (e != cudaSuccess) return e;
     if (p.cluster <= 1) {
         dg_bs_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-            maps.a, maps.b, maps.sfa, maps.sfb, maps.d, p);
+            maps.a, maps.b, maps.d, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -577,8 +567,7 @@ cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.sfa, maps.sfb,
-                              maps.d, p);
+    return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.d, p);
 }
 
 // Largest number of clusters of `cluster` CTAs that can be resident at once.

@@ -90,6 +90,10 @@ struct Bs2Config {
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
+    // full, empty, tfull, tempty, sf_peer, sfree, sf_ready, sf_tfree, drain; then
+    // the TMEM holder and abort flag, all before the unit prefix 512 bytes on
+    static constexpr int kNumBars = 2 * kRing + 2 * kNumAcc + 2 * kSfSlots + 2 * kSfTmemSlots + 1 + kSfWarps;
+    static_assert(kNumBars * 8 + 8 <= 512, "barrier region");
 };
 
 struct PairTile {
@@ -298,10 +302,10 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     if (warp == 0) {
         // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
         // initialise them, each fencing its own inits
-        constexpr int kNumBars = 2 * R + 2 * NUM_ACC + 2 * NSF + 2 * NTS + 1 + Cfg::kSfWarps;
-        for (int i = static_cast<int>(lane); i < kNumBars; i += 32) {
-            const bool is_tempty = i >= 2 * R + NUM_ACC && i < 2 * R + 2 * NUM_ACC;
-            mbar_init(&bars[i], is_tempty ? 2 * Cfg::kEpiWarps : 1);
+        const int num_bars = static_cast<int>(drain_bar + 1 + Cfg::kSfWarps - bars);  // <= Cfg::kNumBars
+        for (int i = static_cast<int>(lane); i < num_bars; i += 32) {
+            uint64_t *b = bars + i;
+            mbar_init(b, b >= tempty_bar && b < tempty_bar + NUM_ACC ? 2 * Cfg::kEpiWarps : 1);
         }
         if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
