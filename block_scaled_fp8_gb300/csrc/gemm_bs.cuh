@@ -187,11 +187,19 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         tmem_relinquish();
     }
     if (p.mode == kModeMasked) build_masked_prefix(p, prefix);
-    tc_fence_before_sync();
-    __syncthreads();
-    if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_holder;
+    // Without a cluster the producer waits for nobody: it signals that the barriers
+    // are initialised and starts loading while the others wait for the TMEM
+    // allocation (and the masked prefix, which it then waits for too).
+    const bool producer_early = csize == 1 && p.mode != kModeMasked;
+    if (producer_early && warp == 0) {
+        named_bar_arrive(1, Cfg::kThreads);
+    } else {
+        tc_fence_before_sync();
+        named_bar_sync(1, Cfg::kThreads);
+        if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast
+        tc_fence_after_sync();
+    }
+    const uint32_t tmem_base = warp != 0 ? *tmem_holder : 0u;
     const uint32_t sf_col0 = NUM_ACC * BN;
     const int num_tiles = total_tiles(p, prefix);
 

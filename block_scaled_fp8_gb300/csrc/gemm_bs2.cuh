@@ -322,10 +322,13 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         tmem_alloc_pair(tmem_holder, Cfg::kTmemCols);
         tmem_relinquish_pair();
     }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_holder;
+    // the producer needs no TMEM: it starts loading while the others wait for the allocation
+    if (warp != 0) {
+        tc_fence_before_sync();
+        named_bar_sync(1, Cfg::kThreads - 32);
+        tc_fence_after_sync();
+    }
+    const uint32_t tmem_base = warp != 0 ? *tmem_holder : 0u;
     const uint32_t sf_col0 = NUM_ACC * ACC;
     const int num_units = pair_units(p, prefix);
     const int num_tiles = num_units * p.num_n_blocks;
