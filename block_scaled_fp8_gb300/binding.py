@@ -25,6 +25,7 @@ DG_DEV_BAD_GROUP = 4
 DG_DEBUG_DROP_ONE_LOAD = 1
 DG_DEBUG_PRINT_CONFIGS = 2
 DG_DEBUG_SINGLE_CTA = 4
+DG_DEBUG_WIDE_PAIR = 8
 
 # Every symbol include/dg.h declares.
 EXPORTS = (

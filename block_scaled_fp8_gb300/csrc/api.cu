@@ -203,9 +203,9 @@ bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
 
 int cached_max_pairs(int bn, bool with_c, int mp) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][257];
+    static int cache[kMaxDevices][2][2][513];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn > 256) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn <= 0 || bn > 512) return 0;
     std::lock_guard<std::mutex> lock(mu);
     int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][bn];
     if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp);
@@ -228,8 +228,15 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
         const char *e = std::getenv("DG_PAIR_BLOCK_N");
         return e ? std::atoi(e) : 0;
     }();
-    for (int cand : {128, 192, 224, 240, 256}) {
+    if ((g_debug_flags.load() & DG_DEBUG_WIDE_PAIR) && !with_c) {
+        KernelInfo ki;
+        if (get_bs2_kernel_info(384, false, 256, &ki) && usable_pairs(384, false, 256, num_sms) > 0) return 384;
+    }
+    for (int cand : {128, 192, 224, 240, 256, 384}) {
         if (forced_bn && cand != forced_bn) continue;
+        // 384-column tiles: dense GEMMs only (3 % slower on the contiguous MoE shape
+        // with N=4096, K=7168)
+        if (cand > 256 && p.mode != kModeDense && !forced_bn) continue;
         KernelInfo ki;
         if (!get_bs2_kernel_info(cand, with_c, 256, &ki)) continue;
         const int pairs = usable_pairs(cand, with_c, 256, num_sms);
@@ -237,9 +244,11 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
         const int64_t nb = cdiv64(p.n, cand);
         const int64_t tiles = m_pairs * nb;
         const int64_t waves = cdiv64(tiles, pairs);
-        const double score = static_cast<double>(tiles) / static_cast<double>(waves * pairs) *
-                             static_cast<double>(p.n) / static_cast<double>(nb * cand) *
-                             (cand / (cand + 64.0));
+        double score = static_cast<double>(tiles) / static_cast<double>(waves * pairs) *
+                       static_cast<double>(p.n) / static_cast<double>(nb * cand) * (cand / (cand + 64.0));
+        // with one accumulator the MMAs stop for about 1.5 K-blocks per tile while the
+        // epilogue reads the accumulator out
+        if (ki.num_acc == 1) score *= 1.0 - 1.5 / static_cast<double>(cdiv64(p.k, kBlockK));
         if (score > best + 1e-9) { best = score; bn = cand; }
     }
     return bn;
@@ -294,16 +303,25 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     bool ok = true;
     // K a multiple of 128: one 3-D load per operand fills a ring slot
     p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
+    // a tile wider than 256 columns runs two MMAs (256 and bn - 256 columns); each CTA
+    // loads half of each one's B rows through its own map
+    const uint32_t b1_rows = static_cast<uint32_t>((bn > 256 ? 256 : bn) / 2);
+    const uint32_t b2_rows = static_cast<uint32_t>(bn > 256 ? (bn - 256) / 2 : 0);
     if (p.ab_3d) {
         const uint64_t kblocks = static_cast<uint64_t>(k / kBlockK);
         ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, a_rows, info.group_kb);
-        ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, bn / 2, info.group_kb);
+        ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, b1_rows, info.group_kb);
+        if (b2_rows) ok &= encode_kblocked_3d(&maps.b2, o.b, o.b_rows, o.ldb, kblocks, b2_rows, info.group_kb);
     } else {
         ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
                         a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
-                        bn / 2, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                        b1_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (b2_rows)
+            ok &= encode_2d(&maps.b2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
+                            b2_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
+    if (!b2_rows) maps.b2 = maps.b;   // not read
     ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                     32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;

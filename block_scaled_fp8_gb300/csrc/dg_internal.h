@@ -54,6 +54,7 @@ struct GemmParams {
 
 struct TensorMaps {
     CUtensorMap a, b, d;
+    CUtensorMap b2;   // pair tiles wider than 256 columns: the second MMA's rows of B
 };
 
 // Per-instantiation launch information.
@@ -63,6 +64,7 @@ struct KernelInfo {
     int smem_bytes;
     int threads;
     int group_kb;   // K-blocks per ring slot (the depth of a 3-D A/B load)
+    int num_acc;    // TMEM accumulators (1: the next tile's MMAs wait for the epilogue's reads)
 };
 
 // Block-scaled (UE8M0) tcgen05 kernel family: returns false if block_n is not

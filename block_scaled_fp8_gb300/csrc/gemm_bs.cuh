@@ -609,6 +609,7 @@ void fill_bs_info(KernelInfo *info) {
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
     info->group_kb = Cfg::kGroupKb;
+    info->num_acc = Cfg::kNumAcc;
 }
 
 }  // namespace dg

@@ -41,7 +41,15 @@ struct Bs2Config {
     // with MP=128 each half of N is whole 16-column epilogue chunks
     static_assert(MP == 256 || MP == 128, "pair tile rows");
     static_assert(MP == 256 ? (BN % 16 == 0 && BN >= 64) : (BN % 32 == 0 && BN >= 32), "tile columns");
-    static_assert(BN <= 256, "N <= 256");
+    static_assert(BN <= 256 || MP == 256, "wide tiles are 256-row tiles");
+    // A pair MMA takes N <= 256: a wider tile issues a second MMA for columns
+    // [kBN1, BN).  Each CTA holds kB1Rows + kB2Rows rows of B: its half of each
+    // MMA's columns, in two regions (one TMA box each).
+    static constexpr int kBN1 = BN > 256 ? 256 : BN;
+    static constexpr int kBN2 = BN - kBN1;
+    static_assert(kBN2 == 0 || (kBN2 % 16 == 0 && kBN2 <= 256), "second MMA columns");
+    static constexpr int kB1Rows = kBN1 / 2;
+    static constexpr int kB2Rows = kBN2 / 2;
     static constexpr int kThreads = 384;
     static constexpr int kEpiWarps = 8;
     static constexpr int kSfWarp = 10;                           // first scale warp
@@ -66,7 +74,9 @@ struct Bs2Config {
     static constexpr int kSfTmemSlots =
         (2 * kAccCols + 4 * kSfCols <= 512 || 2 * kAccCols + 2 * kSfCols > 512) ? 4 : 2;
     static constexpr int kABytes = kARows * kBlockK;            // this CTA's rows of A
-    static constexpr int kBBytes = (BN / 2) * kBlockK;          // this CTA's half of B
+    static constexpr int kB1Bytes = kB1Rows * kBlockK;
+    static constexpr int kB2Bytes = kB2Rows * kBlockK;
+    static constexpr int kBBytes = kB1Bytes + kB2Bytes;         // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = 512 * kSfbChunks;
@@ -101,7 +111,8 @@ struct PairTile {
     int sfa_x;       // MN index of that row in the packed SFA view
     int sfa_y0;      // row of the packed SFA view for K-slice 0
     int n0;          // first output column of the tile
-    int b_row0;      // this CTA's first row of B ([E*N, K] view): its half of the tile's columns
+    int b_row0;      // this CTA's first row of B ([E*N, K] view): its half of the first MMA's columns
+    int b2_row0;     // and of the second MMA's (tiles wider than 256 columns)
     int sfb_y0;      // row of the packed SFB view for K-slice 0
     int valid_rows;  // rows of this CTA's MP/2 that are stored (0: none)
 };
@@ -248,7 +259,8 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
         tile.sfa_y0 = e * psf_k;
         tile.valid_rows = v <= 0 ? 0 : (v < kBlockM ? v : kBlockM);
     }
-    tile.b_row0 = group * p.n + tile.n0 + rank * (BN / 2);
+    tile.b_row0 = group * p.n + tile.n0 + rank * Bs2Config<BN, MP>::kB1Rows;
+    tile.b2_row0 = group * p.n + tile.n0 + Bs2Config<BN, MP>::kBN1 + rank * Bs2Config<BN, MP>::kB2Rows;
     tile.sfb_y0 = group * psf_k;
 }
 
@@ -256,6 +268,7 @@ template <int BN, bool WITH_C, int MP>
 __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
+                       const __grid_constant__ CUtensorMap tm_b2,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
     using Cfg = Bs2Config<BN, MP>;
     constexpr int S = Cfg::kStages;
@@ -313,6 +326,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        if constexpr (Cfg::kBN2 > 0) tma_prefetch_desc(&tm_b2);
         tma_prefetch_desc(&tm_d);
     }
     if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo);  // ends with __syncthreads
@@ -355,17 +369,26 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         // end of K are out of bounds (zero-filled) and still count their bytes
                         if (elect_one()) {
                             if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * G * Cfg::kStageBytes);
+                            uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
                             tma_load_3d_pair(smem_a + slot * G * Cfg::kABytes, &tm_a, fb, 0, tile.a_row0, kb0);
-                            tma_load_3d_pair(smem_b + slot * G * Cfg::kBBytes, &tm_b, fb, 0, tile.b_row0, kb0);
+                            tma_load_3d_pair(b_slot, &tm_b, fb, 0, tile.b_row0, kb0);
+                            if constexpr (Cfg::kBN2 > 0)
+                                tma_load_3d_pair(b_slot + G * Cfg::kB1Bytes, &tm_b2, fb, 0, tile.b2_row0, kb0);
                         }
                     } else if (elect_one()) {
                         // the leader expects both CTAs' bytes; each CTA's loads count there
                         if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kStageBytes);
+                        // a slot's B: the G K-blocks of the first MMA's rows, then the G
+                        // K-blocks of the second's
                         auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
-                            const int stage = slot * G + j;
-                            tma_load_2d_pair(smem_a + stage * Cfg::kABytes, &tm_a, fb, kb * kBlockK, tile.a_row0);
-                            tma_load_2d_pair(smem_b + stage * Cfg::kBBytes, &tm_b, fb, kb * kBlockK, tile.b_row0);
+                            uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
+                            tma_load_2d_pair(smem_a + (slot * G + j) * Cfg::kABytes, &tm_a, fb, kb * kBlockK,
+                                             tile.a_row0);
+                            tma_load_2d_pair(b_slot + j * Cfg::kB1Bytes, &tm_b, fb, kb * kBlockK, tile.b_row0);
+                            if constexpr (Cfg::kBN2 > 0)
+                                tma_load_2d_pair(b_slot + G * Cfg::kB1Bytes + j * Cfg::kB2Bytes, &tm_b2, fb,
+                                                 kb * kBlockK, tile.b2_row0);
                         };
                         if (nk == G) {
 #pragma unroll
@@ -397,7 +420,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             int g = 0;
             const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
             const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
-            constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, BN, 0, 0);
+            constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, Cfg::kBN1, 0, 0);
+            constexpr uint32_t idesc2_base = make_idesc_mxf8(MMA_M, Cfg::kBN2 > 0 ? Cfg::kBN2 : 16, 0, 0);
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
                 if (!mbar_wait_cluster_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
@@ -422,11 +446,21 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             const uint32_t sf = static_cast<uint32_t>(kb & 3);
                             const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
                             const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
-                            const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kBBytes >> 4));
+                            const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kB1Bytes >> 4));
 #pragma unroll
-                            for (int k = 0; k < kBlockK / 32; ++k)
+                            for (int k = 0; k < kBlockK / 32; ++k) {
                                 tc_mma_mxf8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
                                                  sfa_tmem + 4, (kb | k) != 0);
+                                if constexpr (Cfg::kBN2 > 0) {
+                                    // columns [kBN1, BN): their accumulator columns, B rows and
+                                    // B scale cells (column x at lane x % 32, cell x / 32)
+                                    const uint64_t b2_desc =
+                                        b_desc0 + static_cast<uint64_t>((G * Cfg::kB1Bytes + j * Cfg::kB2Bytes) >> 4);
+                                    tc_mma_mxf8_pair(d_tmem + Cfg::kBN1, a_desc + 2 * k, b2_desc + 2 * k,
+                                                     idesc2_base | (sf << 4) | (sf << 29), sfa_tmem,
+                                                     sfa_tmem + 4 + Cfg::kBN1 / 32, (kb | k) != 0);
+                                }
+                            }
                         };
                         if (nk == G) {
 #pragma unroll
@@ -752,7 +786,7 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     dg_bs2_gemm_kernel<BN, WITH_C, MP><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-        maps.a, maps.b, maps.d, p);
+        maps.a, maps.b, maps.b2, maps.d, p);
     return cudaGetLastError();
 }
 
@@ -786,6 +820,7 @@ void fill_bs2_info(KernelInfo *info) {
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
     info->group_kb = Cfg::kGroupKb;
+    info->num_acc = Cfg::kNumAcc;
 }
 
 }  // namespace dg

@@ -15,6 +15,7 @@ template cudaError_t launch_bs2_gemm_impl<32, false, 128>(const TensorMaps &, co
 template cudaError_t launch_bs2_gemm_impl<64, false, 128>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
 template cudaError_t launch_bs2_gemm_impl<96, false, 128>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
 template cudaError_t launch_bs2_gemm_impl<128, false, 128>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
+template cudaError_t launch_bs2_gemm_impl<384, false, 256>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
 template int max_active_pairs_impl<128, false, 256>();
 template int max_active_pairs_impl<128, true, 256>();
 template int max_active_pairs_impl<192, false, 256>();
@@ -28,4 +29,5 @@ template int max_active_pairs_impl<32, false, 128>();
 template int max_active_pairs_impl<64, false, 128>();
 template int max_active_pairs_impl<96, false, 128>();
 template int max_active_pairs_impl<128, false, 128>();
+template int max_active_pairs_impl<384, false, 256>();
 }  // namespace dg

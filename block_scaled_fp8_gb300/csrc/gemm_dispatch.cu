@@ -23,7 +23,7 @@ DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #define DG_BS2_LIST(X)                                                                             \
     X(128, false, 256) X(128, true, 256) X(192, false, 256) X(192, true, 256) X(224, false, 256)      \
     X(224, true, 256) X(240, false, 256) X(240, true, 256) X(256, false, 256) X(32, false, 128)       \
-    X(64, false, 128) X(96, false, 128) X(128, false, 128)
+    X(64, false, 128) X(96, false, 128) X(128, false, 128) X(384, false, 256)
 #define DG_EXTERN2(BN, C, MP)                                                                      \
     extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP>(const TensorMaps &, const GemmParams &, \
                                                                 int, cudaStream_t);                      \

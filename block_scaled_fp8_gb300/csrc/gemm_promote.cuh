@@ -298,6 +298,7 @@ void fill_promote_info(KernelInfo *info) {
     info->smem_bytes = Cfg::kSmemBytes;
     info->threads = Cfg::kThreads;
     info->group_kb = 1;
+    info->num_acc = 1;
 }
 
 }  // namespace dg

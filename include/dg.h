@@ -189,8 +189,10 @@ void dg_set_wait_timeout_ms(int ms);
  * the flag clears itself after one launch).  DG_DEBUG_PRINT_CONFIGS prints
  * the chosen tile configuration of each GEMM to stderr.  DG_DEBUG_SINGLE_CTA
  * runs dense GEMMs on single CTAs (128-row tiles) where CTA pairs (256-row
- * tiles) would be chosen; results are bit-identical either way. */
-enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2, DG_DEBUG_SINGLE_CTA = 4 };
+ * tiles) would be chosen; results are bit-identical either way.
+ * DG_DEBUG_WIDE_PAIR makes 256-row pair GEMMs without C use 384-column tiles
+ * (two MMAs per K step), whatever the tile chooser would pick. */
+enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2, DG_DEBUG_SINGLE_CTA = 4, DG_DEBUG_WIDE_PAIR = 8 };
 void dg_set_debug_flags(uint32_t flags);
 
 /* Human-readable name of a dg_status value. */

@@ -19,13 +19,13 @@ pytestmark = [pytest.mark.gpu,
 DEV = "cuda"
 
 
-def _gemm(case, single_cta, c=None):
+def _gemm(case, single_cta, c=None, flags=0):
     M, N, K = case.shape
     sfa = binding.transform_sf(case.sfa.to(DEV), 1, M)
     sfb = binding.transform_sf(case.sfb.to(DEV), 128, N)
     d = torch.full((M, N), 3.0, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    binding.set_debug_flags(binding.DG_DEBUG_SINGLE_CTA if single_cta else 0)
+    binding.set_debug_flags((binding.DG_DEBUG_SINGLE_CTA if single_cta else 0) | flags)
     try:
         binding.dg_fp8_gemm_nt(case.a.to(DEV), sfa, case.b.to(DEV), sfb, d, c=c, status=status)
         cfg = binding.last_config()
@@ -87,6 +87,30 @@ def test_pair_full_compare_several_waves(orc):
     ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
                               sb_rows(case.sfb, N), rows, cols)
     assert_close(bf16_bits(d)[rows, cols], ref, "pair several waves")
+
+
+# ------------------------------------------------------------------ 384-column pair tiles
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (300, 520, 1024), (512, 1000, 336), (1000, 7168, 1536),
+                                   (2048, 4096, 640)])
+def test_wide_pair_matches_single_cta_and_oracle(orc, M, N, K):
+    """384-column tiles: two MMAs per K step (256 and 128 columns), each CTA
+    holding half of each one's B rows; one TMEM accumulator, so tiles after
+    the first wait for the epilogue.  Ragged N leaves the second MMA's rows
+    partly or wholly past the end of B; K=336 is not a multiple of 128."""
+    case = inputs.dense_case(M, N, K, seed=M + 2 * N + K, b_scale_exp_range=(-8, 4))
+    d_wide, cfg = _gemm(case, single_cta=False, flags=binding.DG_DEBUG_WIDE_PAIR)
+    d_one, _ = _gemm(case, single_cta=True)
+    assert cfg["kind"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 384, cfg
+    assert torch.equal(d_wide, d_one), f"{M}x{N}x{K}: 384-column pairs and single CTAs differ"
+    rng = np.random.default_rng(M + N)
+    rows = rng.integers(0, M, 3000)
+    cols = rng.integers(0, N, 3000)
+    rows[:4] = [0, 0, M - 1, M - 1]
+    cols[:4] = [0, N - 1, 0, N - 1]
+    ref = orc.gemm_nt_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                              sb_rows(case.sfb, N), rows, cols)
+    assert_close(bf16_bits(d_wide)[rows, cols], ref, f"wide pair {M}x{N}x{K}")
 
 
 # ------------------------------------------------------------------ grouped layouts on pairs
