@@ -186,6 +186,11 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         tmem_alloc(tmem_holder, Cfg::kTmemCols);
         tmem_relinquish();
     }
+    // Nothing above reads global memory: it overlaps the previous grid's tail when
+    // launched as a programmatic dependent.  From here on every thread may read
+    // inputs or write D.
+    grid_launch_dependents();
+    grid_dependency_wait();
     if (p.mode == kModeMasked) build_masked_prefix(p, prefix);
     // Without a cluster the producer waits for nobody: it signals that the barriers
     // are initialised and starts loading while the others wait for the TMEM
@@ -558,23 +563,21 @@ cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (p.cluster <= 1) {
-        dg_bs_gemm_kernel<BN, WITH_C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-            maps.a, maps.b, maps.d, p);
-        return cudaGetLastError();
-    }
+    // a programmatic dependent of the stream's previous grid; clusters along x for A multicast
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.cluster > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.d, p);
 }
 

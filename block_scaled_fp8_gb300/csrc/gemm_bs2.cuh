@@ -329,6 +329,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         if constexpr (Cfg::kBN2 > 0) tma_prefetch_desc(&tm_b2);
         tma_prefetch_desc(&tm_d);
     }
+    // Nothing above reads global memory: it overlaps the previous grid's tail when
+    // launched as a programmatic dependent.  From here on every thread may read
+    // inputs or write D.
+    grid_launch_dependents();
+    grid_dependency_wait();
     if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo);  // ends with __syncthreads
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
@@ -785,9 +790,19 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dg_bs2_gemm_kernel<BN, WITH_C, MP><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(
-        maps.a, maps.b, maps.b2, maps.d, p);
-    return cudaGetLastError();
+    // a programmatic dependent of the stream's previous grid (the cluster shape is
+    // the kernel's own)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP>, maps.a, maps.b, maps.b2, maps.d, p);
 }
 
 template <int BN, bool WITH_C, int MP>

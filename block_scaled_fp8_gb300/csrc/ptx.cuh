@@ -191,6 +191,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 }
 
 // All threads of all CTAs of the cluster (release/acquire ordering).
+// Programmatic dependent launch: let the next grid in the stream start launching
+// (its CTAs run up to their own wait), and wait until the grids this one depends
+// on have completed with their memory visible.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named CTA barrier `id` (1..15) over `count` threads: wait, or only arrive.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
