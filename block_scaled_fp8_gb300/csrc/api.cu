@@ -115,7 +115,7 @@ constexpr int kMaxBlockNWithC = 160;
 // (wave quantisation x N padding) weighted by a per-tile efficiency that grows
 // with BLOCK_N (larger tiles re-read less operand data per FLOP).  Split-K is
 // never used: with few M blocks, narrow BLOCK_N is what fills the SMs (the
-// non-power-of-two block idea of PaperTrace §4.3).
+// non-power-of-two block idea of "02 · DeepGEMM 技术解析" §4.3).
 int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c) {
     static const int forced_bn = [] {
         const char *e = std::getenv("DG_BLOCK_N");

@@ -11,9 +11,8 @@
 // Blackwell form of the pages' two-level accumulation, §13.3 point 1).
 //
 // CTA layout (one CTA per SM, persistent):
-//   warp 0      TMA producer: A and B per K-block, plus the packed scale words
-//               once per 4 K-blocks (one int32 holds 4 K-groups), into a ring
-//               of STAGES shared-memory stages (full/empty mbarriers).
+//   warp 0      TMA producer: A and B per K-block into a ring of STAGES
+//               shared-memory stages (full/empty mbarriers).
 //   warp 1      TMEM owner and MMA issuer: 4 MMAs (K=32 each) per stage; the
 //               scale byte of K-block kb is selected by the instruction's
 //               scale-factor id (kb % 4); signals the accumulator to the epilogue.
@@ -21,9 +20,10 @@
 //               at once), optional + C, bf16 RNE, swizzled staging in shared
 //               memory, TMA store (direct stores where masked rows end inside
 //               the tile).
-//   warp 10     scale-factor warp: re-orders each group's scale words for
-//               tcgen05.cp and copies them into a ring of TMEM scale slots,
-//               off the MMA issuer's critical path.
+//   warps 10-11 scale-factor warps, alternate 4-K-block groups: load the
+//               group's packed scale words (one int32 holds 4 K-groups) with
+//               cp.async in tcgen05.cp order, then copy them into a ring of
+//               TMEM scale slots, off the producer's and MMA issuer's paths.
 // Accumulators: NUM_ACC buffers of BLOCK_N TMEM columns each, so the next
 // tile's MMAs overlap this tile's stores.
 #pragma once

@@ -15,12 +15,15 @@
 //     and writes each CTA's rows of D into that CTA's TMEM;
 //   - each CTA's TMEM holds the A scales of its own rows and the B scales of
 //     all BN columns (lane n%32, column n/32; for MP=128 per half of N, see
-//     Bs2Config); tcgen05.cp.cta_group::2 copies each CTA's reordered words
+//     Bs2Config); tcgen05.cp.cta_group::2 copies each CTA's scale words
 //     into its own TMEM;
 //   - commits reach both CTAs (multicast), and the peer's epilogue and scale
-//     warps signal the leader's barriers through their cluster addresses.
+//     warps signal the leader's barriers through their cluster addresses;
+//   - tiles wider than 256 columns (MP=256) issue a second MMA per K step for
+//     columns [256, BN), from a second B region.
 // Ring slots group kGroupKb K-blocks under one barrier pair to keep the MMA
-// warp's per-K-block work below the tensor time.
+// warp's per-K-block work below the tensor time.  Roles: warp 0 producer,
+// warp 1 MMA issuer (leader), warps 2-9 epilogue, warps 10-11 scale words.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -61,10 +64,10 @@ struct Bs2Config {
     static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
     static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4);
     // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
-    // destination, reordered in place) and kSfTmemSlots TMEM slots (what the
-    // MMA reads).  The scale warp loads a group kSfLookahead groups before it
-    // copies it to TMEM: the load takes a global-memory latency, the peer
-    // hands its reordered words to the leader, and the copy into TMEM queues
+    // destination, already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what
+    // the MMA reads).  A scale warp loads a group up to kSfLookahead groups before
+    // it copies it to TMEM: the load takes a global-memory latency, the peer
+    // tells the leader its words have landed, and the copy into TMEM queues
     // behind the issued MMAs.  A shared-memory slot frees when its copy into
     // TMEM completes, which is kSfSlots - kSfLookahead groups before the slot
     // is loaded again.  Four TMEM slots where two accumulators fit beside
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     uint64_t *empty_bar = full_bar + R;               // [R] both: MMAs done with the slot
     uint64_t *tfull_bar = empty_bar + R;              // [NUM_ACC] both: accumulator complete
     uint64_t *tempty_bar = tfull_bar + NUM_ACC;       // [NUM_ACC] leader: both epilogues drained
-    uint64_t *sf_peer_bar = tempty_bar + NUM_ACC;     // [NSF] leader: peer's words reordered
+    uint64_t *sf_peer_bar = tempty_bar + NUM_ACC;     // [NSF] leader: peer's words landed
     uint64_t *sf_sfree_bar = sf_peer_bar + NSF;       // [NSF] both: words copied out of the slot
     uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] leader: words in both TMEMs
     uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] leader: MMAs done with the slot

@@ -11,12 +11,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -153,29 +147,11 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t num_clusters_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
 // Address of the same shared-memory location in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
-}
-
-// Arrive on an mbarrier given by its shared::cluster address (possibly in a peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
 }
 
 // Arrive on a peer CTA's mbarrier with the default (release, CTA-scope)
@@ -190,7 +166,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// All threads of all CTAs of the cluster (release/acquire ordering).
 // Programmatic dependent launch: let the next grid in the stream start launching
 // (its CTAs run up to their own wait), and wait until the grids this one depends
 // on have completed with their memory visible.
@@ -207,6 +182,7 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
     asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// All threads of all CTAs of the cluster (release/acquire ordering).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -231,16 +207,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map,
-                                                 uint64_t *bar, int32_t x, int32_t y,
-                                                 uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -314,14 +280,7 @@ __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ----------------------------------------------------------------- cp.async (16-byte chunks)
-
-// Copies 16 bytes from global to shared memory asynchronously (L2 only); a
-// src_bytes of 0 reads nothing and writes zeros.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
+// ----------------------------------------------------------------- cp.async (plain asynchronous copies)
 
 // Copies 4 bytes from global to shared memory asynchronously; a src_bytes of 0
 // reads nothing and writes zeros.
@@ -350,18 +309,6 @@ __device__ __forceinline__ void cp_async_wait_dyn(int n) {
         case 6: cp_async_wait<6>(); break;
         default: cp_async_wait<7>(); break;
     }
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -503,10 +450,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // 32 lanes x 16 consecutive 32-bit columns: thread t of the warp receives
 // lane (base lane + t), columns col..col+15.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -525,11 +468,6 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                    "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
-}
-
-__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
-                 : "memory");
 }
 
 // ----------------------------------------------------------------- descriptors
