@@ -186,7 +186,12 @@ def measure_other_workloads(dev, flush, reps, stream):
     record(f"dense NT + C {m}x{n}x{k}",
            lambda: binding.dg_fp8_gemm_nt(c_.a, sfa, c_.b, sfb, d, c=c_.c, status=status),
            flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {})
-    del c_, sfa, sfb, d
+    # the same GEMM given FP32 scales: the exact two-level promotion kernel
+    sfa32, sfb32 = c_.sfa.contiguous(), c_.sfb.contiguous()
+    record(f"dense NT + C {m}x{n}x{k}, FP32 scales (promotion)",
+           lambda: binding.dg_fp8_gemm_nt(c_.a, sfa32, c_.b, sfb32, d, c=c_.c, status=status),
+           flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {"scales": "fp32"})
+    del c_, sfa, sfb, sfa32, sfb32, d
 
     # contiguous grouped: 8 experts, M_e ~ U[128, 4096] padded to 128
     for (n, k) in ((4096, 7168), (7168, 2048)):

@@ -7,13 +7,18 @@
 // words MN-major with a K-slice stride of align(mn, 4) words; the scale rows are
 // broadcast from gran_mn to one per MN index.  Memory bound: one thread per
 // output word, consecutive threads write consecutive MN rows (coalesced).
+// Launched as programmatic dependents: a kernel lets the next grid start its
+// prologue at once and waits for the previous one before touching memory.
 #include "dg_internal.h"
+#include "ptx.cuh"
 
 namespace dg {
 
 __global__ void __launch_bounds__(256) dg_transform_sf_packed_kernel(
     const float *__restrict__ sf, int mn_rows, int sf_k, int gran_mn, int mn, int psf_k,
     int stride, uint32_t *__restrict__ out, int32_t *status) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int pslice = blockIdx.y;
     const int b = blockIdx.z;
@@ -41,6 +46,8 @@ __global__ void __launch_bounds__(256) dg_transform_sf_packed_kernel(
 __global__ void __launch_bounds__(256) dg_transform_sf_f32_kernel(
     const float *__restrict__ sf, int mn_rows, int sf_k, int gran_mn, int mn, int stride,
     float *__restrict__ out) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int k = blockIdx.y;
     const int b = blockIdx.z;
@@ -55,17 +62,23 @@ cudaError_t launch_transform_sf(const float *sf, int batch, int mn_rows, int sf_
                                 cudaStream_t stream) {
     const int stride = (mn + 3) / 4 * 4;
     const int psf_k = (sf_k + 3) / 4;
-    const dim3 block(256);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (out_fmt == DG_SF_UE8M0_PACKED) {
-        const dim3 grid((stride + 255) / 256, psf_k, batch);
-        dg_transform_sf_packed_kernel<<<grid, block, 0, stream>>>(
-            sf, mn_rows, sf_k, gran_mn, mn, psf_k, stride, static_cast<uint32_t *>(out), status);
-    } else {
-        const dim3 grid((stride + 255) / 256, sf_k, batch);
-        dg_transform_sf_f32_kernel<<<grid, block, 0, stream>>>(sf, mn_rows, sf_k, gran_mn, mn,
-                                                               stride, static_cast<float *>(out));
+        cfg.gridDim = dim3((stride + 255) / 256, psf_k, batch);
+        return cudaLaunchKernelEx(&cfg, dg_transform_sf_packed_kernel, sf, mn_rows, sf_k, gran_mn, mn, psf_k,
+                                  stride, static_cast<uint32_t *>(out), status);
     }
-    return cudaGetLastError();
+    cfg.gridDim = dim3((stride + 255) / 256, sf_k, batch);
+    return cudaLaunchKernelEx(&cfg, dg_transform_sf_f32_kernel, sf, mn_rows, sf_k, gran_mn, mn, stride,
+                              static_cast<float *>(out));
 }
 
 }  // namespace dg
