@@ -267,3 +267,44 @@ def m_grouped_masked(a, sa, b, sb_rows, masked_m, d_init=None, nthreads: int = 0
                                 _ptr(np.ascontiguousarray(sb_rows, dtype=np.float64)), _ptr(mm),
                                 _ptr(d), nthreads)
     return d
+
+
+def psum_segments(psum, m_total: int):
+    """Row segments of the PSUM contiguous layout (PaperTrace DeepGEMM §5.1: the
+    per-expert prefix sums of received token counts are the group offsets; §3.1:
+    groups are separated by gap rows).  Reading: psum[e] is the inclusive prefix
+    sum of the token counts m_e; expert e's rows start at S_e with S_0 = 0 and
+    S_{e+1} = align128(S_e + m_e); rows [S_e + m_e, S_{e+1}) are gap rows.
+
+    Returns (starts [E+1] = S_0..S_E, counts [E]).  Raises ValueError if psum
+    decreases or the segments end past m_total."""
+    psum = [int(x) for x in psum]
+    starts, counts, prev, s = [0], [], 0, 0
+    for v in psum:
+        m = v - prev
+        if m < 0:
+            raise ValueError("psum decreases")
+        counts.append(m)
+        s = (s + m + 127) // 128 * 128
+        starts.append(s)
+        prev = v
+    if starts[-1] > m_total:
+        raise ValueError("segments end past m_total")
+    return starts, counts
+
+
+def m_grouped_contiguous_psum(a, sa, b, sb_rows, psum, d_init=None, nthreads: int = 0):
+    """Contiguous M-grouped GEMM with PSUM offsets (PaperTrace DeepGEMM §5.1,
+    §3.1): expert e's rows [S_e, S_e + m_e) are computed with expert e's B; gap
+    rows [S_e + m_e, S_{e+1}) are written 0; rows at or past S_E keep d_init
+    (default 0).  Returns uint16 bf16 bits [m_total, N]."""
+    a = _u8(a)
+    M = a.shape[0]
+    starts, counts = psum_segments(psum, M)
+    layout = np.full(M, -1, dtype=np.int32)
+    for e, m in enumerate(counts):
+        layout[starts[e]:starts[e] + m] = e
+    d = m_grouped_contiguous(a, sa, b, sb_rows, layout, d_init=d_init, nthreads=nthreads)
+    for e, m in enumerate(counts):
+        d[starts[e] + m:starts[e + 1]] = 0
+    return d

@@ -462,3 +462,46 @@ def test_generator_recipe_scales_are_pow2_and_codes_fit():
     # amax of each group lands in (224, 448]
     deq = case.a.float().view(64, 3, 128).abs().amax(-1)
     assert torch.all(deq <= 448) and torch.all(deq > 224 - 32)
+
+
+# ---------------------------------------------------------------- PSUM contiguous layout
+
+def test_psum_segments_golden(orc):
+    """Hand-worked segment starts and counts (tests/golden/psum_segments.txt)."""
+    rows = _golden("psum_segments.txt")
+    assert rows
+    for case, m_total, psum, starts, counts in rows:
+        s, c = orc.psum_segments([int(x) for x in psum.split(",")], int(m_total))
+        assert s == [int(x) for x in starts.split(",")], case
+        assert c == [int(x) for x in counts.split(",")], case
+
+
+def test_psum_segments_rejects_bad_offsets(orc):
+    with pytest.raises(ValueError):
+        orc.psum_segments([10, 5], 256)       # decreasing
+    with pytest.raises(ValueError):
+        orc.psum_segments([100, 300], 256)    # segments end at 384 > 256
+
+
+def test_psum_layout_dense_per_expert_and_gap_rows(orc):
+    """Each expert's rows equal a dense GEMM of those rows with its B; gap rows
+    are 0; rows past the last segment keep the initial value."""
+    counts = [5, 0, 130, 1]
+    psum = np.cumsum(counts).tolist()
+    m_total = 128 + 256 + 128 + 128          # segments end at 512; one slack block
+    E, N, K = 4, 136, 256
+    rng = np.random.default_rng(5)
+    a = rng.integers(0, 0x7E, (m_total, K), dtype=np.uint8)   # finite E4M3 codes
+    b = rng.integers(0, 0x7E, (E, N, K), dtype=np.uint8)
+    sa = np.exp2(rng.integers(-3, 3, (m_total, 2))).astype(np.float64)
+    sb_rows = np.exp2(rng.integers(-3, 3, (E, N, 2))).astype(np.float64)
+    sentinel = np.full((m_total, N), 0x7FC1, dtype=np.uint16)
+    d = orc.m_grouped_contiguous_psum(a, sa, b, sb_rows, psum, d_init=sentinel)
+    starts = [0, 128, 128, 384, 512]
+    for e, m in enumerate(counts):
+        r0 = starts[e]
+        if m:
+            ref = orc.gemm_nt(a[r0:r0 + m], sa[r0:r0 + m], b[e], sb_rows[e])
+            assert np.array_equal(d[r0:r0 + m], ref), e
+        assert np.all(d[r0 + m:starts[e + 1]] == 0), e
+    assert np.all(d[512:] == 0x7FC1)
