@@ -208,6 +208,14 @@ def measure_other_workloads(dev, flush, reps, stream):
                                                                    status=status),
                flops(valid, n, k), valid * k + used * n * k + 2 * valid * n,
                {"valid_rows": valid, "rows": mt})
+        if n == 4096:
+            # the same problem with the groups given as PSUM offsets (gap rows written 0)
+            psum = torch.tensor(cc.m_per_expert, dtype=torch.int32).cumsum(0).to(torch.int32).to(dev)
+            record(f"m-grouped contiguous PSUM offsets 8 experts N={n} K={k}",
+                   lambda: binding.dg_m_grouped_fp8_gemm_nt_contiguous_psum(cc.a, sfa, cc.b, sfb, d, psum,
+                                                                            status=status),
+                   flops(valid, n, k), valid * k + used * n * k + 2 * mt * n,
+                   {"valid_rows": valid, "rows": mt})
         del cc, sfa, sfb, d
 
     # masked grouped decode: 32 experts, max_m 256

@@ -30,6 +30,7 @@ DG_DEBUG_WIDE_PAIR = 8
 # Every symbol include/dg.h declares.
 EXPORTS = (
     "dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
+    "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
     "dg_set_wait_timeout_ms", "dg_set_debug_flags", "dg_status_string", "dg_get_last_config",
@@ -63,10 +64,12 @@ def lib():
             L.dg_transform_sf.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P]
             L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes = [P, i64, P, i32, P, i64, P, i32, P,
                                                               i64, P, i32, i32, i32, i32, P, P]
+            L.dg_m_grouped_fp8_gemm_nt_contiguous_psum.argtypes = \
+                L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes
             L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
                                                           i32, i32, i32, P, P]
             for f in ("dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
-                      "dg_m_grouped_fp8_gemm_nt_masked"):
+                      "dg_m_grouped_fp8_gemm_nt_contiguous_psum", "dg_m_grouped_fp8_gemm_nt_masked"):
                 getattr(L, f).restype = i32
             L.dg_get_mk_alignment_for_contiguous_layout.restype = i32
             L.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
@@ -201,6 +204,20 @@ def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, grouped_layout,
     _check("dg_m_grouped_fp8_gemm_nt_contiguous", lib().dg_m_grouped_fp8_gemm_nt_contiguous(
         _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(1), _p(sfb), _sf_fmt(sfb),
         _p(d), d.stride(0), _p(grouped_layout), M, N, K, E, _p(status), _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nt_contiguous_psum(a, sfa, b, sfb, d, psum,
+                                             status: torch.Tensor | None = None, stream=None):
+    """As dg_m_grouped_fp8_gemm_nt_contiguous, with psum int32 [E] (device):
+    inclusive prefix sums of the experts' row counts; each expert's rows start
+    on a multiple of 128 after the previous expert's; gap rows of D get 0."""
+    M, K = a.shape
+    E, N, _ = b.shape
+    assert b.stride(0) == N * b.stride(1) and b.stride(2) == 1
+    _check("dg_m_grouped_fp8_gemm_nt_contiguous_psum", lib().dg_m_grouped_fp8_gemm_nt_contiguous_psum(
+        _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(1), _p(sfb), _sf_fmt(sfb),
+        _p(d), d.stride(0), _p(psum), M, N, K, E, _p(status), _stream(stream)))
     return d
 
 

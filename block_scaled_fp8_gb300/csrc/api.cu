@@ -662,6 +662,45 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const 
                                static_cast<cudaStream_t>(stream));
 }
 
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous_psum(const void *a, int64_t lda, const void *sfa,
+                                                   int sfa_fmt, const void *b, int64_t ldb,
+                                                   const void *sfb, int sfb_fmt, void *d, int64_t ldd,
+                                                   const int32_t *psum, int m_total, int n, int k,
+                                                   int num_groups, int32_t *status_dev, void *stream) {
+    if (m_total < 0 || n < 0 || k < 0 || num_groups < 1) return DG_ERR_INVALID_ARG;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != DG_SF_UE8M0_PACKED || sfb_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_UNSUPPORTED;
+    if (m_total % kBlockM != 0) return DG_ERR_LAYOUT;
+    // the PSUM layout runs on 256-row CTA pairs only
+    if (num_groups > kMaxPsumGroups || cdiv64(m_total, 2 * kBlockM) > kMaxPairPrefix) return DG_ERR_UNSUPPORTED;
+    if (m_total == 0 || n == 0) return DG_OK;
+    if (k == 0) return DG_ERR_UNSUPPORTED;
+    dg_status st = check_operand_rules(a, lda, b, ldb, n, k);
+    if (st != DG_OK) return st;
+    if (d == nullptr || sfa == nullptr || sfb == nullptr || psum == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || !aligned16(sfa) || !aligned16(sfb) || ldd < n || ldd % 8 != 0)
+        return DG_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(num_groups) * n > INT32_MAX) return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeContiguous, m_total, n, k, status_dev);
+    p.num_groups = num_groups;
+    p.psum = psum;
+    p.num_m_blocks = m_total / kBlockM;
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    BsOperands o{a,   lda, static_cast<uint64_t>(m_total),
+                 b,   ldb, static_cast<uint64_t>(num_groups) * n,
+                 sfa, static_cast<uint64_t>(m_total), static_cast<uint64_t>(psf_k),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k * num_groups),
+                 d,   ldd, static_cast<uint64_t>(m_total)};
+    const int64_t units_hint = cdiv64(p.num_m_blocks, 2);
+    return launch_pair(p, o, 256, choose_pair_block_n(p, false, units_hint, sms), p.num_m_blocks, sms,
+                       static_cast<cudaStream_t>(stream));
+}
+
 dg_status dg_m_grouped_fp8_gemm_nt_masked(const void *a, const void *sfa, int sfa_fmt,
                                           const void *b, const void *sfb, int sfb_fmt, void *d,
                                           const int32_t *masked_m, int num_groups, int max_m,

@@ -15,6 +15,8 @@ constexpr int kGran = 128;     // scale granularity along K (and N for FP32 B sc
 constexpr int kMaxGroupsMasked = 1024;
 // Grouped layouts on CTA pairs: at most this many m-pairs (contiguous) or experts (masked).
 constexpr int kMaxPairPrefix = 512;
+// Experts of the PSUM contiguous layout (8-bit ids in the pair kernel's unit info).
+constexpr int kMaxPsumGroups = 255;
 
 enum GemmMode : int { kModeDense = 0, kModeContiguous = 1, kModeMasked = 2 };
 
@@ -30,7 +32,8 @@ struct GemmParams {
     int num_n_groups;    // ceil(num_n_blocks / cluster): n-block groups, one per cluster tile
     int num_groups;
     int group_m;         // tile-order group size along M (L2 reuse)
-    const int32_t *grouped_layout;  // contiguous
+    const int32_t *grouped_layout;  // contiguous: expert id per row
+    const int32_t *psum;            // contiguous with PSUM offsets instead: [num_groups]
     const int32_t *masked_m;        // masked
     const uint16_t *c;   // dense: bf16 C or nullptr
     int64_t ldc;

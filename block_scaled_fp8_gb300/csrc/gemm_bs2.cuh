@@ -107,6 +107,7 @@ struct Bs2Config {
     // the TMEM holder and abort flag, all before the unit prefix 512 bytes on
     static constexpr int kNumBars = 2 * kRing + 2 * kNumAcc + 2 * kSfSlots + 2 * kSfTmemSlots + 1 + kSfWarps;
     static_assert(kNumBars * 8 + 8 <= 512, "barrier region");
+    static_assert(kSfSlots * kSfSlotBytes >= 2 * (kMaxPsumGroups + 1) * 4, "PSUM segments fit the scale ring");
 };
 
 struct PairTile {
@@ -118,6 +119,7 @@ struct PairTile {
     int b2_row0;     // and of the second MMA's (tiles wider than 256 columns)
     int sfb_y0;      // row of the packed SFB view for K-slice 0
     int valid_rows;  // rows of this CTA's MP/2 that are stored (0: none)
+    int zero_tail;   // the rest of this CTA's rows are gap rows, written 0 (PSUM layout)
 };
 
 // Pair units.  A unit is the row range of one pair tile; the tiles are the
@@ -127,13 +129,17 @@ struct PairTile {
 //               blocks, each of one expert or padding.  Both blocks of one
 //               expert: one unit.  Otherwise one unit per block that has an
 //               expert: the pair still computes 256 rows, but only the CTA
-//               holding that block stores.
+//               holding that block stores.  With PSUM offsets a block's
+//               expert comes from the segment starts, and the block's rows
+//               past the expert's last row are gap rows, stored as 0.
 //   masked:     (MP = 256) expert e gets ceil(masked_m[e] / 256) units of 256
 //               of its rows; rows at or past masked_m[e] are not stored.
 // For the grouped layouts prefix[i] = units before m-pair (expert) i, built
 // once per CTA in shared memory; total units = prefix[count].  info[i] keeps
 // what the tile lookup needs without touching global memory: the two blocks'
-// experts (contiguous, 16 bits each) or the clamped masked_m (masked).
+// experts (contiguous, 16 bits each; PSUM: 8 bits each, 0xFF for none, then
+// each block's rows of its expert in 8 bits each) or the clamped masked_m
+// (masked).
 
 // Experts of the two blocks of m-pair j (contiguous layout); -1 for padding,
 // past the end, or an out-of-range id (reported).
@@ -160,10 +166,68 @@ __device__ __forceinline__ int clamp_masked_m(const GemmParams &p, int e) {
     return mm;
 }
 
+// Largest i with prefix[i] <= u (prefix is non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int prefix_find(const int *prefix, int count, int u) {
+    int lo = 0, hi = count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Prefix sums by warp 0 (call with all 32 lanes): on entry x[1..count] hold
+// counts; on exit x[i] = x[1] + ... + x[i] and x[0] = 0.
+__device__ __forceinline__ void warp0_prefix_sums(int *x, int count, uint32_t lane) {
+    const int per = (count + 31) / 32;
+    const int lo = static_cast<int>(lane) * per, hi = lo + per < count ? lo + per : count;
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += x[i + 1];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (static_cast<int>(lane) >= o) incl += v;
+    }
+    int run = incl - sum;
+    if (lane == 0) x[0] = 0;
+    for (int i = lo; i < hi; ++i) {
+        run += x[i + 1];
+        x[i + 1] = run;
+    }
+}
+
+// PSUM contiguous layout: the segment of expert e starts at S_e, S_0 = 0 and
+// S_{e+1} = align128(S_e + m_e) = S_e + align128(m_e) (m_e = psum[e] -
+// psum[e-1]); rows [S_e + m_e, S_{e+1}) are gap rows.  Fills seg[0..E] and
+// cnt[0..E) with the whole CTA; ends with __syncthreads.  A decreasing psum
+// (the count is taken as 0) or segments ending past the rows set
+// DG_DEV_BAD_GROUP.
+__device__ __forceinline__ void build_psum_segments(const GemmParams &p, int *seg, int *cnt) {
+    const int E = p.num_groups;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        int m = __ldg(p.psum + i) - (i > 0 ? __ldg(p.psum + i - 1) : 0);
+        if (m < 0) {
+            if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+            m = 0;
+        }
+        cnt[i] = m;
+        seg[i + 1] = (m + kBlockM - 1) / kBlockM * kBlockM;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) warp0_prefix_sums(seg, E, threadIdx.x);
+    __syncthreads();
+    if (threadIdx.x == 0 && seg[E] > p.rows && p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+}
+
 // Builds prefix[0..count] and info[0..count) (count = m-pairs or experts)
-// with the whole CTA: unit counts in parallel, then one warp scans them.  Ends
-// with __syncthreads.
-__device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *prefix, int *info) {
+// with the whole CTA: unit counts in parallel, then one warp scans them.
+// scratch (2 * (kMaxPsumGroups + 1) ints, dead afterwards) holds the PSUM
+// segments.  Ends with __syncthreads.
+__device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *prefix, int *info, int *scratch) {
+    const bool psum = p.mode == kModeContiguous && p.psum != nullptr;
+    int *seg = scratch, *cnt = scratch + kMaxPsumGroups + 1;
+    if (psum) build_psum_segments(p, seg, cnt);
     const int count = p.mode == kModeMasked ? p.num_groups : p.num_m_blocks;
     for (int i = threadIdx.x; i < count; i += blockDim.x) {
         int units;
@@ -171,6 +235,29 @@ __device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *pref
             const int mm = clamp_masked_m(p, i);
             info[i] = mm;
             units = (mm + 2 * kBlockM - 1) / (2 * kBlockM);
+        } else if (psum) {
+            // each block's expert (0xFF: none) and the rows of it that are the expert's
+            uint32_t word = 0;
+            int e[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row0 = (2 * i + h) * kBlockM;
+                int s = -1, v = 0;
+                if (row0 < p.rows) {
+                    s = prefix_find(seg, p.num_groups + 1, row0);
+                    if (s >= p.num_groups) {
+                        s = -1;
+                    } else {
+                        v = seg[s] + cnt[s] - row0;
+                        v = v < kBlockM ? v : kBlockM;
+                        v = v < p.rows - row0 ? v : p.rows - row0;
+                    }
+                }
+                e[h] = s;
+                word |= (static_cast<uint32_t>(s & 0xFF) << (8 * h)) | (static_cast<uint32_t>(v) << (16 + 8 * h));
+            }
+            info[i] = static_cast<int>(word);
+            units = (e[0] >= 0 && e[0] == e[1]) ? 1 : (e[0] >= 0) + (e[1] >= 0);
         } else {
             int e0, e1;
             pair_block_experts(p, i, e0, e1);
@@ -180,36 +267,8 @@ __device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *pref
         prefix[i + 1] = units;
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const int per = (count + 31) / 32;
-        const int lo = lane * per, hi = lo + per < count ? lo + per : count;
-        int sum = 0;
-        for (int i = lo; i < hi; ++i) sum += prefix[i + 1];
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - sum;
-        if (lane == 0) prefix[0] = 0;
-        for (int i = lo; i < hi; ++i) {
-            run += prefix[i + 1];
-            prefix[i + 1] = run;
-        }
-    }
+    if (threadIdx.x < 32) warp0_prefix_sums(prefix, count, threadIdx.x);
     __syncthreads();
-}
-
-// Largest i with prefix[i] <= u (prefix is non-decreasing, prefix[0] = 0).
-__device__ __forceinline__ int prefix_find(const int *prefix, int count, int u) {
-    int lo = 0, hi = count - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
-    }
-    return lo;
 }
 
 __device__ __forceinline__ int pair_units(const GemmParams &p, const int *prefix) {
@@ -232,6 +291,7 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     const int nb = r / gsize;
     tile.n0 = nb * BN;
     int group = 0;
+    tile.zero_tail = 0;
     if (MP == 128 || p.mode == kModeDense) {
         tile.a_row0 = u * MP + rank * (MP / 2);
         tile.sfa_x = tile.a_row0;
@@ -239,19 +299,30 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
         tile.valid_rows = MP / 2;
     } else if (p.mode == kModeContiguous) {
         const int j = prefix_find(prefix, p.num_m_blocks, u);
-        const int e0 = static_cast<int16_t>(info[j] & 0xFFFF), e1 = info[j] >> 16;
+        int e0, e1, v0 = kBlockM, v1 = kBlockM;
+        if (p.psum != nullptr) {
+            const uint32_t w = static_cast<uint32_t>(info[j]);
+            e0 = (w & 0xFFu) == 0xFFu ? -1 : static_cast<int>(w & 0xFFu);
+            e1 = ((w >> 8) & 0xFFu) == 0xFFu ? -1 : static_cast<int>((w >> 8) & 0xFFu);
+            v0 = static_cast<int>((w >> 16) & 0xFFu);
+            v1 = static_cast<int>(w >> 24);
+        } else {
+            e0 = static_cast<int16_t>(info[j] & 0xFFFF);
+            e1 = info[j] >> 16;
+        }
         tile.a_row0 = j * 2 * kBlockM + rank * kBlockM;
         tile.sfa_x = tile.a_row0;
         tile.sfa_y0 = 0;
         if (e0 >= 0 && e0 == e1) {
             group = e0;
-            tile.valid_rows = kBlockM;
+            tile.valid_rows = rank == 0 ? v0 : v1;
         } else {
             // the unit's block: the first valid one, or the second if this is the pair's second unit
             const int h = (e0 >= 0 && u > prefix[j]) || e0 < 0 ? 1 : 0;
             group = h == 0 ? e0 : e1;
-            tile.valid_rows = rank == h ? kBlockM : 0;
+            tile.valid_rows = rank == h ? (h == 0 ? v0 : v1) : 0;
         }
+        tile.zero_tail = p.psum != nullptr && tile.valid_rows > 0;
     } else {
         const int e = prefix_find(prefix, p.num_groups, u);
         const int local0 = (u - prefix[e]) * 2 * kBlockM + rank * kBlockM;
@@ -337,7 +408,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     // inputs or write D.
     grid_launch_dependents();
     grid_dependency_wait();
-    if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo);  // ends with __syncthreads
+    // (the scale ring is free until the roles start: PSUM segments go there)
+    if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo, reinterpret_cast<int *>(smem_sf));
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     if (warp == 1) {
@@ -669,14 +741,18 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
                 if (tile.valid_rows == 0 || col0 >= p.n) return;
                 if (tile.valid_rows < MP / 2) {
+                    // the valid rows; with zero_tail the block's other rows get 0
                     const int local_row = row_off + static_cast<int>(lane);
-                    if (local_row < tile.valid_rows) {
+                    const bool value = local_row < tile.valid_rows;
+                    // (zero_tail: contiguous layout, where a_row0 indexes the D rows directly)
+                    if (value || (tile.zero_tail && tile.a_row0 + local_row < p.rows)) {
                         uint16_t *drow = p.d + static_cast<int64_t>(tile.a_row0 + local_row) * p.ldd + col0;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
                             if (col0 + 8 * h < p.n)
                                 *reinterpret_cast<uint4 *>(drow + 8 * h) =
-                                    make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+                                    value ? make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3])
+                                          : make_uint4(0u, 0u, 0u, 0u);
                     }
                     return;
                 }

@@ -142,6 +142,29 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const 
                                               void *stream);
 
 /*
+ * dg_m_grouped_fp8_gemm_nt_contiguous_psum -- the contiguous MoE GEMM with
+ * the groups given as prefix sums of their row counts (PaperTrace §5.1: the
+ * per-expert prefix sums of received tokens serve as group offsets; §3.1: gap
+ * rows lie between groups).  Reading taken: psum[e] = m_0 + ... + m_e (int32,
+ * device memory, non-decreasing); expert e's rows are [S_e, S_e + m_e) with
+ * S_0 = 0 and S_{e+1} = S_e rounded up past m_e rows to a multiple of 128.
+ *
+ *   a, sfa, b, sfb, d, strides: as for dg_m_grouped_fp8_gemm_nt_contiguous.
+ *   psum   int32 [num_groups] in device memory (read by the kernel).
+ *   D rows [S_e + m_e, S_{e+1}) (gap rows) are written 0; rows at or past
+ *   S_E are not written.  A decreasing psum (that count is taken as 0) or
+ *   S_E > m_total sets DG_DEV_BAD_GROUP.
+ *   num_groups <= 255 and m_total <= 131072 (the layout runs on 256-row CTA
+ *   pairs only; DG_DEBUG_SINGLE_CTA does not apply), else DG_ERR_UNSUPPORTED.
+ *   Only DG_SF_UE8M0_PACKED scales are accepted.
+ */
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous_psum(const void *a, int64_t lda, const void *sfa,
+                                                   int sfa_fmt, const void *b, int64_t ldb,
+                                                   const void *sfb, int sfb_fmt, void *d, int64_t ldd,
+                                                   const int32_t *psum, int m_total, int n, int k,
+                                                   int num_groups, int32_t *status_dev, void *stream);
+
+/*
  * dg_m_grouped_fp8_gemm_nt_masked -- MoE decode GEMM with static shapes
  * (PaperTrace §5.2; "DeepSeek V4 源码剖析 第13章" §13.6): expert e multiplies
  * its first masked_m[e] rows; nothing else of D is read or written.
