@@ -71,6 +71,8 @@ def _get():
             lib.orc_expand_block_rows.argtypes = [P, i32, i32, P]
             lib.orc_gemm_nt.restype = None
             lib.orc_gemm_nt.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, P, i32]
+            lib.orc_gemm_nt_f32.restype = None
+            lib.orc_gemm_nt_f32.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, i32]
             lib.orc_gemm_nt_sampled.restype = None
             lib.orc_gemm_nt_sampled.argtypes = [i32, P, i64, P, P, i64, P, P, i64, i64, P, P, P, P,
                                                 i32]
@@ -215,6 +217,26 @@ def gemm_nt(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
     _get().orc_gemm_nt(M, N, K, _ptr(a), K, _ptr(sa), _ptr(b), K, _ptr(sb_rows), _ptr(c), N,
                        _ptr(d), N, _ptr(pre), nthreads)
     return (d, pre) if want_pre else d
+
+
+def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
+                c: np.ndarray | None = None, nthreads: int = 0) -> np.ndarray:
+    """D = C + A @ B^T as gemm_nt, with FP32 C (or none) and FP32 D: the fp64
+    sum rounded once to FP32.  Returns float32 [M, N]."""
+    a, b = _u8(a), _u8(b)
+    M, K = a.shape
+    N = b.shape[0]
+    sf_k = (K + 127) // 128
+    sa = np.ascontiguousarray(sa, dtype=np.float64)
+    sb_rows = np.ascontiguousarray(sb_rows, dtype=np.float64)
+    assert sa.shape == (M, sf_k) and sb_rows.shape == (N, sf_k) and b.shape[1] == K
+    if c is not None:
+        c = np.ascontiguousarray(c, dtype=np.float32)
+        assert c.shape == (M, N)
+    d = np.empty((M, N), dtype=np.float32)
+    _get().orc_gemm_nt_f32(M, N, K, _ptr(a), K, _ptr(sa), _ptr(b), K, _ptr(sb_rows), _ptr(c), N,
+                           _ptr(d), N, nthreads)
+    return d
 
 
 def gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, c=None, want_pre=False, nthreads: int = 0):

@@ -214,6 +214,30 @@ static double dot_element(int K, const uint8_t *arow, const double *sarow, const
 }
 
 /*
+ * Full GEMM with FP32 C and D (the survey's FP32-output row; same sum as
+ * orc_gemm_nt): D[m][n] = fp32_rne(C[m][n] + sum), the sum in fp64 starting
+ * from C (0 if C is NULL), one rounding to FP32 (C's double -> float
+ * conversion rounds to nearest even).
+ */
+void orc_gemm_nt_f32(int M, int N, int K, const uint8_t *A, int64_t lda, const double *sa,
+                     const uint8_t *B, int64_t ldb, const double *sb, const float *C, int64_t ldc,
+                     float *D, int64_t ldd, int nthreads) {
+    int sf_k = (K + 127) / 128;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int m = 0; m < M; m++) {
+        for (int n = 0; n < N; n++) {
+            double c = C ? (double)C[(int64_t)m * ldc + n] : 0.0;
+            double v = dot_element(K, A + (int64_t)m * lda, sa + (int64_t)m * sf_k,
+                                   B + (int64_t)n * ldb, sb + (int64_t)n * sf_k, c);
+            D[(int64_t)m * ldd + n] = (float)v;
+        }
+    }
+}
+
+/*
  * Full GEMM, NT layout [P2 13.3]: A [M][lda] (K contiguous), B [N][ldb] (K
  * contiguous), sa [M][sf_k], sb [N][sf_k] (per row), C bf16 [M][ldc] or NULL,
  * D bf16 [M][ldd].  pre (optional, [M][N]) receives the fp64 value before

@@ -505,3 +505,37 @@ def test_psum_layout_dense_per_expert_and_gap_rows(orc):
             assert np.array_equal(d[r0:r0 + m], ref), e
         assert np.all(d[r0 + m:starts[e + 1]] == 0), e
     assert np.all(d[512:] == 0x7FC1)
+
+
+# ---------------------------------------------------------------- FP32 output
+
+def test_gemm_f32_integer_exact(orc):
+    """Integer codes and power-of-two scales (A's down to 2^-2): the result is
+    a multiple of 1/4 below 2^22, exact in FP32, so the FP32 output must equal
+    the float64 torch matmul (plus an integer C) exactly."""
+    case = inputs.integer_exact_case(64, 96, 384, seed=41)
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(96) // 128]
+    x = case.a.double() * torch.from_numpy(sa).repeat_interleave(128, 1)[:, :384]
+    w = case.b.double() * torch.from_numpy(sb_rows).repeat_interleave(128, 1)[:, :384]
+    c = torch.randint(-50, 50, (64, 96), generator=torch.Generator().manual_seed(3)).float()
+    exact = (x @ w.T + c.double()).numpy()
+    assert np.all(np.abs(exact) < 2 ** 22) and np.all(exact * 4 == np.round(exact * 4))
+    got = orc.gemm_nt_f32(a, sa, b, sb_rows, c=c.numpy())
+    assert np.array_equal(got.astype(np.float64), exact)
+
+
+def test_gemm_f32_rounds_once_to_fp32(orc):
+    """Random operands: the FP32 output is the fp64 pre-rounding value of the
+    bf16 oracle (C = 0) rounded to FP32 by numpy, and bf16 of it matches the
+    bf16 oracle except where the two roundings straddle a bf16 tie."""
+    case = inputs.dense_case(40, 72, 640, seed=9)
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(72) // 128]
+    _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
+    got = orc.gemm_nt_f32(a, sa, b, sb_rows)
+    assert np.array_equal(got, pre.astype(np.float32))
