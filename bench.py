@@ -191,7 +191,13 @@ def measure_other_workloads(dev, flush, reps, stream):
     record(f"dense NT + C {m}x{n}x{k}, FP32 scales (promotion)",
            lambda: binding.dg_fp8_gemm_nt(c_.a, sfa32, c_.b, sfb32, d, c=c_.c, status=status),
            flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {"scales": "fp32"})
-    del c_, sfa, sfb, sfa32, sfb32, d
+    # the same GEMM with FP32 C and D
+    c32 = c_.c.float()
+    d32 = torch.empty(m, n, dtype=torch.float32, device=dev)
+    record(f"dense NT + C {m}x{n}x{k}, FP32 C and D",
+           lambda: binding.dg_fp8_gemm_nt_f32(c_.a, sfa, c_.b, sfb, d32, c=c32, status=status),
+           flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n + 4 * m * n, {"d": "fp32"})
+    del c_, sfa, sfb, sfa32, sfb32, d, c32, d32
 
     # contiguous grouped: 8 experts, M_e ~ U[128, 4096] padded to 128
     for (n, k) in ((4096, 7168), (7168, 2048)):

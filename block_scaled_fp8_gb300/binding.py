@@ -29,7 +29,7 @@ DG_DEBUG_WIDE_PAIR = 8
 
 # Every symbol include/dg.h declares.
 EXPORTS = (
-    "dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
+    "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
     "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
@@ -61,6 +61,7 @@ def lib():
             P, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32
             L.dg_fp8_gemm_nt.argtypes = [P, i64, P, i32, P, i64, P, i32, P, i64, P, i64, i32, i32,
                                          i32, P, P]
+            L.dg_fp8_gemm_nt_f32.argtypes = L.dg_fp8_gemm_nt.argtypes
             L.dg_transform_sf.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P]
             L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes = [P, i64, P, i32, P, i64, P, i32, P,
                                                               i64, P, i32, i32, i32, i32, P, P]
@@ -68,7 +69,8 @@ def lib():
                 L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes
             L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
                                                           i32, i32, i32, P, P]
-            for f in ("dg_fp8_gemm_nt", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
+            for f in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_transform_sf",
+                      "dg_m_grouped_fp8_gemm_nt_contiguous",
                       "dg_m_grouped_fp8_gemm_nt_contiguous_psum", "dg_m_grouped_fp8_gemm_nt_masked"):
                 getattr(L, f).restype = i32
             L.dg_get_mk_alignment_for_contiguous_layout.restype = i32
@@ -188,6 +190,21 @@ def dg_fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: tor
     assert a.stride(1) == 1 and b.stride(1) == 1 and d.stride(1) == 1
     assert d.dtype == torch.bfloat16 and (c is None or (c.dtype == torch.bfloat16 and c.stride(1) == 1))
     _check("dg_fp8_gemm_nt", lib().dg_fp8_gemm_nt(
+        _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(0), _p(sfb), _sf_fmt(sfb),
+        _p(c), 0 if c is None else c.stride(0), _p(d), d.stride(0), M, N, K, _p(status),
+        _stream(stream)))
+    return d
+
+
+def dg_fp8_gemm_nt_f32(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                       d: torch.Tensor, c: torch.Tensor | None = None,
+                       status: torch.Tensor | None = None, stream=None):
+    """D = C + A @ B^T with FP32 d (and c) [M, N], unit column stride; scales packed."""
+    M, K = a.shape
+    N = b.shape[0]
+    assert a.stride(1) == 1 and b.stride(1) == 1 and d.stride(1) == 1
+    assert d.dtype == torch.float32 and (c is None or (c.dtype == torch.float32 and c.stride(1) == 1))
+    _check("dg_fp8_gemm_nt_f32", lib().dg_fp8_gemm_nt_f32(
         _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(0), _p(sfb), _sf_fmt(sfb),
         _p(c), 0 if c is None else c.stride(0), _p(d), d.stride(0), M, N, K, _p(status),
         _stream(stream)))

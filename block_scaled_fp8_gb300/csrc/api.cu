@@ -151,6 +151,15 @@ __global__ void dg_fill_d_kernel(const uint16_t *c, int64_t ldc, uint16_t *d, in
     }
 }
 
+__global__ void dg_fill_d_f32_kernel(const float *c, int64_t ldc, float *d, int64_t ldd, int m, int n) {
+    const int64_t total = static_cast<int64_t>(m) * n;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / n, col = i % n;
+        d[r * ldd + col] = c ? c[r * ldc + col] : 0.0f;
+    }
+}
+
 // Operand views of one block-scaled launch (all 2-D, K or MN contiguous).
 struct BsOperands {
     const void *a;  int64_t lda;  uint64_t a_rows;
@@ -201,19 +210,19 @@ bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
     return p.rows > kBlockM && p.num_groups <= kMaxPairPrefix && m_blocks_hint > 2LL * p.num_groups;
 }
 
-int cached_max_pairs(int bn, bool with_c, int mp) {
+int cached_max_pairs(int bn, bool with_c, int mp, bool f32 = false) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][513];
+    static int cache[kMaxDevices][2][2][2][513];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn <= 0 || bn > 512) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][bn];
-    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp);
+    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32);
     return v;
 }
 
-int usable_pairs(int bn, bool with_c, int mp, int num_sms) {
-    int pairs = cached_max_pairs(bn, with_c, mp);
+int usable_pairs(int bn, bool with_c, int mp, int num_sms, bool f32 = false) {
+    int pairs = cached_max_pairs(bn, with_c, mp, f32);
     if (pairs * 2 > num_sms) pairs = num_sms / 2;
     return pairs;
 }
@@ -228,7 +237,8 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
         const char *e = std::getenv("DG_PAIR_BLOCK_N");
         return e ? std::atoi(e) : 0;
     }();
-    if ((g_debug_flags.load() & DG_DEBUG_WIDE_PAIR) && !with_c) {
+    const bool f32 = p.d_f32 != nullptr;
+    if ((g_debug_flags.load() & DG_DEBUG_WIDE_PAIR) && !with_c && !f32) {
         KernelInfo ki;
         if (get_bs2_kernel_info(384, false, 256, &ki) && usable_pairs(384, false, 256, num_sms) > 0) return 384;
     }
@@ -238,8 +248,8 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
         // with N=4096, K=7168)
         if (cand > 256 && p.mode != kModeDense && !forced_bn) continue;
         KernelInfo ki;
-        if (!get_bs2_kernel_info(cand, with_c, 256, &ki)) continue;
-        const int pairs = usable_pairs(cand, with_c, 256, num_sms);
+        if (!get_bs2_kernel_info(cand, with_c, 256, &ki, f32)) continue;
+        const int pairs = usable_pairs(cand, with_c, 256, num_sms, f32);
         if (pairs <= 0) continue;
         const int64_t nb = cdiv64(p.n, cand);
         const int64_t tiles = m_pairs * nb;
@@ -292,10 +302,12 @@ void set_scale_words(GemmParams &p, const BsOperands &o) {
 // max_units bounds the number of mp-row units (the grid size).
 dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_t max_units,
                       int num_sms, cudaStream_t stream) {
-    const bool with_c = p.c != nullptr;
+    // FP32 D: the caller sets d_f32 (and c_f32 for an FP32 C) before the call
+    const bool f32 = p.d_f32 != nullptr;
+    const bool with_c = f32 ? p.c_f32 != nullptr : p.c != nullptr;
     KernelInfo info;
-    if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info)) return DG_ERR_UNSUPPORTED;
-    const int pairs = usable_pairs(bn, with_c, mp, num_sms);
+    if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info, f32)) return DG_ERR_UNSUPPORTED;
+    const int pairs = usable_pairs(bn, with_c, mp, num_sms, f32);
     if (pairs <= 0) return DG_ERR_UNSUPPORTED;
     const uint32_t a_rows = static_cast<uint32_t>(mp / 2);   // rows of A each CTA loads
     TensorMaps maps;
@@ -322,8 +334,13 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
                             b2_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (!b2_rows) maps.b2 = maps.b;   // not read
-    ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
-                    32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    // D store boxes: 32 rows of 32 bytes (16 bf16 or 8 FP32 columns)
+    if (f32)
+        ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, o.d, p.n, o.d_rows, o.ldd * 4, 8, 32,
+                        CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    else
+        ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
+                        32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
     set_scale_words(p, o);
     // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused)
@@ -333,7 +350,8 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     p.cluster = 2;
     p.num_n_groups = p.num_n_blocks;
     p.group_m = 8;
-    p.d = static_cast<uint16_t *>(o.d);
+    if (f32) p.d_f32 = static_cast<float *>(o.d);
+    else p.d = static_cast<uint16_t *>(o.d);
     p.ldd = o.ldd;
     p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
     uint32_t dbg = g_debug_flags.load();
@@ -622,6 +640,49 @@ dg_status dg_fp8_gemm_nt(const void *a, int64_t lda, const void *sfa, int sfa_fm
                  d,   ldd, static_cast<uint64_t>(m)};
     return launch_block_scaled(p, o, p.num_m_blocks, p.num_m_blocks, sms,
                                static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_gemm_nt_f32(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                             int64_t ldb, const void *sfb, int sfb_fmt, const float *c, int64_t ldc,
+                             float *d, int64_t ldd, int m, int n, int k, int32_t *status_dev,
+                             void *stream) {
+    if (m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != DG_SF_UE8M0_PACKED || sfb_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0) return DG_OK;
+    if (d == nullptr) return DG_ERR_INVALID_ARG;
+    // FP32 rows: 16-byte aligned starts and 4-column multiples
+    if (!aligned16(d) || ldd < n || ldd % 4 != 0 || n % 4 != 0) return DG_ERR_ALIGNMENT;
+    if (c != nullptr && (!aligned16(c) || ldc < n || ldc % 4 != 0)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    if (k == 0) {
+        dg_status st = check_device(&sms);
+        if (st != DG_OK) return st;
+        dg_fill_d_f32_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(c, ldc, d, ldd, m, n);
+        g_last_config[5] = 1;
+        return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    }
+    dg_status st = check_operand_rules(a, lda, b, ldb, n, k);
+    if (st != DG_OK) return st;
+    if (sfa == nullptr || sfb == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeDense, m, n, k, status_dev);
+    p.d_f32 = d;
+    p.c_f32 = c;
+    p.ldc = ldc;
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),
+                 sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(psf_k),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k),
+                 d,   ldd, static_cast<uint64_t>(m)};
+    // FP32 output runs on 256-row CTA pairs for every M
+    const int64_t units = cdiv64(m, 2 * kBlockM);
+    return launch_pair(p, o, 256, choose_pair_block_n(p, c != nullptr, units, sms), units, sms,
+                       static_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,

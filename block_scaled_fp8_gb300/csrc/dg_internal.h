@@ -38,6 +38,8 @@ struct GemmParams {
     const uint16_t *c;   // dense: bf16 C or nullptr
     int64_t ldc;
     uint16_t *d;         // bf16 D (used for direct stores)
+    float *d_f32;        // FP32 D (FP32-output GEMMs; then c_f32 is the FP32 C or null)
+    const float *c_f32;
     int64_t ldd;
     int32_t *status;
     uint64_t timeout_ns;
@@ -78,13 +80,13 @@ cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams
 // Largest number of co-resident clusters of `cluster` CTAs for that kernel (0 on error).
 int bs_max_active_clusters(int block_n, bool with_c, int cluster);
 
-// CTA-pair (cta_group::2) block-scaled kernel family, dense layout.  mp = rows
-// of a pair tile: 256 (BLOCK_N in {128, 192, 224, 240, 256}, up to 240 with C)
-// or 128 (BLOCK_N in {32, 64, 96, 128}, no C).
-bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info);
+// CTA-pair (cta_group::2) block-scaled kernel family (the instantiations are
+// listed in gemm_bs2_list.h).  mp = rows of a pair tile: 256 or 128; f32 picks
+// the FP32-output (and FP32-C) epilogue; launch_bs2_gemm takes C and f32 from p.
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32 = false);
 cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream);
-int bs2_max_active_pairs(int block_n, bool with_c, int mp);
+int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32 = false);
 
 // FP32-scale promotion kernel family.
 bool get_promote_kernel_info(int block_n, KernelInfo *info);

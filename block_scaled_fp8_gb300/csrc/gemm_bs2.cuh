@@ -338,7 +338,7 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     tile.sfb_y0 = group * psf_k;
 }
 
-template <int BN, bool WITH_C, int MP>
+template <int BN, bool WITH_C, int MP, bool F32 = false>
 __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
@@ -720,11 +720,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         };
         // With C, each chunk's registers are refilled with the next tile's C as soon
         // as this tile's chunk is stored, so the C loads run a whole tile ahead.
-        uint32_t cpk[WITH_C ? Cfg::kChunksPerWarp : 1][8];
+        uint32_t cpk[(WITH_C && !F32) ? Cfg::kChunksPerWarp : 1][8];
         PairTile tile;
         if (pair_id < num_tiles) {
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
-            if constexpr (WITH_C) {
+            if constexpr (WITH_C && !F32) {
 #pragma unroll
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
             }
@@ -774,7 +774,80 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             };
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
             tc_fence_after_sync();
-            if constexpr (WITH_C) {
+            if constexpr (F32) {
+                // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> two
+                // 8-column FP32 boxes through the staging buffers; the accumulator is
+                // released after its last chunk is read
+                const int row = tile.a_row0 + row_off + static_cast<int>(lane);
+#pragma unroll 1
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                    const int c = 2 * j + half;
+                    if (c >= Cfg::kNumChunks) break;
+                    const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
+                    float4 cv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        cv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if constexpr (WITH_C) {
+                            if (tile.valid_rows > 0 && row < p.rows && col0 + 4 * q < p.n)
+                                cv[q] = __ldg(reinterpret_cast<const float4 *>(
+                                    p.c_f32 + static_cast<int64_t>(row) * p.ldc + col0 + 4 * q));
+                        }
+                    }
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v);
+                    tmem_ld_wait();
+                    reg_fence16(v);
+                    float f[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        f[4 * q + 0] = __uint_as_float(v[4 * q + 0]) + cv[q].x;
+                        f[4 * q + 1] = __uint_as_float(v[4 * q + 1]) + cv[q].y;
+                        f[4 * q + 2] = __uint_as_float(v[4 * q + 2]) + cv[q].z;
+                        f[4 * q + 3] = __uint_as_float(v[4 * q + 3]) + cv[q].w;
+                    }
+                    if (tile.valid_rows == 0 || col0 >= p.n) continue;
+                    if (tile.valid_rows < MP / 2) {
+                        const int local_row = row_off + static_cast<int>(lane);
+                        const bool value = local_row < tile.valid_rows;
+                        if (value || (tile.zero_tail && row < p.rows)) {
+                            float *drow = p.d_f32 + static_cast<int64_t>(row) * p.ldd + col0;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (col0 + 4 * q < p.n)
+                                    *reinterpret_cast<float4 *>(drow + 4 * q) =
+                                        value ? make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3])
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        if (col0 + 8 * part >= p.n) break;
+                        uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            // 32-byte swizzle: 16-byte unit h of row r sits at unit h ^ ((r >> 2) & 1)
+                            const uint32_t off = lane * 32 + ((h ^ ((lane >> 2) & 1)) * 16);
+                            const float *x = f + 8 * part + 4 * h;
+                            *reinterpret_cast<float4 *>(sbuf + off) = make_float4(x[0], x[1], x[2], x[3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.a_row0 + row_off);
+                            bulk_commit_group();
+                        }
+                        buf ^= 1;
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+            } else if constexpr (WITH_C) {
                 // C is held as bf16 (prefetched above), so the FP32 accumulator stays in
                 // TMEM until each chunk is converted and stored; the other accumulator
                 // keeps the MMAs busy meanwhile
@@ -861,11 +934,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     }
 }
 
-template <int BN, bool WITH_C, int MP>
+template <int BN, bool WITH_C, int MP, bool F32>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
     using Cfg = Bs2Config<BN, MP>;
-    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP>,
+    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -881,13 +954,13 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP>, maps.a, maps.b, maps.b2, maps.d, p);
+    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>, maps.a, maps.b, maps.b2, maps.d, p);
 }
 
-template <int BN, bool WITH_C, int MP>
+template <int BN, bool WITH_C, int MP, bool F32>
 int max_active_pairs_impl() {
     using Cfg = Bs2Config<BN, MP>;
-    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP>,
+    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -902,7 +975,7 @@ int max_active_pairs_impl() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C, MP>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 

@@ -3,6 +3,7 @@
 #include "gemm_bs.cuh"
 #include "gemm_promote.cuh"
 #include "gemm_bs2.cuh"
+#include "gemm_bs2_list.h"
 
 namespace dg {
 
@@ -20,20 +21,16 @@ DG_BS_BLOCK_N_LIST(DG_EXTERN)
 DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #undef DG_EXTERN
 
-#define DG_BS2_LIST(X)                                                                             \
-    X(128, false, 256) X(128, true, 256) X(192, false, 256) X(192, true, 256) X(224, false, 256)      \
-    X(224, true, 256) X(240, false, 256) X(240, true, 256) X(256, false, 256) X(32, false, 128)       \
-    X(64, false, 128) X(96, false, 128) X(128, false, 128) X(384, false, 256)
-#define DG_EXTERN2(BN, C, MP)                                                                      \
-    extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP>(const TensorMaps &, const GemmParams &, \
-                                                                int, cudaStream_t);                      \
-    extern template int max_active_pairs_impl<BN, C, MP>();
+#define DG_EXTERN2(BN, C, MP, F32)                                                                 \
+    extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP, F32>(const TensorMaps &,             \
+                                                                     const GemmParams &, int, cudaStream_t); \
+    extern template int max_active_pairs_impl<BN, C, MP, F32>();
 DG_BS2_LIST(DG_EXTERN2)
 #undef DG_EXTERN2
 
-bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info) {
-#define DG_CASE2(BN, C, MP) \
-    if (block_n == BN && with_c == C && mp == MP) { fill_bs2_info<BN, MP>(info); return true; }
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32) {
+#define DG_CASE2(BN, C, MP, F32) \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32) { fill_bs2_info<BN, MP>(info); return true; }
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return false;
@@ -41,17 +38,19 @@ bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info) {
 
 cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream) {
-    const bool with_c = p.c != nullptr;
-#define DG_CASE2(BN, C, MP) \
-    if (block_n == BN && with_c == C && mp == MP) return launch_bs2_gemm_impl<BN, C, MP>(maps, p, grid, stream);
+    const bool f32 = p.d_f32 != nullptr;
+    const bool with_c = f32 ? p.c_f32 != nullptr : p.c != nullptr;
+#define DG_CASE2(BN, C, MP, F32)                                            \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32)             \
+        return launch_bs2_gemm_impl<BN, C, MP, F32>(maps, p, grid, stream);
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return cudaErrorInvalidValue;
 }
 
-int bs2_max_active_pairs(int block_n, bool with_c, int mp) {
-#define DG_CASE2(BN, C, MP) \
-    if (block_n == BN && with_c == C && mp == MP) return max_active_pairs_impl<BN, C, MP>();
+int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32) {
+#define DG_CASE2(BN, C, MP, F32) \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32) return max_active_pairs_impl<BN, C, MP, F32>();
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return 0;

@@ -117,6 +117,26 @@ dg_status dg_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int
                           int out_fmt, void *out, int32_t *status_dev, void *stream);
 
 /*
+ * dg_fp8_gemm_nt_f32 -- dg_fp8_gemm_nt with FP32 D and an optional FP32 C
+ * ("DeepSeek V4 源码剖析 第13章" §13.3: D = C + A @ B^T; the pages fix no D
+ * type, and this form keeps the FP32 accumulator, e.g. to accumulate in place
+ * with c == d).  D = C + the FP32 accumulator, added in FP32, no further
+ * rounding.
+ *
+ *   a, sfa, b, sfb, lda, ldb, m, n, k: as for dg_fp8_gemm_nt; only
+ *          DG_SF_UE8M0_PACKED scales are accepted (else DG_ERR_UNSUPPORTED).
+ *   c      FP32 [m, ldc] or NULL; may alias d.
+ *   d      FP32 [m, ldd].
+ *   d and c 16-byte aligned, n, ldd and ldc multiples of 4 (else
+ *   DG_ERR_ALIGNMENT).  Runs on 256-row CTA pairs for every m.  k == 0 gives D = C
+ *   (or 0).
+ */
+dg_status dg_fp8_gemm_nt_f32(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                             int64_t ldb, const void *sfb, int sfb_fmt, const float *c, int64_t ldc,
+                             float *d, int64_t ldd, int m, int n, int k, int32_t *status_dev,
+                             void *stream);
+
+/*
  * dg_m_grouped_fp8_gemm_nt_contiguous -- MoE GEMM grouped along M only
  * (PaperTrace §5.1; "DeepSeek V4 源码剖析 第13章" §13.6): the rows of all
  * experts are concatenated along M, each expert's segment starting on a
