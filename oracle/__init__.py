@@ -219,6 +219,24 @@ def gemm_nt(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
     return (d, pre) if want_pre else d
 
 
+def gemm(layout: str, a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
+         c: np.ndarray | None = None, want_pre: bool = False, nthreads: int = 0):
+    """D = C + op(A) op(B) for the four layouts "nt", "nn", "tn", "tt".
+
+    "DeepSeek V4 源码剖析 第13章" §13.3: the GEMMs compute D = C + A @ B, the
+    two suffix letters telling whether A and B are transposed; fp8_gemm_nt is
+    D = C + A @ B.T.  As stored: A is [M, K] for "n", [K, M] for "t"; B is
+    [K, N] for "n", [N, K] for "t".  The scales belong to the product's
+    indices, not to the storage order: sa [M, sf_k], sb_rows [N, sf_k].
+    Each operand is brought to the NT form by a transpose of its storage.
+    """
+    assert layout in ("nt", "nn", "tn", "tt")
+    a, b = _u8(a), _u8(b)
+    a_mk = np.ascontiguousarray(a.T) if layout[0] == "t" else a
+    b_nk = np.ascontiguousarray(b.T) if layout[1] == "n" else b
+    return gemm_nt(a_mk, sa, b_nk, sb_rows, c=c, want_pre=want_pre, nthreads=nthreads)
+
+
 def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
                 c: np.ndarray | None = None, nthreads: int = 0) -> np.ndarray:
     """D = C + A @ B^T as gemm_nt, with FP32 C (or none) and FP32 D: the fp64

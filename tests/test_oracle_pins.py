@@ -539,3 +539,39 @@ def test_gemm_f32_rounds_once_to_fp32(orc):
     _, pre = orc.gemm_nt(a, sa, b, sb_rows, want_pre=True)
     got = orc.gemm_nt_f32(a, sa, b, sb_rows)
     assert np.array_equal(got, pre.astype(np.float32))
+
+
+# ---------------------------------------------------------------- NN / TN / TT layouts
+
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt", "nt"])
+@pytest.mark.parametrize("M,N,K,seed", [(3, 130, 256, 51), (5, 4, 200, 52)])
+def test_gemm_layouts_bruteforce_from_storage(orc, layout, M, N, K, seed):
+    """"DeepSeek V4 源码剖析 第13章" §13.3 naming: D = C + A @ B with "t" meaning
+    transposed, so A is stored [K, M] for "t" and B [K, N] for "n".  The brute
+    force reads each element straight from that storage by index (no
+    transpose); power-of-two scales keep every term exact, so the oracle's
+    pre-rounding values must equal the rational sums exactly.  N=130 spans two
+    128-row B scale blocks and M != N != K, so a swapped operand, index or scale
+    axis changes the values or the shapes."""
+    case = inputs.dense_case(M, N, K, seed=seed, with_c=True)
+    a_mk, b_nk = _case_np(case)
+    a = np.ascontiguousarray(a_mk.T) if layout[0] == "t" else a_mk
+    b = np.ascontiguousarray(b_nk.T) if layout[1] == "n" else b_nk
+    A = _decode_codes_torch(torch.from_numpy(a))
+    B = _decode_codes_torch(torch.from_numpy(b))
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(N) // 128]
+    c = case.c.view(torch.int16).numpy().view(np.uint16)
+    d, pre = orc.gemm(layout, a, sa, b, sb_rows, c=c, want_pre=True)
+    assert d.shape == (M, N)
+    for m in range(M):
+        for n in range(N):
+            s = Fraction(_bf16_value(int(c[m, n])))
+            for k in range(K):
+                av = A[k, m] if layout[0] == "t" else A[m, k]
+                bv = B[k, n] if layout[1] == "n" else B[n, k]
+                if av and bv:
+                    s += (Fraction(float(av)) * Fraction(float(sa[m, k // 128])) *
+                          Fraction(float(bv)) * Fraction(float(sb_rows[n, k // 128])))
+            assert Fraction(pre[m, n]) == s, (layout, m, n)
+            assert d[m, n] == _bf16_nearest_bruteforce(s)
