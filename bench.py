@@ -197,7 +197,16 @@ def measure_other_workloads(dev, flush, reps, stream):
     record(f"dense NT + C {m}x{n}x{k}, FP32 C and D",
            lambda: binding.dg_fp8_gemm_nt_f32(c_.a, sfa, c_.b, sfb, d32, c=c32, status=status),
            flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n + 4 * m * n, {"d": "fp32"})
-    del c_, sfa, sfb, sfa32, sfb32, d, c32, d32
+    # the same GEMM with M- / N-contiguous operands (A stored [K, M], B [K, N])
+    a_t = c_.a.view(torch.uint8).t().contiguous().view(torch.float8_e4m3fn)
+    b_t = c_.b.view(torch.uint8).t().contiguous().view(torch.float8_e4m3fn)
+    for name, fn, a_, b_ in (("NN", binding.dg_fp8_gemm_nn, c_.a, b_t),
+                             ("TN", binding.dg_fp8_gemm_tn, a_t, b_t),
+                             ("TT", binding.dg_fp8_gemm_tt, a_t, c_.b)):
+        record(f"dense {name} + C {m}x{n}x{k}",
+               lambda fn=fn, a_=a_, b_=b_: fn(a_, sfa, b_, sfb, d, c=c_.c, status=status),
+               flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {"layout": name.lower()})
+    del c_, sfa, sfb, sfa32, sfb32, d, c32, d32, a_t, b_t
 
     # contiguous grouped: 8 experts, M_e ~ U[128, 4096] padded to 128
     for (n, k) in ((4096, 7168), (7168, 2048)):

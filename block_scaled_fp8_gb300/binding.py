@@ -29,8 +29,8 @@ DG_DEBUG_WIDE_PAIR = 8
 
 # Every symbol include/dg.h declares.
 EXPORTS = (
-    "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous",
-    "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
+    "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn", "dg_fp8_gemm_tt",
+    "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
     "dg_set_wait_timeout_ms", "dg_set_debug_flags", "dg_status_string", "dg_get_last_config",
@@ -61,7 +61,8 @@ def lib():
             P, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32
             L.dg_fp8_gemm_nt.argtypes = [P, i64, P, i32, P, i64, P, i32, P, i64, P, i64, i32, i32,
                                          i32, P, P]
-            L.dg_fp8_gemm_nt_f32.argtypes = L.dg_fp8_gemm_nt.argtypes
+            for f in ("dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn", "dg_fp8_gemm_tt"):
+                getattr(L, f).argtypes = L.dg_fp8_gemm_nt.argtypes
             L.dg_transform_sf.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P]
             L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes = [P, i64, P, i32, P, i64, P, i32, P,
                                                               i64, P, i32, i32, i32, i32, P, P]
@@ -69,7 +70,8 @@ def lib():
                 L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes
             L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
                                                           i32, i32, i32, P, P]
-            for f in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_transform_sf",
+            for f in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn",
+                      "dg_fp8_gemm_tt", "dg_transform_sf",
                       "dg_m_grouped_fp8_gemm_nt_contiguous",
                       "dg_m_grouped_fp8_gemm_nt_contiguous_psum", "dg_m_grouped_fp8_gemm_nt_masked"):
                 getattr(L, f).restype = i32
@@ -209,6 +211,36 @@ def dg_fp8_gemm_nt_f32(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb:
         _p(c), 0 if c is None else c.stride(0), _p(d), d.stride(0), M, N, K, _p(status),
         _stream(stream)))
     return d
+
+
+def _gemm_layout(fn: str, a_mn: bool, b_mn: bool, a, sfa, b, sfb, d, c, status, stream):
+    # a is [M, K] (K-contiguous) or [K, M] (M-contiguous); b is [N, K] or [K, N]
+    M = a.shape[1] if a_mn else a.shape[0]
+    K = a.shape[0] if a_mn else a.shape[1]
+    N = b.shape[1] if b_mn else b.shape[0]
+    assert (b.shape[0] if b_mn else b.shape[1]) == K
+    assert a.stride(1) == 1 and b.stride(1) == 1 and d.stride(1) == 1
+    assert d.dtype == torch.bfloat16 and (c is None or (c.dtype == torch.bfloat16 and c.stride(1) == 1))
+    _check(fn, getattr(lib(), fn)(
+        _p(a), a.stride(0), _p(sfa), _sf_fmt(sfa), _p(b), b.stride(0), _p(sfb), _sf_fmt(sfb),
+        _p(c), 0 if c is None else c.stride(0), _p(d), d.stride(0), M, N, K, _p(status),
+        _stream(stream)))
+    return d
+
+
+def dg_fp8_gemm_nn(a, sfa, b, sfb, d, c=None, status=None, stream=None):
+    """D = C + A @ B: a [M, K], b [K, N] (N contiguous); packed scales as for the NT call."""
+    return _gemm_layout("dg_fp8_gemm_nn", False, True, a, sfa, b, sfb, d, c, status, stream)
+
+
+def dg_fp8_gemm_tn(a, sfa, b, sfb, d, c=None, status=None, stream=None):
+    """D = C + A^T @ B: a [K, M] (M contiguous), b [K, N] (N contiguous)."""
+    return _gemm_layout("dg_fp8_gemm_tn", True, True, a, sfa, b, sfb, d, c, status, stream)
+
+
+def dg_fp8_gemm_tt(a, sfa, b, sfb, d, c=None, status=None, stream=None):
+    """D = C + A^T @ B^T: a [K, M] (M contiguous), b [N, K] (K contiguous)."""
+    return _gemm_layout("dg_fp8_gemm_tt", True, False, a, sfa, b, sfb, d, c, status, stream)
 
 
 def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, grouped_layout,

@@ -210,19 +210,19 @@ bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
     return p.rows > kBlockM && p.num_groups <= kMaxPairPrefix && m_blocks_hint > 2LL * p.num_groups;
 }
 
-int cached_max_pairs(int bn, bool with_c, int mp, bool f32 = false) {
+int cached_max_pairs(int bn, bool with_c, int mp, bool f32 = false, int lay = 0) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][2][513];
+    static int cache[kMaxDevices][2][2][2][4][513];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn <= 0 || bn > 512) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][bn];
-    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32);
+    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][lay & 3][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32, lay & 3);
     return v;
 }
 
-int usable_pairs(int bn, bool with_c, int mp, int num_sms, bool f32 = false) {
-    int pairs = cached_max_pairs(bn, with_c, mp, f32);
+int usable_pairs(int bn, bool with_c, int mp, int num_sms, bool f32 = false, int lay = 0) {
+    int pairs = cached_max_pairs(bn, with_c, mp, f32, lay);
     if (pairs * 2 > num_sms) pairs = num_sms / 2;
     return pairs;
 }
@@ -305,16 +305,17 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     // FP32 D: the caller sets d_f32 (and c_f32 for an FP32 C) before the call
     const bool f32 = p.d_f32 != nullptr;
     const bool with_c = f32 ? p.c_f32 != nullptr : p.c != nullptr;
+    const int lay = p.layout;   // MN-major operands: bit 0 A, bit 1 B
     KernelInfo info;
-    if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info, f32)) return DG_ERR_UNSUPPORTED;
-    const int pairs = usable_pairs(bn, with_c, mp, num_sms, f32);
+    if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info, f32, lay)) return DG_ERR_UNSUPPORTED;
+    const int pairs = usable_pairs(bn, with_c, mp, num_sms, f32, lay);
     if (pairs <= 0) return DG_ERR_UNSUPPORTED;
     const uint32_t a_rows = static_cast<uint32_t>(mp / 2);   // rows of A each CTA loads
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
     // K a multiple of 128: one 3-D load per operand fills a ring slot
-    p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
+    p.ab_3d = (lay == 0 && k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
     // a tile wider than 256 columns runs two MMAs (256 and bn - 256 columns); each CTA
     // loads half of each one's B rows through its own map
     const uint32_t b1_rows = static_cast<uint32_t>((bn > 256 ? 256 : bn) / 2);
@@ -325,10 +326,20 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
         ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, b1_rows, info.group_kb);
         if (b2_rows) ok &= encode_kblocked_3d(&maps.b2, o.b, o.b_rows, o.ldb, kblocks, b2_rows, info.group_kb);
     } else {
-        ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                        a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
-                        b1_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        // an MN-major operand ([K][MN], MN contiguous): boxes of 128 MN-bytes x G K-blocks of rows
+        const uint32_t k_rows = static_cast<uint32_t>(info.group_kb * kBlockK);
+        if (lay & 1)
+            ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, o.a_rows, k, o.lda, a_rows, k_rows,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        else
+            ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
+                            a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (lay & 2)
+            ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, o.b_rows, k, o.ldb, b1_rows, k_rows,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        else
+            ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
+                            b1_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (b2_rows)
             ok &= encode_2d(&maps.b2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
                             b2_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
@@ -683,6 +694,73 @@ dg_status dg_fp8_gemm_nt_f32(const void *a, int64_t lda, const void *sfa, int sf
     const int64_t units = cdiv64(m, 2 * kBlockM);
     return launch_pair(p, o, 256, choose_pair_block_n(p, c != nullptr, units, sms), units, sms,
                        static_cast<cudaStream_t>(stream));
+}
+
+// NN / TN / TT: D = C + op(A) op(B) with MN-major operands where the layout
+// letter says so; 256x256 CTA-pair tiles.
+static dg_status gemm_mn_layout(int lay, const void *a, int64_t lda, const void *sfa, int sfa_fmt,
+                                const void *b, int64_t ldb, const void *sfb, int sfb_fmt, const void *c,
+                                int64_t ldc, void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev,
+                                void *stream) {
+    if (m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if ((sfa_fmt != DG_SF_FP32 && sfa_fmt != DG_SF_UE8M0_PACKED) ||
+        (sfb_fmt != DG_SF_FP32 && sfb_fmt != DG_SF_UE8M0_PACKED))
+        return DG_ERR_INVALID_ARG;
+    if (sfa_fmt != DG_SF_UE8M0_PACKED || sfb_fmt != DG_SF_UE8M0_PACKED) return DG_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0) return DG_OK;
+    if (d == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || ldd < n || ldd % 8 != 0 || n % 8 != 0) return DG_ERR_ALIGNMENT;
+    if (c != nullptr && (!aligned16(c) || ldc < n || ldc % 8 != 0)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    if (k == 0) {
+        dg_status st = check_device(&sms);
+        if (st != DG_OK) return st;
+        dg_fill_d_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint16_t *>(c), ldc, static_cast<uint16_t *>(d), ldd, m, n);
+        g_last_config[5] = 1;
+        return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    }
+    if (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    // the contiguous dimension of each operand: K (K-major) or M / N (MN-major)
+    const int64_t a_inner = (lay & 1) ? m : k, b_inner = (lay & 2) ? n : k;
+    if (lda < a_inner || ldb < b_inner) return DG_ERR_INVALID_ARG;
+    if (lda % 16 != 0 || ldb % 16 != 0) return DG_ERR_ALIGNMENT;
+    if ((!(lay & 1) || !(lay & 2)) && k % 16 != 0) return DG_ERR_ALIGNMENT;
+    dg_status st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeDense, m, n, k, status_dev);
+    p.c = static_cast<const uint16_t *>(c);
+    p.ldc = ldc;
+    p.layout = lay;
+    const int64_t psf_k = cdiv64(cdiv64(k, kGran), 4);
+    BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),
+                 sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(psf_k),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k),
+                 d,   ldd, static_cast<uint64_t>(m)};
+    const int64_t units = cdiv64(m, 2 * kBlockM);
+    return launch_pair(p, o, 256, 256, units, sms, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_gemm_nn(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                         int64_t ldb, const void *sfb, int sfb_fmt, const void *c, int64_t ldc,
+                         void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev, void *stream) {
+    return gemm_mn_layout(2, a, lda, sfa, sfa_fmt, b, ldb, sfb, sfb_fmt, c, ldc, d, ldd, m, n, k, status_dev,
+                          stream);
+}
+
+dg_status dg_fp8_gemm_tn(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                         int64_t ldb, const void *sfb, int sfb_fmt, const void *c, int64_t ldc,
+                         void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev, void *stream) {
+    return gemm_mn_layout(3, a, lda, sfa, sfa_fmt, b, ldb, sfb, sfb_fmt, c, ldc, d, ldd, m, n, k, status_dev,
+                          stream);
+}
+
+dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
+                         int64_t ldb, const void *sfb, int sfb_fmt, const void *c, int64_t ldc,
+                         void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev, void *stream) {
+    return gemm_mn_layout(1, a, lda, sfa, sfa_fmt, b, ldb, sfb, sfb_fmt, c, ldc, d, ldd, m, n, k, status_dev,
+                          stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,

@@ -45,6 +45,7 @@ struct GemmParams {
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
+    int layout;          // operand layouts: bit 0 A MN-major ([K][M]), bit 1 B MN-major ([K][N])
     // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the
     // block-scaled kernels' scale warps read them with cp.async
     const uint32_t *sfa_words;
@@ -83,10 +84,10 @@ int bs_max_active_clusters(int block_n, bool with_c, int cluster);
 // CTA-pair (cta_group::2) block-scaled kernel family (the instantiations are
 // listed in gemm_bs2_list.h).  mp = rows of a pair tile: 256 or 128; f32 picks
 // the FP32-output (and FP32-C) epilogue; launch_bs2_gemm takes C and f32 from p.
-bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32 = false);
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32 = false, int lay = 0);
 cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const GemmParams &p, int grid,
                             cudaStream_t stream);
-int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32 = false);
+int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32 = false, int lay = 0);
 
 // FP32-scale promotion kernel family.
 bool get_promote_kernel_info(int block_n, KernelInfo *info);

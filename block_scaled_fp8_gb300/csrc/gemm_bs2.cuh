@@ -338,16 +338,25 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     tile.sfb_y0 = group * psf_k;
 }
 
-template <int BN, bool WITH_C, int MP, bool F32 = false>
+// LAY: operand layouts, bit 0 = A MN-major (stored [K][M]), bit 1 = B MN-major
+// (stored [K][N]); 0 is the NT layout (both K-major).  An MN-major operand's
+// stage is a TMA box of 128 MN-bytes x 128 K-rows with 128-byte swizzle: one
+// swizzle atom along MN (so MP=256 and BN=256 only), 8-row groups 1024 bytes
+// apart, and a 32-K step of the MMA 4096 bytes on; the instruction descriptor's
+// transpose bits (15: A, 16: B) select the layout.
+template <int BN, bool WITH_C, int MP, bool F32 = false, int LAY = 0>
 __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_b2,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
     using Cfg = Bs2Config<BN, MP>;
+    constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0;
+    static_assert(LAY == 0 || (MP == 256 && BN == 256), "MN-major operands: 256x256 pair tiles");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
     constexpr int G = Cfg::kGroupKb;
+    static_assert(LAY == 0 || G * kBlockK <= 256, "an MN-major box holds at most 256 K rows");
     constexpr int NUM_ACC = Cfg::kNumAcc;
     constexpr int NSF = Cfg::kSfSlots;       // shared-memory scale slots
     constexpr int NTS = Cfg::kSfTmemSlots;   // TMEM scale slots
@@ -444,7 +453,32 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     drop = false;  // diagnostic: leave this slot empty
                 } else {
                     const uint32_t fb = leader_full + slot * 8;
-                    if (p.ab_3d) {
+                    if constexpr (LAY != 0) {
+                        // an MN-major operand: one box of 128 MN-bytes x G*128 K-rows fills the
+                        // slot; the K-major one: G boxes (K-blocks past K are out of bounds,
+                        // zero-filled, and still count their bytes)
+                        if (elect_one()) {
+                            if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * G * Cfg::kStageBytes);
+                            uint8_t *a_slot = smem_a + slot * G * Cfg::kABytes;
+                            uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
+                            if constexpr (A_MN) {
+                                tma_load_2d_pair(a_slot, &tm_a, fb, tile.a_row0, kb0 * kBlockK);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < G; ++j)
+                                    tma_load_2d_pair(a_slot + j * Cfg::kABytes, &tm_a, fb, (kb0 + j) * kBlockK,
+                                                     tile.a_row0);
+                            }
+                            if constexpr (B_MN) {
+                                tma_load_2d_pair(b_slot, &tm_b, fb, tile.b_row0, kb0 * kBlockK);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < G; ++j)
+                                    tma_load_2d_pair(b_slot + j * Cfg::kB1Bytes, &tm_b, fb, (kb0 + j) * kBlockK,
+                                                     tile.b_row0);
+                            }
+                        }
+                    } else if (p.ab_3d) {
                         // one load per operand fills the slot's G stages; K-blocks past the
                         // end of K are out of bounds (zero-filled) and still count their bytes
                         if (elect_one()) {
@@ -498,9 +532,14 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             int acc = 0;
             uint32_t acc_phase = 0;
             int g = 0;
-            const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
-            const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
-            constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, Cfg::kBN1, 0, 0);
+            const uint64_t a_desc_base = A_MN ? make_smem_desc(smem_u32(smem_a), 16384, 1024, kSwizzle128B)
+                                              : make_desc_kmajor_sw128(smem_u32(smem_a));
+            const uint64_t b_desc_base = B_MN ? make_smem_desc(smem_u32(smem_b), 16384, 1024, kSwizzle128B)
+                                              : make_desc_kmajor_sw128(smem_u32(smem_b));
+            // a 32-K step: 32 bytes along a K-major row, 32 rows (4096 bytes) of an MN-major tile
+            constexpr uint64_t kStepA = A_MN ? (4096 >> 4) : 2, kStepB = B_MN ? (4096 >> 4) : 2;
+            constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, Cfg::kBN1, 0, 0) | (A_MN ? 1u << 15 : 0u) |
+                                            (B_MN ? 1u << 16 : 0u);
             constexpr uint32_t idesc2_base = make_idesc_mxf8(MMA_M, Cfg::kBN2 > 0 ? Cfg::kBN2 : 16, 0, 0);
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
                 if (!mbar_wait_cluster_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
@@ -529,7 +568,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kB1Bytes >> 4));
 #pragma unroll
                             for (int k = 0; k < kBlockK / 32; ++k) {
-                                tc_mma_mxf8_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, sfa_tmem,
+                                tc_mma_mxf8_pair(d_tmem, a_desc + kStepA * k, b_desc + kStepB * k, idesc, sfa_tmem,
                                                  sfa_tmem + 4, (kb | k) != 0);
                                 if constexpr (Cfg::kBN2 > 0) {
                                     // columns [kBN1, BN): their accumulator columns, B rows and
@@ -934,11 +973,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     }
 }
 
-template <int BN, bool WITH_C, int MP, bool F32>
+template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
     using Cfg = Bs2Config<BN, MP>;
-    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>,
+    cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -954,13 +993,13 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>, maps.a, maps.b, maps.b2, maps.d, p);
+    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>, maps.a, maps.b, maps.b2, maps.d, p);
 }
 
-template <int BN, bool WITH_C, int MP, bool F32>
+template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 int max_active_pairs_impl() {
     using Cfg = Bs2Config<BN, MP>;
-    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>,
+    if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -975,7 +1014,7 @@ int max_active_pairs_impl() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 

@@ -3,10 +3,10 @@
 #include "gemm_bs2_list.h"
 
 namespace dg {
-#define DG_INST2(BN, C, MP, F32)                                                                   \
-    template cudaError_t launch_bs2_gemm_impl<BN, C, MP, F32>(const TensorMaps &, const GemmParams &, \
+#define DG_INST2(BN, C, MP, F32, LAY)                                                                   \
+    template cudaError_t launch_bs2_gemm_impl<BN, C, MP, F32, LAY>(const TensorMaps &, const GemmParams &, \
                                                               int, cudaStream_t);                      \
-    template int max_active_pairs_impl<BN, C, MP, F32>();
+    template int max_active_pairs_impl<BN, C, MP, F32, LAY>();
 DG_BS2_LIST_F32(DG_INST2)
 #undef DG_INST2
 }  // namespace dg

@@ -1,16 +1,22 @@
 // The compiled instantiations of the CTA-pair kernel: (BLOCK_N, with C, rows per
-// pair tile, FP32 D).  The bf16-output ones are instantiated in gemm_bs2_inst.cu,
-// the FP32-output ones in gemm_bs2_inst_f32.cu.
+// pair tile, FP32 D, operand layouts: bit 0 A MN-major, bit 1 B MN-major).  The
+// bf16-output NT ones are instantiated in gemm_bs2_inst.cu, the FP32-output ones
+// in gemm_bs2_inst_f32.cu, the NN/TN/TT ones in gemm_bs2_inst_mn.cu.
 #pragma once
 
 #define DG_BS2_LIST_BF16(X)                                                                        \
-    X(128, false, 256, false) X(128, true, 256, false) X(192, false, 256, false)                   \
-    X(192, true, 256, false) X(224, false, 256, false) X(224, true, 256, false)                    \
-    X(240, false, 256, false) X(240, true, 256, false) X(256, false, 256, false)                   \
-    X(32, false, 128, false) X(64, false, 128, false) X(96, false, 128, false)                     \
-    X(128, false, 128, false) X(384, false, 256, false)
+    X(128, false, 256, false, 0) X(128, true, 256, false, 0) X(192, false, 256, false, 0)                   \
+    X(192, true, 256, false, 0) X(224, false, 256, false, 0) X(224, true, 256, false, 0)                    \
+    X(240, false, 256, false, 0) X(240, true, 256, false, 0) X(256, false, 256, false, 0)                   \
+    X(32, false, 128, false, 0) X(64, false, 128, false, 0) X(96, false, 128, false, 0)                     \
+    X(128, false, 128, false, 0) X(384, false, 256, false, 0)
 
 #define DG_BS2_LIST_F32(X)                                                                         \
-    X(128, false, 256, true) X(128, true, 256, true) X(224, false, 256, true) X(224, true, 256, true)
+    X(128, false, 256, true, 0) X(128, true, 256, true, 0) X(224, false, 256, true, 0) X(224, true, 256, true, 0)
 
-#define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X)
+// NN (B MN-major), TN (both), TT (A MN-major)
+#define DG_BS2_LIST_MN(X)                                                                          \
+    X(256, false, 256, false, 2) X(256, true, 256, false, 2) X(256, false, 256, false, 3)          \
+    X(256, true, 256, false, 3) X(256, false, 256, false, 1) X(256, true, 256, false, 1)
+
+#define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X) DG_BS2_LIST_MN(X)

@@ -21,16 +21,16 @@ DG_BS_BLOCK_N_LIST(DG_EXTERN)
 DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
 #undef DG_EXTERN
 
-#define DG_EXTERN2(BN, C, MP, F32)                                                                 \
-    extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP, F32>(const TensorMaps &,             \
+#define DG_EXTERN2(BN, C, MP, F32, LAY)                                                                 \
+    extern template cudaError_t launch_bs2_gemm_impl<BN, C, MP, F32, LAY>(const TensorMaps &,             \
                                                                      const GemmParams &, int, cudaStream_t); \
-    extern template int max_active_pairs_impl<BN, C, MP, F32>();
+    extern template int max_active_pairs_impl<BN, C, MP, F32, LAY>();
 DG_BS2_LIST(DG_EXTERN2)
 #undef DG_EXTERN2
 
-bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32) {
-#define DG_CASE2(BN, C, MP, F32) \
-    if (block_n == BN && with_c == C && mp == MP && f32 == F32) { fill_bs2_info<BN, MP>(info); return true; }
+bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32, int lay) {
+#define DG_CASE2(BN, C, MP, F32, LAY) \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32 && lay == LAY) { fill_bs2_info<BN, MP>(info); return true; }
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return false;
@@ -40,17 +40,18 @@ cudaError_t launch_bs2_gemm(int block_n, int mp, const TensorMaps &maps, const G
                             cudaStream_t stream) {
     const bool f32 = p.d_f32 != nullptr;
     const bool with_c = f32 ? p.c_f32 != nullptr : p.c != nullptr;
-#define DG_CASE2(BN, C, MP, F32)                                            \
-    if (block_n == BN && with_c == C && mp == MP && f32 == F32)             \
-        return launch_bs2_gemm_impl<BN, C, MP, F32>(maps, p, grid, stream);
+#define DG_CASE2(BN, C, MP, F32, LAY)                                       \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32 && p.layout == LAY) \
+        return launch_bs2_gemm_impl<BN, C, MP, F32, LAY>(maps, p, grid, stream);
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return cudaErrorInvalidValue;
 }
 
-int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32) {
-#define DG_CASE2(BN, C, MP, F32) \
-    if (block_n == BN && with_c == C && mp == MP && f32 == F32) return max_active_pairs_impl<BN, C, MP, F32>();
+int bs2_max_active_pairs(int block_n, bool with_c, int mp, bool f32, int lay) {
+#define DG_CASE2(BN, C, MP, F32, LAY) \
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32 && lay == LAY) \
+        return max_active_pairs_impl<BN, C, MP, F32, LAY>();
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return 0;

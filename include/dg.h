@@ -137,6 +137,41 @@ dg_status dg_fp8_gemm_nt_f32(const void *a, int64_t lda, const void *sfa, int sf
                              void *stream);
 
 /*
+ * dg_fp8_gemm_nn / dg_fp8_gemm_tn / dg_fp8_gemm_tt -- the other three operand
+ * layouts of "DeepSeek V4 源码剖析 第13章" §13.3 (D = C + A @ B, the two suffix
+ * letters giving the transpose state of A and B; the SM100 generation supports
+ * all four).  The product and its scales are those of dg_fp8_gemm_nt; only the
+ * memory order of A and B changes:
+ *
+ *   call  A storage            B storage            D[m,n] = C + sum_k ...
+ *   nn    [m][lda], K contig.  [k][ldb], N contig.  A[m,k] B[k,n]
+ *   tn    [k][lda], M contig.  [k][ldb], N contig.  A[k,m] B[k,n]
+ *   tt    [k][lda], M contig.  [n][ldb], K contig.  A[k,m] B[n,k]
+ *
+ *   Scales: sfa, sfb as for dg_fp8_gemm_nt (one A scale per (m, 128-K block),
+ *   one B scale per (128-N block, 128-K block)); only DG_SF_UE8M0_PACKED is
+ *   accepted here (DG_SF_FP32 gives DG_ERR_UNSUPPORTED).
+ *   Leading dimensions: lda >= k (A K-contiguous) or >= m (M-contiguous);
+ *   ldb >= k or >= n likewise; all multiples of 16 (else DG_ERR_ALIGNMENT).
+ *   k must be a multiple of 16 when an operand is K-contiguous.
+ *   c (bf16 [m, ldc], nullable, may equal d) and d (bf16 [m, ldd]) as for
+ *   dg_fp8_gemm_nt; n, ldd, ldc multiples of 8.  Runs on 256x256 CTA-pair tiles.
+ *   m == 0 or n == 0 is a no-op; k == 0 gives D = C (or 0).
+ */
+dg_status dg_fp8_gemm_nn(const void *a, int64_t lda, const void *sfa, int sfa_fmt,
+                         const void *b, int64_t ldb, const void *sfb, int sfb_fmt,
+                         const void *c, int64_t ldc, void *d, int64_t ldd,
+                         int m, int n, int k, int32_t *status_dev, void *stream);
+dg_status dg_fp8_gemm_tn(const void *a, int64_t lda, const void *sfa, int sfa_fmt,
+                         const void *b, int64_t ldb, const void *sfb, int sfb_fmt,
+                         const void *c, int64_t ldc, void *d, int64_t ldd,
+                         int m, int n, int k, int32_t *status_dev, void *stream);
+dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fmt,
+                         const void *b, int64_t ldb, const void *sfb, int sfb_fmt,
+                         const void *c, int64_t ldc, void *d, int64_t ldd,
+                         int m, int n, int k, int32_t *status_dev, void *stream);
+
+/*
  * dg_m_grouped_fp8_gemm_nt_contiguous -- MoE GEMM grouped along M only
  * (PaperTrace §5.1; "DeepSeek V4 源码剖析 第13章" §13.6): the rows of all
  * experts are concatenated along M, each expert's segment starting on a
