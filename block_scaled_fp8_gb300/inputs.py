@@ -222,3 +222,47 @@ def masked_case(num_groups: int, max_m: int, N: int, K: int, seed: int = 0,
 # (7168, 16384)).
 V3_NK = [(2112, 7168), (24576, 1536), (7168, 16384)]
 V3_M = [128, 4096]
+
+
+@dataclass
+class KGroupedCase:
+    """K-grouped weight-gradient inputs (PaperTrace DeepGEMM §3.3, §5.2): the
+    groups' K rows are concatenated; group e owns rows [K_e, K_e + ks[e]) of A
+    and B and scale rows [K_e/128, (K_e + ks[e])/128)."""
+    a: torch.Tensor      # float8 [K_total, M] (M contiguous)
+    sfa: torch.Tensor    # fp32 [K_total/128, M], one scale per (128-K block, m)
+    b: torch.Tensor      # float8 [K_total, N] (N contiguous)
+    sfb: torch.Tensor    # fp32 [K_total/128, N]
+    c: torch.Tensor      # fp32 [E, M, N]
+    ks: list[int]
+    meta: dict = field(default_factory=dict)
+
+
+def k_grouped_case(num_groups: int, M: int, N: int, seed: int = 0, ks: list[int] | None = None,
+                   k_lo: int = 128, k_hi: int = 4096, align: int = 128, device="cpu") -> KGroupedCase:
+    """Group sizes uniform in [k_lo, k_hi] rounded up to `align` (the token
+    counts per expert of the MoE shapes, stored padded), unless given.  Each
+    group's A and B come from N(0,1), quantised with one scale per 128 rows of
+    K and per column (the 1x128 recipe applied along K)."""
+    g = generator(seed, device)
+    if ks is None:
+        ks = [cdiv(int(v), align) * align
+              for v in torch.randint(k_lo, k_hi + 1, (num_groups,), generator=g, device=device)]
+    assert all(k % GRAN == 0 and k >= 0 for k in ks)
+    k_total = sum(ks)
+    a = torch.empty(k_total, M, dtype=torch.float8_e4m3fn, device=device)
+    b = torch.empty(k_total, N, dtype=torch.float8_e4m3fn, device=device)
+    sfa = torch.empty(k_total // GRAN, M, dtype=torch.float32, device=device)
+    sfb = torch.empty(k_total // GRAN, N, dtype=torch.float32, device=device)
+    k0 = 0
+    for k in ks:
+        if k:
+            for x_out, s_out, mn in ((a, sfa, M), (b, sfb, N)):
+                q, s = quantize_1x128(torch.randn(mn, k, generator=g, dtype=torch.float32, device=device))
+                x_out[k0:k0 + k] = q.t()
+                s_out[k0 // GRAN:(k0 + k) // GRAN] = s.t()
+        k0 += k
+    c = torch.randn(num_groups, M, N, generator=g, dtype=torch.float32, device=device)
+    return KGroupedCase(a, sfa, b, sfb, c, list(ks),
+                        {"E": num_groups, "M": M, "N": N, "K_total": k_total, "seed": seed})
+

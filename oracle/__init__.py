@@ -257,6 +257,68 @@ def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarra
     return d
 
 
+def k_grouped_pack_sf(sf: np.ndarray, ks) -> np.ndarray:
+    """Packed scales of the K-grouped GEMM (PaperTrace DeepGEMM §3.3).
+
+    sf: FP32 [sum_k ks/128, mn], one row per 128-K block of the concatenated
+    groups, mn contiguous, mn % 4 == 0.  Each group is packed on its own and
+    the results are concatenated: packed row q of group e holds in byte j the
+    UE8M0 byte (the exponent bits, >> 23) of the group's scale row 4q + j, and 0
+    where the group has no such row.  Returns int32 [sum_e ceil(ks[e]/512), mn].
+    """
+    sf = np.ascontiguousarray(sf, dtype=np.float32)
+    mn = sf.shape[1]
+    assert mn % 4 == 0
+    rows = [k // 128 for k in ks]
+    assert all(k % 128 == 0 and k >= 0 for k in ks) and sum(rows) == sf.shape[0]
+    exp = ((sf.view(np.uint32) >> 23) & 0xFF).astype(np.uint32)
+    out = []
+    r0 = 0
+    for s in rows:
+        for q in range((s + 3) // 4):
+            word = np.zeros(mn, dtype=np.uint32)
+            for j in range(4):
+                if 4 * q + j < s:
+                    word |= exp[r0 + 4 * q + j] << np.uint32(8 * j)
+            out.append(word)
+        r0 += s
+    return np.array(out, dtype=np.uint32).reshape(len(out), mn).view(np.int32)
+
+
+def k_grouped_gemm_tn(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarray, ks,
+                      c: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """K-grouped GEMM for MoE weight gradients (PaperTrace DeepGEMM §5.2,
+    §3.3; "DeepSeek V4 源码剖析 第13章" §13.3 naming): M and N are fixed and
+    the groups are concatenated along K; for each group e
+
+        D_e[m, n] = C_e[m, n] + sum over group e's k of A[k, m] sa(k/128, m) B[k, n] sb(k/128, n)
+
+    a: uint8 E4M3 [K_total, M] (M contiguous, the "t" operand); b: uint8
+    [K_total, N] (N contiguous, the "n" operand); sa: fp64 [K_total/128, M];
+    sb: fp64 [K_total/128, N]; ks: group sizes, multiples of 128 (0 allowed);
+    c: FP32 [E, M, N] (required, as the pages make C mandatory here).
+    fp64 sum started from C, rounded once to FP32.  Returns FP32 [E, M, N].
+    """
+    a, b = _u8(a), _u8(b)
+    M, N = a.shape[1], b.shape[1]
+    c = np.ascontiguousarray(c, dtype=np.float32)
+    E = len(ks)
+    assert c.shape == (E, M, N) and a.shape[0] == b.shape[0] == sum(ks)
+    d = np.empty((E, M, N), dtype=np.float32)
+    k0 = 0
+    for e, k in enumerate(ks):
+        assert k % 128 == 0 and k >= 0
+        if k == 0:
+            d[e] = c[e]
+        else:
+            s0, s1 = k0 // 128, (k0 + k) // 128
+            d[e] = gemm_nt_f32(np.ascontiguousarray(a[k0:k0 + k].T), np.ascontiguousarray(sa[s0:s1].T),
+                               np.ascontiguousarray(b[k0:k0 + k].T), np.ascontiguousarray(sb[s0:s1].T),
+                               c=c[e], nthreads=nthreads)
+        k0 += k
+    return d
+
+
 def gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, c=None, want_pre=False, nthreads: int = 0):
     """The elements (rows[i], cols[i]) of gemm_nt, computed one by one."""
     a, b = _u8(a), _u8(b)

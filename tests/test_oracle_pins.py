@@ -575,3 +575,78 @@ def test_gemm_layouts_bruteforce_from_storage(orc, layout, M, N, K, seed):
                           Fraction(float(bv)) * Fraction(float(sb_rows[n, k // 128])))
             assert Fraction(pre[m, n]) == s, (layout, m, n)
             assert d[m, n] == _bf16_nearest_bruteforce(s)
+
+
+# ---------------------------------------------------------------- K-grouped GEMM
+
+def test_k_grouped_bruteforce_from_storage(orc):
+    """PaperTrace DeepGEMM §5.2 / §3.3: groups concatenated along K, one D per
+    group, C mandatory.  The brute force reads A[k, m], B[k, n] and the scale
+    rows straight from storage by index; power-of-two scales keep every term
+    exact, so each FP32 output is the single rounding of the rational sum.
+    The empty group must give D = C exactly."""
+    ks = [128, 0, 256]
+    M, N = 3, 5
+    case = inputs.k_grouped_case(3, M, N, seed=61, ks=ks)
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    A = _decode_codes_torch(case.a.view(torch.uint8))
+    B = _decode_codes_torch(case.b.view(torch.uint8))
+    sa = case.sfa.double().numpy()
+    sb = case.sfb.double().numpy()
+    c = case.c.numpy()
+    d = orc.k_grouped_gemm_tn(a, sa, b, sb, ks, c)
+    assert d.shape == (3, M, N) and d.dtype == np.float32
+    assert np.array_equal(d[1], c[1])
+    k0 = 0
+    for e, k in enumerate(ks):
+        for m in range(M):
+            for n in range(N):
+                s = Fraction(float(c[e, m, n]))
+                for kk in range(k0, k0 + k):
+                    if A[kk, m] and B[kk, n]:
+                        s += (Fraction(float(A[kk, m])) * Fraction(float(sa[kk // 128, m])) *
+                              Fraction(float(B[kk, n])) * Fraction(float(sb[kk // 128, n])))
+                assert d[e, m, n] == np.float32(float(s)), (e, m, n)
+        k0 += k
+
+
+def test_k_grouped_split_invariance_integer_exact(orc):
+    """Integer codes and power-of-two scales make every sum exact in FP32: with
+    C = 0, splitting one group of 512 rows into two of 256 and adding the two
+    outputs must give the one-group output, and both must equal the float64
+    matmul of the decoded operands."""
+    g = torch.Generator().manual_seed(62)
+    K, M, N = 512, 8, 12
+    ai = torch.randint(-8, 9, (K, M), generator=g).float()
+    bi = torch.randint(-8, 9, (K, N), generator=g).float()
+    sa = torch.ldexp(torch.ones(K // 128, M, dtype=torch.float64), torch.randint(-2, 1, (K // 128, M), generator=g))
+    sb = torch.ldexp(torch.ones(K // 128, N, dtype=torch.float64), torch.randint(0, 3, (K // 128, N), generator=g))
+    a = ai.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    b = bi.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    one = orc.k_grouped_gemm_tn(a, sa.numpy(), b, sb.numpy(), [512], np.zeros((1, M, N), np.float32))
+    two = orc.k_grouped_gemm_tn(a, sa.numpy(), b, sb.numpy(), [256, 256], np.zeros((2, M, N), np.float32))
+    x = ai.double() * sa.repeat_interleave(128, 0)
+    w = bi.double() * sb.repeat_interleave(128, 0)
+    exact = (x.T @ w).numpy()
+    assert np.array_equal(one[0].astype(np.float64), exact)
+    assert np.array_equal(two[0].astype(np.float64) + two[1].astype(np.float64), exact)
+    assert np.array_equal((x[:256].T @ w[:256]).numpy(), two[0].astype(np.float64))
+
+
+def test_k_grouped_pack_hand_worked(orc):
+    """PaperTrace DeepGEMM §3.3: each group packed on its own, 4 scale rows per
+    int32, the last packed row of a group zero-filled past its rows.  ks =
+    [256, 640, 0, 128] gives 2, 5, 0 and 1 scale rows, hence 1 + 2 + 0 + 1
+    packed rows.  Scale row r, column i is 2^(r - i): UE8M0 byte 0x7F + r - i.
+    The words below were worked out by hand (byte j = row 4q + j of the group)."""
+    mn = 4
+    sf = np.array([[2.0 ** (r - i) for i in range(mn)] for r in range(8)], dtype=np.float32)
+    got = orc.k_grouped_pack_sf(sf, [256, 640, 0, 128]).view(np.uint32)
+    want = np.array([
+        [0x0000807F, 0x00007F7E, 0x00007E7D, 0x00007D7C],   # group 0: rows 0, 1
+        [0x84838281, 0x83828180, 0x8281807F, 0x81807F7E],   # group 1: rows 2..5
+        [0x00000085, 0x00000084, 0x00000083, 0x00000082],   # group 1: row 6
+        [0x00000086, 0x00000085, 0x00000084, 0x00000083],   # group 3: row 7
+    ], dtype=np.uint32)
+    assert np.array_equal(got, want)
