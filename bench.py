@@ -233,6 +233,20 @@ def measure_other_workloads(dev, flush, reps, stream):
                    {"valid_rows": valid, "rows": mt})
         del cc, sfa, sfb, d
 
+    # K-grouped weight gradient of the contiguous MoE layer (8 experts, N=4096 x K=7168
+    # weights): D_e[4096, 7168] += dY_e^T X_e over each expert's tokens, in place in FP32
+    kc = inputs.k_grouped_case(8, 4096, 7168, seed=3, device=dev)
+    sfa = binding.dg_transform_sf_k_grouped(kc.sfa, kc.ks)
+    sfb = binding.dg_transform_sf_k_grouped(kc.sfb, kc.ks)
+    ks_dev = torch.tensor(kc.ks, dtype=torch.int32, device=dev)
+    kt = sum(kc.ks)
+    record(f"k-grouped weight gradient 8 groups M=4096 N=7168 K_total={kt}",
+           lambda: binding.dg_k_grouped_fp8_gemm_tn_contiguous(kc.a, sfa, kc.b, sfb, kc.c, kc.ks, ks_dev=ks_dev,
+                                                               c=kc.c, status=status),
+           flops(4096, 7168, kt), kt * (4096 + 7168) + 2 * 4 * 8 * 4096 * 7168,
+           {"d": "fp32, in place", "ks": kc.ks})
+    del kc, sfa, sfb, ks_dev
+
     # masked grouped decode: 32 experts, max_m 256
     n, k, e, max_m = 4096, 7168, 32, 256
     mc = inputs.masked_case(e, max_m, n, k, seed=4, device=dev)

@@ -31,6 +31,7 @@ DG_DEBUG_WIDE_PAIR = 8
 EXPORTS = (
     "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn", "dg_fp8_gemm_tt",
     "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
+    "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped", "dg_k_grouped_packed_sf_rows",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
     "dg_set_wait_timeout_ms", "dg_set_debug_flags", "dg_status_string", "dg_get_last_config",
@@ -70,6 +71,13 @@ def lib():
                 L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes
             L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
                                                           i32, i32, i32, P, P]
+            L.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [P, i64, P, P, i64, P, P, P, i32, i32, P, P, i32,
+                                                              P, P]
+            L.dg_transform_sf_k_grouped.argtypes = [P, i32, P, i32, P, P, P]
+            L.dg_k_grouped_packed_sf_rows.restype = i64
+            L.dg_k_grouped_packed_sf_rows.argtypes = [P, i32]
+            for f in ("dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped"):
+                getattr(L, f).restype = i32
             for f in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn",
                       "dg_fp8_gemm_tt", "dg_transform_sf",
                       "dg_m_grouped_fp8_gemm_nt_contiguous",
@@ -241,6 +249,47 @@ def dg_fp8_gemm_tn(a, sfa, b, sfb, d, c=None, status=None, stream=None):
 def dg_fp8_gemm_tt(a, sfa, b, sfb, d, c=None, status=None, stream=None):
     """D = C + A^T @ B^T: a [K, M] (M contiguous), b [N, K] (K contiguous)."""
     return _gemm_layout("dg_fp8_gemm_tt", True, False, a, sfa, b, sfb, d, c, status, stream)
+
+
+def _ks_host(ks):
+    arr = (ctypes.c_int * max(1, len(ks)))(*[int(k) for k in ks])
+    return arr
+
+
+def k_grouped_packed_sf_rows(ks) -> int:
+    """Packed scale rows of the K-grouped layout for group sizes ks (-1 if invalid)."""
+    return int(lib().dg_k_grouped_packed_sf_rows(_ks_host(ks), len(ks)))
+
+
+def dg_transform_sf_k_grouped(sf: torch.Tensor, ks, out: torch.Tensor | None = None,
+                              status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """sf FP32 [sum(ks)/128, mn] -> packed int32 [k_grouped_packed_sf_rows(ks), mn]."""
+    assert sf.dtype == torch.float32 and sf.is_contiguous()
+    mn = sf.shape[1]
+    if out is None:
+        out = torch.empty(max(0, k_grouped_packed_sf_rows(ks)), mn, dtype=torch.int32, device=sf.device)
+    _check("dg_transform_sf_k_grouped", lib().dg_transform_sf_k_grouped(
+        _p(sf), mn, _ks_host(ks), len(ks), _p(out), _p(status), _stream(stream)))
+    return out
+
+
+def dg_k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, d, ks, ks_dev=None, c=None,
+                                        status: torch.Tensor | None = None, stream=None):
+    """D[e] = C[e] + A_e^T B_e.  a [K_total, M] and b [K_total, N] float8_e4m3fn
+    (unit column stride, row stride = stride(0)); sfa/sfb packed int32
+    [P, M] / [P, N]; c (required, may be d) and d FP32 [E, M, N] contiguous;
+    ks host list of group sizes (multiples of 128); ks_dev the same as a
+    device int32 tensor (made here if not given)."""
+    K, M = a.shape
+    N = b.shape[1]
+    assert a.stride(1) == 1 and b.stride(1) == 1 and d.is_contiguous() and d.dtype == torch.float32
+    assert c is not None and c.is_contiguous() and c.dtype == torch.float32
+    if ks_dev is None:
+        ks_dev = torch.tensor(list(ks), dtype=torch.int32, device=d.device)
+    _check("dg_k_grouped_fp8_gemm_tn_contiguous", lib().dg_k_grouped_fp8_gemm_tn_contiguous(
+        _p(a), a.stride(0), _p(sfa), _p(b), b.stride(0), _p(sfb), _p(c), _p(d), M, N, _ks_host(ks),
+        _p(ks_dev), len(ks), _p(status), _stream(stream)))
+    return d
 
 
 def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, grouped_layout,

@@ -354,8 +354,9 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
                         32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
     set_scale_words(p, o);
-    // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused)
-    if (p.mode != kModeMasked) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));
+    // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused;
+    // K-grouped: the caller sets the m-units of one group)
+    if (p.mode == kModeDense || p.mode == kModeContiguous) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
     p.cluster = 2;
@@ -879,6 +880,102 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void *a, const void *sfa, int sf
     return launch_block_scaled(p, o, m_blocks_hint,
                                static_cast<int64_t>(num_groups) * p.num_m_blocks, sms,
                                static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------ K-grouped (weight gradient)
+
+// Packed rows of the K-grouped scales (sum of ceil(ks[e] / 512)), or -1 if ks
+// is invalid: null with groups, more than 255 groups, a size negative or not a
+// multiple of 128, or more than 65535 packed rows.
+static int64_t k_grouped_rows(const int *ks, int num_groups, KGroupRows *t) {
+    if (num_groups < 0 || num_groups > kMaxPsumGroups || (num_groups > 0 && ks == nullptr)) return -1;
+    int64_t srow = 0, prow = 0;
+    if (t) t->num_groups = num_groups;
+    for (int e = 0; e < num_groups; ++e) {
+        if (ks[e] < 0 || ks[e] % kBlockK != 0) return -1;
+        if (t) {
+            t->srow[e] = static_cast<int>(srow);
+            t->prow[e] = static_cast<int>(prow);
+        }
+        srow += ks[e] / kBlockK;
+        prow += (ks[e] / kBlockK + 3) / 4;
+        if (prow > 65535) return -1;
+    }
+    if (t) {
+        t->srow[num_groups] = static_cast<int>(srow);
+        t->prow[num_groups] = static_cast<int>(prow);
+    }
+    return prow;
+}
+
+int64_t dg_k_grouped_packed_sf_rows(const int *ks, int num_groups) {
+    return k_grouped_rows(ks, num_groups, nullptr);
+}
+
+dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                    int32_t *status_dev, void *stream) {
+    if (mn < 0) return DG_ERR_INVALID_ARG;
+    KGroupRows t;
+    const int64_t prows = k_grouped_rows(ks, num_groups, &t);
+    if (prows < 0) return DG_ERR_INVALID_ARG;
+    if (mn % 4 != 0) return DG_ERR_LAYOUT;
+    if (mn == 0 || prows == 0) return DG_OK;
+    if (sf == nullptr || out == nullptr) return DG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(sf) & 3u) || !aligned16(out)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    dg_status st = check_device(&sms);
+    if (st != DG_OK) return st;
+    cudaError_t e = launch_transform_sf_k_grouped(sf, mn, t, static_cast<int>(prows), out, status_dev,
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
+                                              int64_t ldb, const void *sfb, const float *c, float *d, int m,
+                                              int n, const int *ks, const int32_t *ks_dev, int num_groups,
+                                              int32_t *status_dev, void *stream) {
+    if (m < 0 || n < 0) return DG_ERR_INVALID_ARG;
+    const int64_t prows = k_grouped_rows(ks, num_groups, nullptr);
+    if (prows < 0) return DG_ERR_INVALID_ARG;
+    if (m == 0 || n == 0 || num_groups == 0) return DG_OK;
+    if (c == nullptr || d == nullptr) return DG_ERR_INVALID_ARG;   // C is required
+    if (m % 4 != 0 || n % 4 != 0) return DG_ERR_LAYOUT;            // packed scales: mn % 4 == 0
+    if (!aligned16(c) || !aligned16(d)) return DG_ERR_ALIGNMENT;
+    const int64_t rows = static_cast<int64_t>(num_groups) * m;
+    if (rows > INT32_MAX || rows * n > (int64_t(1) << 40)) return DG_ERR_UNSUPPORTED;
+    int64_t k_total = 0;
+    for (int e = 0; e < num_groups; ++e) k_total += ks[e];
+    if (k_total > INT32_MAX) return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    dg_status st = check_device(&sms);
+    if (st != DG_OK) return st;
+    if (k_total == 0) {
+        // every group is empty: D = C
+        dg_fill_d_f32_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(c, n, d, n,
+                                                                                      static_cast<int>(rows), n);
+        g_last_config[5] = 1;
+        return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    }
+    if (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr || ks_dev == nullptr)
+        return DG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    if (lda < m || ldb < n) return DG_ERR_INVALID_ARG;
+    if (lda % 16 != 0 || ldb % 16 != 0) return DG_ERR_ALIGNMENT;
+    GemmParams p = base_params(kModeKGrouped, static_cast<int>(rows), n, static_cast<int>(k_total), status_dev);
+    p.num_groups = num_groups;
+    p.ks = ks_dev;
+    p.group_rows = m;
+    p.num_m_blocks = static_cast<int>(cdiv64(m, 2 * kBlockM));   // m-units of one group
+    p.layout = 3;                                                 // A [K][M], B [K][N]
+    p.c_f32 = c;
+    p.d_f32 = d;
+    p.ldc = n;
+    BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),
+                 sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(prows),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(prows),
+                 d,   n,   static_cast<uint64_t>(rows)};
+    const int64_t units = static_cast<int64_t>(num_groups) * p.num_m_blocks;
+    return launch_pair(p, o, 256, 256, units, sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

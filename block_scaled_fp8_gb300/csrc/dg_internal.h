@@ -18,7 +18,7 @@ constexpr int kMaxPairPrefix = 512;
 // Experts of the PSUM contiguous layout (8-bit ids in the pair kernel's unit info).
 constexpr int kMaxPsumGroups = 255;
 
-enum GemmMode : int { kModeDense = 0, kModeContiguous = 1, kModeMasked = 2 };
+enum GemmMode : int { kModeDense = 0, kModeContiguous = 1, kModeMasked = 2, kModeKGrouped = 3 };
 
 // Runtime parameters of one GEMM launch (passed by value).
 struct GemmParams {
@@ -35,6 +35,8 @@ struct GemmParams {
     const int32_t *grouped_layout;  // contiguous: expert id per row
     const int32_t *psum;            // contiguous with PSUM offsets instead: [num_groups]
     const int32_t *masked_m;        // masked
+    const int32_t *ks;              // K-grouped: rows of K per group [num_groups], multiples of 128
+    int group_rows;                 // K-grouped: M, the rows of each group's D
     const uint16_t *c;   // dense: bf16 C or nullptr
     int64_t ldc;
     uint16_t *d;         // bf16 D (used for direct stores)
@@ -95,6 +97,15 @@ cudaError_t launch_promote_gemm(int block_n, const TensorMaps &maps, const GemmP
                                 cudaStream_t stream);
 
 // Scale-factor transform.
+// Scale rows of the K-grouped layout, per group: srow[e] = first 128-K block
+// (FP32 scale row), prow[e] = first packed row; entries 0..num_groups.
+struct KGroupRows {
+    int num_groups;
+    int srow[kMaxPsumGroups + 2];
+    int prow[kMaxPsumGroups + 2];
+};
+cudaError_t launch_transform_sf_k_grouped(const float *sf, int mn, const KGroupRows &t, int packed_rows,
+                                          void *out, int32_t *status, cudaStream_t stream);
 cudaError_t launch_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn,
                                 int mn, int out_fmt, void *out, int32_t *status,
                                 cudaStream_t stream);

@@ -120,6 +120,9 @@ struct PairTile {
     int sfb_y0;      // row of the packed SFB view for K-slice 0
     int valid_rows;  // rows of this CTA's MP/2 that are stored (0: none)
     int zero_tail;   // the rest of this CTA's rows are gap rows, written 0 (PSUM layout)
+    int d_row0;      // this CTA's first row of D (and C): a_row0 except for the K-grouped layout
+    int kb0;         // first 128-K block of the tile's K range
+    int nkb;         // 128-K blocks in the tile's K range (K-grouped: 0 for an empty group)
 };
 
 // Pair units.  A unit is the row range of one pair tile; the tiles are the
@@ -225,6 +228,28 @@ __device__ __forceinline__ void build_psum_segments(const GemmParams &p, int *se
 // scratch (2 * (kMaxPsumGroups + 1) ints, dead afterwards) holds the PSUM
 // segments.  Ends with __syncthreads.
 __device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *prefix, int *info, int *scratch) {
+    if (p.mode == kModeKGrouped) {
+        // prefix[e]: first 128-K block of group e; info[e]: its first packed scale row
+        // (each group's scale rows are packed on their own, 4 per word)
+        const int E = p.num_groups;
+        for (int i = threadIdx.x; i < E; i += blockDim.x) {
+            int k = __ldg(p.ks + i);
+            if (k < 0 || k % kBlockK != 0) {
+                if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
+                k = 0;
+            }
+            prefix[i + 1] = k / kBlockK;
+            info[i + 1] = (k / kBlockK + 3) / 4;
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) warp0_prefix_sums(prefix, E, threadIdx.x);
+        else if (threadIdx.x < 64) warp0_prefix_sums(info, E, threadIdx.x - 32);
+        __syncthreads();
+        // more K than the operands hold: the loads past the end read zeros, the words nothing
+        if (threadIdx.x == 0 && p.status && (prefix[E] > p.num_k_blocks || info[E] > p.sfa_slices))
+            atomicOr(p.status, DG_DEV_BAD_GROUP);
+        return;
+    }
     const bool psum = p.mode == kModeContiguous && p.psum != nullptr;
     int *seg = scratch, *cnt = scratch + kMaxPsumGroups + 1;
     if (psum) build_psum_segments(p, seg, cnt);
@@ -273,6 +298,7 @@ __device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *pref
 
 __device__ __forceinline__ int pair_units(const GemmParams &p, const int *prefix) {
     if (p.mode == kModeDense) return p.num_m_blocks;
+    if (p.mode == kModeKGrouped) return p.num_groups * p.num_m_blocks;   // m-units per group
     return prefix[p.mode == kModeMasked ? p.num_groups : p.num_m_blocks];
 }
 
@@ -292,11 +318,26 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     tile.n0 = nb * BN;
     int group = 0;
     tile.zero_tail = 0;
+    tile.kb0 = 0;
+    tile.nkb = p.num_k_blocks;
     if (MP == 128 || p.mode == kModeDense) {
         tile.a_row0 = u * MP + rank * (MP / 2);
         tile.sfa_x = tile.a_row0;
         tile.sfa_y0 = 0;
         tile.valid_rows = MP / 2;
+    } else if (p.mode == kModeKGrouped) {
+        // unit u = (group e, m-unit): A and B are [K][M] / [K][N], so the tile's
+        // coordinates along M and N are those of a dense tile; D is [E * M][N]
+        const int e = u / p.num_m_blocks;
+        const int m0 = (u - e * p.num_m_blocks) * MP + rank * (MP / 2);
+        tile.a_row0 = m0;
+        tile.sfa_x = m0;
+        tile.sfa_y0 = info[e];
+        tile.d_row0 = e * p.group_rows + m0;
+        const int v = p.group_rows - m0;
+        tile.valid_rows = v <= 0 ? 0 : (v < MP / 2 ? v : MP / 2);
+        tile.kb0 = prefix[e];
+        tile.nkb = prefix[e + 1] - prefix[e];
     } else if (p.mode == kModeContiguous) {
         const int j = prefix_find(prefix, p.num_m_blocks, u);
         int e0, e1, v0 = kBlockM, v1 = kBlockM;
@@ -335,7 +376,8 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     }
     tile.b_row0 = group * p.n + tile.n0 + rank * Bs2Config<BN, MP>::kB1Rows;
     tile.b2_row0 = group * p.n + tile.n0 + Bs2Config<BN, MP>::kBN1 + rank * Bs2Config<BN, MP>::kB2Rows;
-    tile.sfb_y0 = group * psf_k;
+    tile.sfb_y0 = p.mode == kModeKGrouped ? tile.sfa_y0 : group * psf_k;
+    if (p.mode != kModeKGrouped) tile.d_row0 = tile.a_row0;
 }
 
 // LAY: operand layouts, bit 0 = A MN-major (stored [K][M]), bit 1 = B MN-major
@@ -446,8 +488,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
             PairTile tile;
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tile);
-            for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
-                const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+            for (int kb0 = 0; kb0 < tile.nkb; kb0 += G) {
+                const int nk = tile.nkb - kb0 < G ? tile.nkb - kb0 : G;
+                const int kg0 = tile.kb0 + kb0;   // the slot's first 128-K block in the operands
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                 if (drop) {
                     drop = false;  // diagnostic: leave this slot empty
@@ -462,19 +505,19 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             uint8_t *a_slot = smem_a + slot * G * Cfg::kABytes;
                             uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
                             if constexpr (A_MN) {
-                                tma_load_2d_pair(a_slot, &tm_a, fb, tile.a_row0, kb0 * kBlockK);
+                                tma_load_2d_pair(a_slot, &tm_a, fb, tile.a_row0, kg0 * kBlockK);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < G; ++j)
-                                    tma_load_2d_pair(a_slot + j * Cfg::kABytes, &tm_a, fb, (kb0 + j) * kBlockK,
+                                    tma_load_2d_pair(a_slot + j * Cfg::kABytes, &tm_a, fb, (kg0 + j) * kBlockK,
                                                      tile.a_row0);
                             }
                             if constexpr (B_MN) {
-                                tma_load_2d_pair(b_slot, &tm_b, fb, tile.b_row0, kb0 * kBlockK);
+                                tma_load_2d_pair(b_slot, &tm_b, fb, tile.b_row0, kg0 * kBlockK);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < G; ++j)
-                                    tma_load_2d_pair(b_slot + j * Cfg::kB1Bytes, &tm_b, fb, (kb0 + j) * kBlockK,
+                                    tma_load_2d_pair(b_slot + j * Cfg::kB1Bytes, &tm_b, fb, (kg0 + j) * kBlockK,
                                                      tile.b_row0);
                             }
                         }
@@ -484,10 +527,10 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         if (elect_one()) {
                             if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * G * Cfg::kStageBytes);
                             uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
-                            tma_load_3d_pair(smem_a + slot * G * Cfg::kABytes, &tm_a, fb, 0, tile.a_row0, kb0);
-                            tma_load_3d_pair(b_slot, &tm_b, fb, 0, tile.b_row0, kb0);
+                            tma_load_3d_pair(smem_a + slot * G * Cfg::kABytes, &tm_a, fb, 0, tile.a_row0, kg0);
+                            tma_load_3d_pair(b_slot, &tm_b, fb, 0, tile.b_row0, kg0);
                             if constexpr (Cfg::kBN2 > 0)
-                                tma_load_3d_pair(b_slot + G * Cfg::kB1Bytes, &tm_b2, fb, 0, tile.b2_row0, kb0);
+                                tma_load_3d_pair(b_slot + G * Cfg::kB1Bytes, &tm_b2, fb, 0, tile.b2_row0, kg0);
                         }
                     } else if (elect_one()) {
                         // the leader expects both CTAs' bytes; each CTA's loads count there
@@ -495,7 +538,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         // a slot's B: the G K-blocks of the first MMA's rows, then the G
                         // K-blocks of the second's
                         auto load_kb = [&](int j) {
-                            const int kb = kb0 + j;
+                            const int kb = kg0 + j;
                             uint8_t *b_slot = smem_b + slot * G * Cfg::kBBytes;
                             tma_load_2d_pair(smem_a + (slot * G + j) * Cfg::kABytes, &tm_a, fb, kb * kBlockK,
                                              tile.a_row0);
@@ -542,11 +585,19 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                             (B_MN ? 1u << 16 : 0u);
             constexpr uint32_t idesc2_base = make_idesc_mxf8(MMA_M, Cfg::kBN2 > 0 ? Cfg::kBN2 : 16, 0, 0);
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
+                // the tile's 128-K blocks (K-grouped: its group's; none for an empty group,
+                // whose accumulator is then handed over unwritten and read as zero)
+                int nkb = p.num_k_blocks;
+                if (p.mode == kModeKGrouped) {
+                    PairTile tl;
+                    get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tl);
+                    nkb = tl.nkb;
+                }
                 if (!mbar_wait_cluster_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * ACC;
-                for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
-                    const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
+                for (int kb0 = 0; kb0 < nkb; kb0 += G) {
+                    const int nk = nkb - kb0 < G ? nkb - kb0 : G;
                     const int sslot = g % NTS;
                     if ((kb0 & 3) == 0) {
                         if (!mbar_wait_warp(&sf_ready_bar[sslot], (g / NTS) & 1, ctl, DG_DEV_TIMEOUT))
@@ -558,7 +609,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     const uint64_t a_desc0 = a_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kABytes >> 4));
                     const uint64_t b_desc0 = b_desc_base + static_cast<uint64_t>(slot * G * (Cfg::kBBytes >> 4));
                     const int kb_last = kb0 + nk - 1;
-                    const bool group_end = (kb_last & 3) == 3 || kb_last == p.num_k_blocks - 1;
+                    const bool group_end = (kb_last & 3) == 3 || kb_last == nkb - 1;
                     if (elect_one()) {
                         auto mma_kb = [&](int j) {
                             const int kb = kb0 + j;
@@ -622,11 +673,32 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         static_assert(NSF % NW == 0, "scale slots per warp");
         const int sw = static_cast<int>(warp) - Cfg::kSfWarp;
         const uint32_t leader_peer = mapa_shared(smem_u32(sf_peer_bar), 0);
-        // this pair's groups: tiles pair_id, pair_id + num_pairs, ... times groups_per_tile
-        const int num_groups_here =
-            pair_id < num_tiles ? (num_tiles - pair_id + num_pairs - 1) / num_pairs * groups_per_tile : 0;
+        // groups of 4 K-blocks in tile t: the same for every tile, except in the
+        // K-grouped layout, where a tile has its group's K-blocks (maybe none)
+        auto tile_groups = [&](int t) -> int {
+            if (p.mode != kModeKGrouped) return groups_per_tile;
+            PairTile tl;
+            get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, t, rank, tl);
+            return (tl.nkb + 3) >> 2;
+        };
+        // this pair's groups: those of tiles pair_id, pair_id + num_pairs, ...
+        int num_groups_here = 0;
+        if (p.mode != kModeKGrouped)
+            num_groups_here =
+                pair_id < num_tiles ? (num_tiles - pair_id + num_pairs - 1) / num_pairs * groups_per_tile : 0;
+        else
+            for (int t = pair_id; t < num_tiles; t += num_pairs) num_groups_here += tile_groups(t);
         int lt = pair_id, lj = sw;  // tile and group of the next load
-        while (lj >= groups_per_tile) { lj -= groups_per_tile; lt += num_pairs; }
+        int lt_groups = lt < num_tiles ? tile_groups(lt) : 0;
+        // moves (lt, lj) past the end of tile lt's groups
+        auto settle = [&]() {
+            while (lt < num_tiles && lj >= lt_groups) {
+                lj -= lt_groups;
+                lt += num_pairs;
+                lt_groups = lt < num_tiles ? tile_groups(lt) : 0;
+            }
+        };
+        settle();
         int gl = sw;                // next group to load (this warp's: sw, sw + NW, ...)
         int st_t = -1;              // tile whose coordinates st holds
         PairTile st;
@@ -674,7 +746,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                           128 + 4 * (32 * h + lane) + q);
                 }
                 lj += NW;
-                while (lj >= groups_per_tile) { lj -= groups_per_tile; lt += num_pairs; }
+                settle();
             }
             cp_async_commit();
             gl += NW;
@@ -743,7 +815,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         // C (bf16) of one chunk of this thread's row; zero outside [rows, n)
         auto load_c = [&](const PairTile &tl, int j, uint32_t (&dst)[8]) {
             const int c = 2 * j + half;
-            const int row = tl.a_row0 + row_off + lane;
+            const int row = tl.d_row0 + row_off + lane;
             const int col0 = tl.n0 + col_off + c * Cfg::kEpiChunk;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -783,9 +855,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     // the valid rows; with zero_tail the block's other rows get 0
                     const int local_row = row_off + static_cast<int>(lane);
                     const bool value = local_row < tile.valid_rows;
-                    // (zero_tail: contiguous layout, where a_row0 indexes the D rows directly)
-                    if (value || (tile.zero_tail && tile.a_row0 + local_row < p.rows)) {
-                        uint16_t *drow = p.d + static_cast<int64_t>(tile.a_row0 + local_row) * p.ldd + col0;
+                    if (value || (tile.zero_tail && tile.d_row0 + local_row < p.rows)) {
+                        uint16_t *drow = p.d + static_cast<int64_t>(tile.d_row0 + local_row) * p.ldd + col0;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
                             if (col0 + 8 * h < p.n)
@@ -806,7 +877,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tm_d, sbuf, col0, tile.a_row0 + row_off);
+                    tma_store_2d(&tm_d, sbuf, col0, tile.d_row0 + row_off);
                     bulk_commit_group();
                 }
                 buf ^= 1;
@@ -817,7 +888,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> two
                 // 8-column FP32 boxes through the staging buffers; the accumulator is
                 // released after its last chunk is read
-                const int row = tile.a_row0 + row_off + static_cast<int>(lane);
+                const int row = tile.d_row0 + row_off + static_cast<int>(lane);
 #pragma unroll 1
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
                     const int c = 2 * j + half;
@@ -834,9 +905,15 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         }
                     }
                     uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v);
-                    tmem_ld_wait();
-                    reg_fence16(v);
+                    if (tile.nkb > 0) {
+                        tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v);
+                        tmem_ld_wait();
+                        reg_fence16(v);
+                    } else {
+                        // no K-blocks (an empty group): the accumulator was never written
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0u;
+                    }
                     float f[16];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -876,7 +953,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.a_row0 + row_off);
+                            tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
                             bulk_commit_group();
                         }
                         buf ^= 1;

@@ -57,6 +57,64 @@ __global__ void __launch_bounds__(256) dg_transform_sf_f32_kernel(
     out[(static_cast<int64_t>(b) * sf_k + k) * stride + i] = v;
 }
 
+// K-grouped scales (PaperTrace "02 · DeepGEMM 技术解析" §3.3): the input is
+// FP32 [rows][mn], one row per 128-K block of the concatenated groups, mn
+// contiguous; each group's rows are packed on their own, 4 per word (byte j =
+// the group's row 4q + j, 0 past its last row), and the groups' packed rows
+// follow one another.  One thread per output word; consecutive threads take
+// consecutive MN indices.
+__global__ void __launch_bounds__(256) dg_transform_sf_k_grouped_kernel(
+    const float *__restrict__ sf, int mn, const __grid_constant__ KGroupRows t, uint32_t *__restrict__ out,
+    int32_t *status) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int prow = blockIdx.y;
+    // the group holding packed row prow: prow[e] <= prow < prow[e + 1] (empty
+    // groups have prow[e] == prow[e + 1] and are skipped)
+    int lo = 0, hi = t.num_groups;   // number of e in [1, num_groups] with t.prow[e] <= prow
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (t.prow[mid] <= prow) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int r0 = t.srow[e] + 4 * (prow - t.prow[e]);
+    const int nrow = t.srow[e + 1] - r0;
+    uint32_t word = 0;
+    bool inexact = false;
+    if (i < mn) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nrow) {
+                const uint32_t bits = __float_as_uint(__ldg(sf + static_cast<int64_t>(r0 + j) * mn + i));
+                word |= ((bits >> 23) & 0xFFu) << (8 * j);
+                inexact |= (bits & 0x807FFFFFu) != 0u;
+            }
+        }
+        out[static_cast<int64_t>(prow) * mn + i] = word;
+    }
+    if (status != nullptr) {
+        const unsigned any = __ballot_sync(0xFFFFFFFFu, inexact);
+        if (any != 0u && (threadIdx.x & 31) == 0) atomicOr(status, DG_DEV_INEXACT_SCALE);
+    }
+}
+
+cudaError_t launch_transform_sf_k_grouped(const float *sf, int mn, const KGroupRows &t, int packed_rows,
+                                          void *out, int32_t *status, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((mn + 255) / 256, packed_rows, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dg_transform_sf_k_grouped_kernel, sf, mn, t, static_cast<uint32_t *>(out),
+                              status);
+}
+
 cudaError_t launch_transform_sf(const float *sf, int batch, int mn_rows, int sf_k, int gran_mn,
                                 int mn, int out_fmt, void *out, int32_t *status,
                                 cudaStream_t stream) {

@@ -253,6 +253,62 @@ int64_t dg_get_tma_aligned_size(int64_t mn, int elem_size);
  * for a K extent of k elements. */
 int64_t dg_packed_sf_words(int batch, int mn, int k);
 
+/*
+ * K-grouped GEMM for MoE weight gradients (PaperTrace "02 · DeepGEMM 技术解析"
+ * §5.2 and §3.3; "DeepSeek V4 源码剖析 第13章" §13.3 for the "tn" naming):
+ * M and N are fixed and the groups are concatenated along K.  For each group e
+ * with ks[e] rows of K starting at K_e = ks[0] + ... + ks[e-1]:
+ *
+ *   D[e][m][n] = C[e][m][n] + sum_{k in [K_e, K_e + ks[e])} A[k][m] sa(k/128, m) * B[k][n] sb(k/128, n)
+ *
+ *   a    E4M3 [K_total][lda], M contiguous (lda >= m, lda % 16 == 0).
+ *   b    E4M3 [K_total][ldb], N contiguous (ldb >= n, ldb % 16 == 0).
+ *   ks   HOST int array [num_groups]: rows of K per group, each a multiple of
+ *        128 (a group stored padded to 128 rows passes its padded size); 0 is
+ *        an empty group, whose D is C.  0 <= num_groups <= 255.
+ *   ks_dev  the same sizes in device memory (int32 [num_groups]); the kernel
+ *        reads its group table from there.  A size there that is negative or
+ *        not a multiple of 128 counts as 0 and sets DG_DEV_BAD_GROUP, as does a
+ *        total beyond the host sizes' (loads past K_total read zeros).
+ *   sfa, sfb  packed UE8M0 int32 [P][m] and [P][n] with
+ *        P = dg_k_grouped_packed_sf_rows(ks, num_groups): each group's scale
+ *        rows (one per 128 rows of K; per M or N index) packed on their own,
+ *        4 per word little-endian by K, the last word of a group zero-filled
+ *        past its rows, the groups' packed rows one after another.  Pages'
+ *        contract: mn % 4 == 0, no MN padding (else DG_ERR_LAYOUT).  Build them
+ *        from FP32 scales with dg_transform_sf_k_grouped.
+ *   c    FP32 [num_groups][m][n] contiguous, REQUIRED (the pages make C
+ *        mandatory for this layout); may equal d (in-place accumulation).
+ *   d    FP32 [num_groups][m][n] contiguous.
+ *   c, d, a, b, sfa, sfb 16-byte aligned; m, n multiples of 4.
+ *   m == 0, n == 0 or num_groups == 0 is a no-op; all ks 0 gives D = C.
+ *   Runs on 256x256 CTA pairs, one persistent launch over all groups.
+ */
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
+                                              int64_t ldb, const void *sfb, const float *c, float *d, int m,
+                                              int n, const int *ks, const int32_t *ks_dev, int num_groups,
+                                              int32_t *status_dev, void *stream);
+
+/*
+ * dg_transform_sf_k_grouped -- FP32 scales of the K-grouped layout into the
+ * packed form above (PaperTrace §3.3).
+ *   sf   FP32 [sum_e ks[e]/128][mn], mn contiguous; row r = the scales of the
+ *        r-th 128-row K block of the concatenated groups.
+ *   ks   HOST int array [num_groups], as for the GEMM.
+ *   out  int32 [dg_k_grouped_packed_sf_rows(ks, num_groups)][mn]; byte j of
+ *        packed row q of group e = (bits(sf[K_e/128 + 4q + j][i]) >> 23) & 0xff,
+ *        0 past the group's rows; a non-power-of-two scale is truncated and
+ *        sets DG_DEV_INEXACT_SCALE.
+ *   mn % 4 == 0 (else DG_ERR_LAYOUT); ks invalid -> DG_ERR_INVALID_ARG.
+ */
+dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                    int32_t *status_dev, void *stream);
+
+/* Packed scale rows of the K-grouped layout: sum_e ceil(ks[e] / 512), or -1
+ * if ks is invalid (see dg_k_grouped_fp8_gemm_tn_contiguous) or the count
+ * exceeds 65535. */
+int64_t dg_k_grouped_packed_sf_rows(const int *ks, int num_groups);
+
 /* Number of SMs the persistent kernels use (default: all SMs of the current
  * device).  n <= 0 restores the default. */
 void dg_set_num_sms(int n);

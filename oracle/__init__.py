@@ -319,6 +319,32 @@ def k_grouped_gemm_tn(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarr
     return d
 
 
+def k_grouped_gemm_tn_sampled(a, sa, b, sb, ks, c, es, ms, ns, nthreads: int = 0) -> np.ndarray:
+    """The elements (es[i], ms[i], ns[i]) of k_grouped_gemm_tn, one by one: the
+    group's fp64 sum (gemm_nt_sampled on the group's transposed slices), plus
+    C in fp64, rounded once to FP32.  (C is added after the products here, so
+    the fp64 rounding order differs from the full function's; the FP32 result
+    is the same except within an fp64 rounding of an FP32 tie.)"""
+    a, b = _u8(a), _u8(b)
+    es, ms, ns = (np.asarray(x, dtype=np.int64) for x in (es, ms, ns))
+    out = np.empty(len(es), dtype=np.float32)
+    k0 = 0
+    for e, k in enumerate(ks):
+        sel = np.nonzero(es == e)[0]
+        if len(sel):
+            cv = np.asarray(c[e], dtype=np.float64)[ms[sel], ns[sel]]
+            if k == 0:
+                out[sel] = cv.astype(np.float32)
+            else:
+                s0, s1 = k0 // 128, (k0 + k) // 128
+                _, pre = gemm_nt_sampled(np.ascontiguousarray(a[k0:k0 + k].T), np.ascontiguousarray(sa[s0:s1].T),
+                                         np.ascontiguousarray(b[k0:k0 + k].T), np.ascontiguousarray(sb[s0:s1].T),
+                                         ms[sel], ns[sel], want_pre=True, nthreads=nthreads)
+                out[sel] = (pre + cv).astype(np.float32)
+        k0 += k
+    return out
+
+
 def gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, c=None, want_pre=False, nthreads: int = 0):
     """The elements (rows[i], cols[i]) of gemm_nt, computed one by one."""
     a, b = _u8(a), _u8(b)

@@ -84,3 +84,25 @@ def test_host_validation_without_gpu(lib):
                                                2000, 64, 32, 64, 128, None, None) == 4
     assert lib.dg_m_grouped_fp8_gemm_nt_masked(P(16), P(16), 0, P(16), P(16), 0, P(16), P(16),
                                                2, 64, 32, 64, 128, None, None) == 4
+
+
+def test_k_grouped_host_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    ks = (ctypes.c_int * 4)(256, 640, 0, 128)
+    assert lib.dg_k_grouped_packed_sf_rows(ks, 4) == 4      # 1 + 2 + 0 + 1
+    bad = (ctypes.c_int * 2)(128, 130)
+    assert lib.dg_k_grouped_packed_sf_rows(bad, 2) == -1
+    assert lib.dg_k_grouped_packed_sf_rows(ks, 256) == -1     # more than 255 groups
+    assert lib.dg_k_grouped_packed_sf_rows(None, 0) == 0
+
+    def call(m=256, n=256, c=16, ks_arr=ks, groups=4, lda=256, ldb=256):
+        return lib.dg_k_grouped_fp8_gemm_tn_contiguous(P(16), lda, P(16), P(16), ldb, P(16), P(c), P(16), m, n,
+                                                       ks_arr, P(16), groups, None, None)
+    assert call(c=0) == 1            # C is required
+    assert call(ks_arr=bad, groups=2) == 1
+    assert call(m=258) == 3          # packed scales need mn % 4 == 0
+    assert call(n=0) == 0            # empty
+    assert call(groups=0) == 0
+    assert call(m=-4) == 1
+    assert lib.dg_transform_sf_k_grouped(P(16), 6, ks, 4, P(16), None, None) == 3
+    assert lib.dg_transform_sf_k_grouped(P(16), 8, bad, 2, P(16), None, None) == 1

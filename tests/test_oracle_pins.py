@@ -650,3 +650,16 @@ def test_k_grouped_pack_hand_worked(orc):
         [0x00000086, 0x00000085, 0x00000084, 0x00000083],   # group 3: row 7
     ], dtype=np.uint32)
     assert np.array_equal(got, want)
+
+
+def test_k_grouped_sampled_equals_full(orc):
+    case = inputs.k_grouped_case(3, 40, 24, seed=63, ks=[256, 0, 384])
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa, sb, c = case.sfa.double().numpy(), case.sfb.double().numpy(), case.c.numpy()
+    full = orc.k_grouped_gemm_tn(a, sa, b, sb, case.ks, c)
+    rng = np.random.default_rng(0)
+    es, ms, ns = rng.integers(0, 3, 300), rng.integers(0, 40, 300), rng.integers(0, 24, 300)
+    got = orc.k_grouped_gemm_tn_sampled(a, sa, b, sb, case.ks, c, es, ms, ns)
+    ref = full[es, ms, ns]
+    assert np.all(np.abs(got.astype(np.float64) - ref) <= 2.0 ** -23 * np.abs(ref))
