@@ -832,12 +832,35 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         // With C, each chunk's registers are refilled with the next tile's C as soon
         // as this tile's chunk is stored, so the C loads run a whole tile ahead.
         uint32_t cpk[(WITH_C && !F32) ? Cfg::kChunksPerWarp : 1][8];
+        // FP32 C: a ring of kCDepth chunks of this thread's row, loaded kCDepth chunks
+        // ahead of the one being stored (across tiles), so that the loads' latency
+        // overlaps the TMEM reads and stores of the chunks before
+        // (a divisor of the chunks per warp, so that chunk j of every tile has slot j % kCDepth)
+        constexpr int kCDepth = Cfg::kChunksPerWarp % 4 == 0 ? 4 : (Cfg::kChunksPerWarp % 2 == 0 ? 2 : 1);
+        static_assert(Cfg::kChunksPerWarp % kCDepth == 0, "C ring depth");
+        static_assert(!F32 || Cfg::kNumChunks % 2 == 0, "FP32 epilogue: both halves have every chunk");
+        float4 cring[(WITH_C && F32) ? kCDepth : 1][4];
+        auto load_c32 = [&](const PairTile &tl, int j, float4 (&dst)[4]) {
+            const int row = tl.d_row0 + row_off + static_cast<int>(lane);
+            const int col0 = tl.n0 + col_off + (2 * j + static_cast<int>(half)) * Cfg::kEpiChunk;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tl.valid_rows > 0 && row < p.rows && col0 + 4 * q < p.n)
+                    dst[q] = __ldg(reinterpret_cast<const float4 *>(p.c_f32 + static_cast<int64_t>(row) * p.ldc +
+                                                                    col0 + 4 * q));
+            }
+        };
         PairTile tile;
         if (pair_id < num_tiles) {
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
             if constexpr (WITH_C && !F32) {
 #pragma unroll
                 for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
+            }
+            if constexpr (WITH_C && F32) {
+#pragma unroll
+                for (int j = 0; j < kCDepth; ++j) load_c32(tile, j, cring[j]);
             }
         }
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
@@ -889,38 +912,41 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 // 8-column FP32 boxes through the staging buffers; the accumulator is
                 // released after its last chunk is read
                 const int row = tile.d_row0 + row_off + static_cast<int>(lane);
+                // chunks in runs of kCDepth, so that a chunk's ring slot is a constant
 #pragma unroll 1
-                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
-                    const int c = 2 * j + half;
-                    if (c >= Cfg::kNumChunks) break;
-                    const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
-                    float4 cv[4];
+                for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += kCDepth)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        cv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if constexpr (WITH_C) {
-                            if (tile.valid_rows > 0 && row < p.rows && col0 + 4 * q < p.n)
-                                cv[q] = __ldg(reinterpret_cast<const float4 *>(
-                                    p.c_f32 + static_cast<int64_t>(row) * p.ldc + col0 + 4 * q));
-                        }
-                    }
-                    uint32_t v[16];
+                for (int u = 0; u < kCDepth; ++u) {
+                    const int j = j0 + u;
+                    if (j >= Cfg::kChunksPerWarp) break;
+                    const int c = 2 * j + half;
+                    const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
+                    float f[16];
                     if (tile.nkb > 0) {
+                        uint32_t v[16];
                         tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v);
                         tmem_ld_wait();
                         reg_fence16(v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
                     } else {
                         // no K-blocks (an empty group): the accumulator was never written
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0u;
+                        for (int i = 0; i < 16; ++i) f[i] = 0.f;
                     }
-                    float f[16];
+                    if constexpr (WITH_C) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f[4 * q + 0] = __uint_as_float(v[4 * q + 0]) + cv[q].x;
-                        f[4 * q + 1] = __uint_as_float(v[4 * q + 1]) + cv[q].y;
-                        f[4 * q + 2] = __uint_as_float(v[4 * q + 2]) + cv[q].z;
-                        f[4 * q + 3] = __uint_as_float(v[4 * q + 3]) + cv[q].w;
+                        for (int q = 0; q < 4; ++q) {
+                            f[4 * q + 0] += cring[u][q].x;
+                            f[4 * q + 1] += cring[u][q].y;
+                            f[4 * q + 2] += cring[u][q].z;
+                            f[4 * q + 3] += cring[u][q].w;
+                        }
+                        // refill the slot: chunk j + kCDepth of this tile, or of the next
+                        if (j + kCDepth < Cfg::kChunksPerWarp)
+                            load_c32(tile, j + kCDepth, cring[u]);
+                        else if (has_next)
+                            load_c32(next_tile, j + kCDepth - Cfg::kChunksPerWarp, cring[u]);
                     }
                     if (tile.valid_rows == 0 || col0 >= p.n) continue;
                     if (tile.valid_rows < MP / 2) {
