@@ -334,8 +334,8 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
         else
             ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
                             a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (lay & 2)
-            ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, o.b_rows, k, o.ldb, b1_rows, k_rows,
+        if (lay & 2)   // a whole 128-byte atom per CTA, of which the MMA reads bn/2 columns
+            ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, o.b_rows, k, o.ldb, 128, k_rows,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         else
             ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
@@ -740,7 +740,8 @@ static dg_status gemm_mn_layout(int lay, const void *a, int64_t lda, const void 
                  sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_k),
                  d,   ldd, static_cast<uint64_t>(m)};
     const int64_t units = cdiv64(m, 2 * kBlockM);
-    return launch_pair(p, o, 256, 256, units, sms, static_cast<cudaStream_t>(stream));
+    // with C, 224 columns: two TMEM accumulators, so a tile's epilogue overlaps the next one's MMAs
+    return launch_pair(p, o, 256, c != nullptr ? 224 : 256, units, sms, static_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_fp8_gemm_nn(const void *a, int64_t lda, const void *sfa, int sfa_fmt, const void *b,
@@ -975,7 +976,7 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const 
                  sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(prows),
                  d,   n,   static_cast<uint64_t>(rows)};
     const int64_t units = static_cast<int64_t>(num_groups) * p.num_m_blocks;
-    return launch_pair(p, o, 256, 256, units, sms, static_cast<cudaStream_t>(stream));
+    return launch_pair(p, o, 256, 224, units, sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

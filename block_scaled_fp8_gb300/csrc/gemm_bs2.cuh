@@ -38,7 +38,10 @@ namespace dg {
 // columns) or 128 (each CTA 64 rows; TMEM lanes 0-63 hold D columns [0, BN/2)
 // and lanes 64-127 columns [BN/2, BN) of the same 64 rows, so an accumulator is
 // BN/2 columns wide).
-template <int BN, int MP = 256>
+// B_ATOM: B is MN-major ([K][N]); each CTA's B region per K-block is one whole
+// 128-byte swizzle atom wide (128 N-bytes x 128 K-rows) however many of its
+// columns (BN/2 <= 128) the MMA reads.
+template <int BN, int MP = 256, bool B_ATOM = false>
 struct Bs2Config {
     // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
     // with MP=128 each half of N is whole 16-column epilogue chunks
@@ -53,6 +56,7 @@ struct Bs2Config {
     static_assert(kBN2 == 0 || (kBN2 % 16 == 0 && kBN2 <= 256), "second MMA columns");
     static constexpr int kB1Rows = kBN1 / 2;
     static constexpr int kB2Rows = kBN2 / 2;
+    static_assert(!B_ATOM || (MP == 256 && kBN2 == 0 && kB1Rows % 16 == 0), "MN-major B: one atom per CTA");
     static constexpr int kThreads = 384;
     static constexpr int kEpiWarps = 8;
     static constexpr int kSfWarp = 10;                           // first scale warp
@@ -77,7 +81,7 @@ struct Bs2Config {
     static constexpr int kSfTmemSlots =
         (2 * kAccCols + 4 * kSfCols <= 512 || 2 * kAccCols + 2 * kSfCols > 512) ? 4 : 2;
     static constexpr int kABytes = kARows * kBlockK;            // this CTA's rows of A
-    static constexpr int kB1Bytes = kB1Rows * kBlockK;
+    static constexpr int kB1Bytes = (B_ATOM ? 128 : kB1Rows) * kBlockK;
     static constexpr int kB2Bytes = kB2Rows * kBlockK;
     static constexpr int kBBytes = kB1Bytes + kB2Bytes;         // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -383,18 +387,19 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
 // LAY: operand layouts, bit 0 = A MN-major (stored [K][M]), bit 1 = B MN-major
 // (stored [K][N]); 0 is the NT layout (both K-major).  An MN-major operand's
 // stage is a TMA box of 128 MN-bytes x 128 K-rows with 128-byte swizzle: one
-// swizzle atom along MN (so MP=256 and BN=256 only), 8-row groups 1024 bytes
-// apart, and a 32-K step of the MMA 4096 bytes on; the instruction descriptor's
-// transpose bits (15: A, 16: B) select the layout.
+// swizzle atom along MN (MP=256; an MN-major B half of BN/2 <= 128 columns,
+// the rest of the atom unread), 8-row groups 1024 bytes apart, and a 32-K step
+// of the MMA 4096 bytes on; the instruction descriptor's transpose bits (15:
+// A, 16: B) select the layout.
 template <int BN, bool WITH_C, int MP, bool F32 = false, int LAY = 0>
 __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims__(2, 1, 1)
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_b2,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
-    using Cfg = Bs2Config<BN, MP>;
     constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0;
-    static_assert(LAY == 0 || (MP == 256 && BN == 256), "MN-major operands: 256x256 pair tiles");
+    using Cfg = Bs2Config<BN, MP, B_MN>;
+    static_assert(LAY == 0 || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
     constexpr int G = Cfg::kGroupKb;
@@ -832,12 +837,12 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         // With C, each chunk's registers are refilled with the next tile's C as soon
         // as this tile's chunk is stored, so the C loads run a whole tile ahead.
         uint32_t cpk[(WITH_C && !F32) ? Cfg::kChunksPerWarp : 1][8];
-        // FP32 C: a ring of kCDepth chunks of this thread's row, loaded kCDepth chunks
-        // ahead of the one being stored (across tiles), so that the loads' latency
-        // overlaps the TMEM reads and stores of the chunks before
-        // (a divisor of the chunks per warp, so that chunk j of every tile has slot j % kCDepth)
-        constexpr int kCDepth = Cfg::kChunksPerWarp % 4 == 0 ? 4 : (Cfg::kChunksPerWarp % 2 == 0 ? 2 : 1);
-        static_assert(Cfg::kChunksPerWarp % kCDepth == 0, "C ring depth");
+        // FP32 C: a ring of kCDepth chunks of this thread's row; chunk j of every tile
+        // lives in slot j % kCDepth.  Once chunk j is added, its slot is refilled with
+        // chunk j + kCDepth of the tile, or, past the tile's last chunk, with chunk
+        // j % kCDepth of the next tile, so the loads run up to kCDepth chunks ahead
+        // and overlap the TMEM reads and stores of the chunks before.
+        constexpr int kCDepth = Cfg::kChunksPerWarp < 4 ? Cfg::kChunksPerWarp : 4;
         static_assert(!F32 || Cfg::kNumChunks % 2 == 0, "FP32 epilogue: both halves have every chunk");
         float4 cring[(WITH_C && F32) ? kCDepth : 1][4];
         auto load_c32 = [&](const PairTile &tl, int j, float4 (&dst)[4]) {
@@ -942,11 +947,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             f[4 * q + 2] += cring[u][q].z;
                             f[4 * q + 3] += cring[u][q].w;
                         }
-                        // refill the slot: chunk j + kCDepth of this tile, or of the next
+                        // refill the slot: chunk j + kCDepth of this tile, or chunk u of the next
                         if (j + kCDepth < Cfg::kChunksPerWarp)
                             load_c32(tile, j + kCDepth, cring[u]);
                         else if (has_next)
-                            load_c32(next_tile, j + kCDepth - Cfg::kChunksPerWarp, cring[u]);
+                            load_c32(next_tile, u, cring[u]);
                     }
                     if (tile.valid_rows == 0 || col0 >= p.n) continue;
                     if (tile.valid_rows < MP / 2) {
@@ -1079,7 +1084,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
-    using Cfg = Bs2Config<BN, MP>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
     cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
@@ -1101,7 +1106,7 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
 
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 int max_active_pairs_impl() {
-    using Cfg = Bs2Config<BN, MP>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
     if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
@@ -1121,9 +1126,9 @@ int max_active_pairs_impl() {
     return n;
 }
 
-template <int BN, int MP>
+template <int BN, int MP, int LAY = 0>
 void fill_bs2_info(KernelInfo *info) {
-    using Cfg = Bs2Config<BN, MP>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
     info->block_n = BN;
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;

@@ -14,11 +14,12 @@
 #define DG_BS2_LIST_F32(X)                                                                         \
     X(128, false, 256, true, 0) X(128, true, 256, true, 0) X(224, false, 256, true, 0) X(224, true, 256, true, 0)
 
-// NN (B MN-major), TN (both), TT (A MN-major); the last one is the K-grouped
-// weight-gradient GEMM (TN, FP32 C and D)
+// NN (B MN-major), TN (both), TT (A MN-major): 256 columns without C, 224 (two
+// accumulators) with C; the last one is the K-grouped weight-gradient GEMM (TN,
+// FP32 C and D)
 #define DG_BS2_LIST_MN(X)                                                                          \
-    X(256, false, 256, false, 2) X(256, true, 256, false, 2) X(256, false, 256, false, 3)          \
-    X(256, true, 256, false, 3) X(256, false, 256, false, 1) X(256, true, 256, false, 1)           \
-    X(256, true, 256, true, 3)
+    X(256, false, 256, false, 2) X(224, true, 256, false, 2) X(256, false, 256, false, 3)          \
+    X(224, true, 256, false, 3) X(256, false, 256, false, 1) X(224, true, 256, false, 1)           \
+    X(224, true, 256, true, 3)
 
 #define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X) DG_BS2_LIST_MN(X)

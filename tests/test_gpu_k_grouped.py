@@ -60,7 +60,7 @@ def test_k_grouped_matches_oracle(orc, E, M, N, ks, pad):
     case = inputs.k_grouped_case(E, M, N, seed=E + M + N, ks=ks)
     d, sfa, sfb, status, cfg = _run(case, pad)
     assert status == 0
-    assert cfg["kind"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 256, cfg
+    assert cfg["kind"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 224, cfg
     assert np.array_equal(sfa.cpu().numpy(), orc.k_grouped_pack_sf(case.sfa.numpy(), ks))
     assert np.array_equal(sfb.cpu().numpy(), orc.k_grouped_pack_sf(case.sfb.numpy(), ks))
     ref = orc.k_grouped_gemm_tn(u8(case.a), case.sfa.double().numpy(), u8(case.b), case.sfb.double().numpy(),
