@@ -614,6 +614,46 @@ def run_reference(args, rank, world):
     }
 
 
+def run_case_k_grouped(args):
+    """One K-grouped weight-gradient GEMM, `warmup` + `steps` launches (for ncu
+    captures); prints the median per-launch device time."""
+    import torch
+
+    from block_scaled_fp8_gb300 import binding, build, inputs
+    build.build()
+    e, m, n, k = (int(x) for x in args.case_k_grouped.split(","))
+    dev = torch.device("cuda", 0)
+    kc = inputs.k_grouped_case(e, m, n, seed=0, ks=[k] * e, device=dev)
+    sfa = binding.dg_transform_sf_k_grouped(kc.sfa, kc.ks)
+    sfb = binding.dg_transform_sf_k_grouped(kc.sfb, kc.ks)
+    ks_dev = torch.tensor(kc.ks, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        binding.dg_k_grouped_fp8_gemm_tn_contiguous(kc.a, sfa, kc.b, sfb, kc.c, kc.ks, ks_dev=ks_dev, c=kc.c,
+                                                    status=status)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert int(status.item()) == 0, int(status.item())
+    us = statistics.median(times) * 1e3
+    kt = e * k
+    by = kt * (m + n) + 2 * 4 * e * m * n
+    print(json.dumps({"case_k_grouped": [e, m, n, k], "median_us": round(us, 2),
+                      "tflops": round(flops(m, n, kt) / (us * 1e-6) / 1e12, 1),
+                      "gbs": round(by / (us * 1e-6) / 1e9, 1), "config": binding.last_config()}))
+
+
 def run_case(args):
     """One dense GEMM shape, `warmup` + `steps` launches (for ncu captures and
     per-shape timing); prints per-launch device time."""
@@ -713,13 +753,15 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None, help="M,N,K: time one dense GEMM shape only")
     ap.add_argument("--with-c", action="store_true")
+    ap.add_argument("--case-k-grouped", default=None,
+                    help="E,M,N,K: time one K-grouped GEMM (E groups of K rows each, C = D in place)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.warmup < 3 and not args.case:
+    if args.warmup < 3 and not (args.case or args.case_k_grouped):
         ap.error("--warmup must be >= 3")
 
     rank = int(os.environ.get("RANK", "0"))
@@ -730,6 +772,9 @@ def main():
 
     if args.case:
         run_case(args)
+        return
+    if args.case_k_grouped:
+        run_case_k_grouped(args)
         return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
