@@ -35,14 +35,15 @@ def generator(seed: int, device="cpu") -> torch.Generator:
     return g
 
 
-def pow2_scale(amax: torch.Tensor) -> torch.Tensor:
-    """Smallest power of two s (FP32, normal) with amax / s <= 448; 1 where amax == 0."""
-    v = amax.double() / E4M3_MAX
+def pow2_scale(amax: torch.Tensor, qmax: float = E4M3_MAX) -> torch.Tensor:
+    """Smallest power of two s (FP32, normal) with amax / s <= qmax (448 for
+    E4M3, 6 for E2M1); 1 where amax == 0."""
+    v = amax.double() / qmax
     mant, exp = torch.frexp(v)                      # v = mant * 2^exp, mant in [0.5, 1)
     e = torch.where(mant == 0.5, exp - 1, exp)      # ceil(log2 v)
     e = torch.clamp(e, min=-126, max=127)
     s = torch.ldexp(torch.ones_like(v), e)
-    s = torch.where(amax.double() > E4M3_MAX * s, s * 2, s)   # guard, never expected
+    s = torch.where(amax.double() > qmax * s, s * 2, s)   # guard, never expected
     s = torch.where(amax == 0, torch.ones_like(s), s)
     return s.float()
 
@@ -265,4 +266,57 @@ def k_grouped_case(num_groups: int, M: int, N: int, seed: int = 0, ks: list[int]
     c = torch.randn(num_groups, M, N, generator=g, dtype=torch.float32, device=device)
     return KGroupedCase(a, sfa, b, sfb, c, list(ks),
                         {"E": num_groups, "M": M, "N": N, "K_total": k_total, "seed": seed})
+
+
+# E2M1 magnitudes by code (low 3 bits) and the midpoints between neighbours
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+_E2M1_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def quantize_e2m1_1x32(w: torch.Tensor):
+    """w fp32 [N, K] (K % 32 == 0) -> (packed uint8 [N, K/2], scales fp32 [N, K/32]):
+    one power-of-two scale per 32 consecutive K of a row (amax / s <= 6), each
+    value rounded to the nearest E2M1 magnitude (a tie goes to the smaller),
+    two codes per byte with the even-k element in the low nibble."""
+    N, K = w.shape
+    assert K % 32 == 0
+    blocks = w.view(N, K // 32, 32)
+    s = pow2_scale(blocks.abs().amax(-1), 6.0)
+    x = blocks / s[..., None]
+    mid = torch.tensor(_E2M1_MIDPOINTS, dtype=x.dtype, device=x.device)
+    code = torch.bucketize(x.abs().contiguous(), mid).to(torch.uint8)
+    code |= (x < 0).to(torch.uint8) << 3
+    code = code.view(N, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed, s
+
+
+@dataclass
+class Fp4Case:
+    """FP8 x FP4 GEMM inputs ("DeepSeek V4 源码剖析 第13章" §13.1, §13.5): FP8
+    activations with 1x128 scales, FP4 (E2M1) weights with one scale per 32 K."""
+    a: torch.Tensor          # float8_e4m3fn [M, K]
+    sfa: torch.Tensor        # fp32 [M, K/128]
+    b: torch.Tensor          # uint8 [N, K/2], two E2M1 codes per byte (even k low)
+    sfb: torch.Tensor        # fp32 [N, K/32]
+    c: torch.Tensor | None   # bf16 [M, N] or None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def shape(self):
+        return self.a.shape[0], self.b.shape[0], self.a.shape[1]
+
+
+def fp4_case(M: int, N: int, K: int, seed: int = 0, with_c: bool = False, device="cpu") -> Fp4Case:
+    """X, W from N(0,1); X quantised per 1x128 to E4M3, W per 1x32 to E2M1."""
+    g = generator(seed, device)
+    x = torch.randn(M, K, generator=g, dtype=torch.float32, device=device)
+    w = torch.randn(N, K, generator=g, dtype=torch.float32, device=device)
+    a, sfa = quantize_1x128(x)
+    del x
+    b, sfb = quantize_e2m1_1x32(w)
+    del w
+    c = (torch.randn(M, N, generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+         if with_c else None)
+    return Fp4Case(a, sfa, b, sfb, c, {"M": M, "N": N, "K": K, "seed": seed})
 

@@ -81,6 +81,12 @@ def _get():
                                                      i64, i32]
             lib.orc_m_grouped_masked.restype = None
             lib.orc_m_grouped_masked.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, i32]
+            lib.orc_e2m1_decode.restype = ctypes.c_double
+            lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_gemm_fp8_fp4_nt.restype = None
+            lib.orc_gemm_fp8_fp4_nt.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, P, i32]
+            lib.orc_gemm_fp8_fp4_nt_sampled.restype = None
+            lib.orc_gemm_fp8_fp4_nt_sampled.argtypes = [i32, P, i64, P, P, i64, P, i64, P, P, P, i32]
             lib.orc_max_threads.restype = i32
             _lib = lib
     return _lib
@@ -109,6 +115,11 @@ def max_threads() -> int:
 def e4m3_decode(code: int) -> float:
     """OCP FP8 E4M3fn code -> value ("FP8 e4m3" of the pages; torch.float8_e4m3fn)."""
     return float(_get().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e2m1_decode(code: int) -> float:
+    """OCP MX FP4 E2M1 code (low 4 bits) -> value ("DeepSeek V4 源码剖析 第13章" §13.5)."""
+    return float(_get().orc_e2m1_decode(code))
 
 
 def e4m3_table() -> np.ndarray:
@@ -235,6 +246,44 @@ def gemm(layout: str, a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.
     a_mk = np.ascontiguousarray(a.T) if layout[0] == "t" else a
     b_nk = np.ascontiguousarray(b.T) if layout[1] == "n" else b
     return gemm_nt(a_mk, sa, b_nk, sb_rows, c=c, want_pre=want_pre, nthreads=nthreads)
+
+
+def gemm_fp8_fp4_nt(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarray,
+                    c: np.ndarray | None = None, want_pre: bool = False, nthreads: int = 0):
+    """FP8 x FP4 GEMM ("DeepSeek V4 源码剖析 第13章" §13.1 reason 2, §13.5):
+    D = C + A @ B^T with A E4M3 [M, K] and 1x128 scales sa [M, ceil(K/128)],
+    B E2M1 packed two per byte [N, ceil(K/2)] (low nibble = even k) with one
+    scale per 32 K of each row, sb [N, ceil(K/32)]; fp64 sum, one RNE to bf16.
+    Returns uint16 bf16 bits [M, N] (and the fp64 pre-rounding values)."""
+    a, b = _u8(a), _u8(b)
+    M, K = a.shape
+    N = b.shape[0]
+    assert b.shape[1] == (K + 1) // 2
+    sa = np.ascontiguousarray(sa, dtype=np.float64)
+    sb = np.ascontiguousarray(sb, dtype=np.float64)
+    assert sa.shape == (M, (K + 127) // 128) and sb.shape == (N, (K + 31) // 32)
+    if c is not None:
+        c = np.ascontiguousarray(c).view(np.uint16)
+        assert c.shape == (M, N)
+    d = np.empty((M, N), dtype=np.uint16)
+    pre = np.empty((M, N), dtype=np.float64) if want_pre else None
+    _get().orc_gemm_fp8_fp4_nt(M, N, K, _ptr(a), K, _ptr(sa), _ptr(b), b.shape[1], _ptr(sb), _ptr(c), N,
+                               _ptr(d), N, _ptr(pre), nthreads)
+    return (d, pre) if want_pre else d
+
+
+def gemm_fp8_fp4_nt_sampled(a, sa, b, sb, rows, cols, nthreads: int = 0) -> np.ndarray:
+    """The elements (rows[i], cols[i]) of gemm_fp8_fp4_nt (C = 0), one by one."""
+    a, b = _u8(a), _u8(b)
+    K = a.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    sa = np.ascontiguousarray(sa, dtype=np.float64)
+    sb = np.ascontiguousarray(sb, dtype=np.float64)
+    out = np.empty(rows.shape[0], dtype=np.uint16)
+    _get().orc_gemm_fp8_fp4_nt_sampled(K, _ptr(a), K, _ptr(sa), _ptr(b), b.shape[1], _ptr(sb), rows.shape[0],
+                                       _ptr(rows), _ptr(cols), _ptr(out), nthreads)
+    return out
 
 
 def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,

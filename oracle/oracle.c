@@ -64,6 +64,18 @@ double orc_e4m3_decode(uint8_t code) {
     return sign ? -v : v;
 }
 
+/* OCP MX FP4 E2M1 (the weights' type of the FP8 x FP4 GEMM [P2 13.5]): 1 sign
+ * bit, 2 exponent bits (bias 1), 1 mantissa bit; exponent field 0 encodes the
+ * subnormal m/2.  No infinity and no NaN: the magnitudes are 0, 0.5, 1, 1.5, 2,
+ * 3, 4 and 6.  Only the low 4 bits of `code` are read. */
+double orc_e2m1_decode(uint8_t code) {
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
 /* UE8M0: 8-bit unsigned exponent, no mantissa, no sign; 2^(e-127); 0xff is
  * NaN [P1 3.1]. */
 double orc_ue8m0_decode(uint8_t e) {
@@ -279,6 +291,64 @@ void orc_gemm_nt_sampled(int K, const uint8_t *A, int64_t lda, const double *sa,
         double c = C ? orc_bf16_decode(C[m * ldc + n]) : 0.0;
         double v = dot_element(K, A + m * lda, sa + m * sf_k, B + n * ldb, sb + n * sf_k, c);
         if (pre) pre[i] = v;
+        out[i] = orc_bf16_from_double(v);
+    }
+}
+
+/*
+ * FP8 x FP4 GEMM [P2 13.1 (reason 2), 13.5]: FP8 activations times FP4 weights
+ * whose scales run along K with one per 32 elements.
+ *   A  E4M3 [M][lda], sa [M][ceil(K/128)] (the activations' 1x128 scales);
+ *   B  E2M1 packed two per byte, row n at B + n*ldb bytes: element k of the row
+ *      is byte k/2, low nibble for even k, high nibble for odd k;
+ *   sb [N][ceil(K/32)]: one scale per row and 32 consecutive K.
+ * D[m][n] = bf16_rne(C[m][n] + sum_k dec(A[m,k]) sa[m][k/128] * dec(B[n,k]) sb[n][k/32]),
+ * the sum in fp64 in increasing k (C decoded exactly, 0 if NULL).
+ */
+static double dot_element_fp4(int K, const uint8_t *arow, const double *sarow, const uint8_t *brow,
+                              const double *sbrow, double c) {
+    double s = 0.0;
+    for (int k = 0; k < K; k++) {
+        uint8_t byte = brow[k / 2];
+        uint8_t code = (k % 2 == 0) ? (uint8_t)(byte & 0xf) : (uint8_t)(byte >> 4);
+        double a = orc_e4m3_decode(arow[k]) * sarow[k / 128];
+        double b = orc_e2m1_decode(code) * sbrow[k / 32];
+        s += a * b;
+    }
+    return c + s;
+}
+
+void orc_gemm_fp8_fp4_nt(int M, int N, int K, const uint8_t *A, int64_t lda, const double *sa,
+                         const uint8_t *B, int64_t ldb, const double *sb, const uint16_t *C, int64_t ldc,
+                         uint16_t *D, int64_t ldd, double *pre, int nthreads) {
+    int sfa_k = (K + 127) / 128, sfb_k = (K + 31) / 32;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int m = 0; m < M; m++) {
+        for (int n = 0; n < N; n++) {
+            double c = C ? orc_bf16_decode(C[(int64_t)m * ldc + n]) : 0.0;
+            double v = dot_element_fp4(K, A + (int64_t)m * lda, sa + (int64_t)m * sfa_k, B + (int64_t)n * ldb,
+                                       sb + (int64_t)n * sfb_k, c);
+            if (pre) pre[(int64_t)m * N + n] = v;
+            D[(int64_t)m * ldd + n] = orc_bf16_from_double(v);
+        }
+    }
+}
+
+/* The same elements one by one for a list of (row, col) pairs. */
+void orc_gemm_fp8_fp4_nt_sampled(int K, const uint8_t *A, int64_t lda, const double *sa, const uint8_t *B,
+                                 int64_t ldb, const double *sb, int64_t nsamples, const int64_t *rows,
+                                 const int64_t *cols, uint16_t *out, int nthreads) {
+    int sfa_k = (K + 127) / 128, sfb_k = (K + 31) / 32;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
+    for (int64_t i = 0; i < nsamples; i++) {
+        int64_t m = rows[i], n = cols[i];
+        double v = dot_element_fp4(K, A + m * lda, sa + m * sfa_k, B + n * ldb, sb + n * sfb_k, 0.0);
         out[i] = orc_bf16_from_double(v);
     }
 }

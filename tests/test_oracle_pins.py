@@ -663,3 +663,68 @@ def test_k_grouped_sampled_equals_full(orc):
     got = orc.k_grouped_gemm_tn_sampled(a, sa, b, sb, case.ks, c, es, ms, ns)
     ref = full[es, ms, ns]
     assert np.all(np.abs(got.astype(np.float64) - ref) <= 2.0 ** -23 * np.abs(ref))
+
+
+# ---------------------------------------------------------------- FP8 x FP4
+
+# OCP Microscaling FP4 E2M1 by code: sign bit 3, then the eight magnitudes
+E2M1_TEXTBOOK = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_all_codes_textbook(orc):
+    for code, want in enumerate(E2M1_TEXTBOOK):
+        got = orc.e2m1_decode(code)
+        assert got == want and np.signbit(got) == np.signbit(want), code
+    assert orc.e2m1_decode(0xF7) == 6.0      # only the low nibble is read
+
+
+def _nibbles(packed_row, K):
+    """Codes of one packed row, read by index: element k = byte k // 2, low nibble for even k."""
+    return [(int(packed_row[k // 2]) >> (4 * (k % 2))) & 0xF for k in range(K)]
+
+
+def test_fp8_fp4_bruteforce_from_packed_storage(orc):
+    """"DeepSeek V4 源码剖析 第13章" §13.1 reason 2: weight scales run along K,
+    one per 32 elements.  Rational sums read straight from the packed bytes
+    with distinct scales per 32-K block; power-of-two scales keep every term
+    exact, so the oracle's fp64 values must equal them."""
+    M, N, K = 3, 5, 256
+    case = inputs.fp4_case(M, N, K, seed=81, with_c=True)
+    rng = np.random.default_rng(81)
+    sb = np.ldexp(1.0, rng.integers(-6, 4, (N, K // 32)))
+    a = case.a.view(torch.uint8).numpy()
+    A = _decode_codes_torch(case.a.view(torch.uint8))
+    sa = case.sfa.double().numpy()
+    b = case.b.numpy()
+    c = case.c.view(torch.int16).numpy().view(np.uint16)
+    d, pre = orc.gemm_fp8_fp4_nt(a, sa, b, sb, c=c, want_pre=True)
+    for n in range(N):
+        codes = _nibbles(b[n], K)
+        for m in range(M):
+            s = Fraction(_bf16_value(int(c[m, n])))
+            for k in range(K):
+                if A[m, k] and codes[k] & 7:
+                    s += (Fraction(float(A[m, k])) * Fraction(float(sa[m, k // 128])) *
+                          Fraction(E2M1_TEXTBOOK[codes[k]]) * Fraction(float(sb[n, k // 32])))
+            assert Fraction(pre[m, n]) == s, (m, n)
+            assert d[m, n] == _bf16_nearest_bruteforce(s)
+
+
+def test_fp8_fp4_reduces_to_fp8_nt(orc):
+    """With each row's four 32-K scales of a 128-K block equal, the FP8 x FP4
+    GEMM is the NT GEMM of the same values: the E2M1 weights re-encoded as
+    E4M3 (exact) with those scales as per-row 128-K scales."""
+    M, N, K = 20, 24, 384
+    case = inputs.fp4_case(M, N, K, seed=82)
+    rng = np.random.default_rng(82)
+    s128 = np.ldexp(1.0, rng.integers(-5, 5, (N, K // 128)))
+    sb = np.repeat(s128, 4, axis=1)
+    b = case.b.numpy()
+    vals = np.array([[E2M1_TEXTBOOK[cd] for cd in _nibbles(b[n], K)] for n in range(N)])
+    b8 = torch.from_numpy(vals).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(torch.from_numpy(b8).view(torch.float8_e4m3fn).double().numpy(), vals)
+    a = case.a.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    got = orc.gemm_fp8_fp4_nt(a, sa, b, sb)
+    want = orc.gemm_nt(a, sa, b8, s128)
+    assert np.array_equal(got, want)
