@@ -208,6 +208,19 @@ def measure_other_workloads(dev, flush, reps, stream):
                flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n, {"layout": name.lower()})
     del c_, sfa, sfb, sfa32, sfb32, d, c32, d32, a_t, b_t
 
+    # FP8 activations x FP4 (E2M1) weights with one scale per 32 K: the largest V3-like
+    # shape and its M=128 decode form (where the weight bytes bound the time)
+    for (m, n, k) in ((4096, 7168, 16384), (128, 7168, 16384)):
+        fc = inputs.fp4_case(m, n, k, seed=5, device=dev)
+        sfa = binding.transform_sf(fc.sfa, 1, m)
+        sfb = binding.transform_sf(fc.sfb.contiguous(), 1, n)
+        d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        record(f"dense FP8 x FP4 {m}x{n}x{k}",
+               lambda: binding.dg_fp8_fp4_gemm_nt(fc.a, sfa, fc.b, sfb, d, status=status),
+               flops(m, n, k), m * k + n * k // 2 + 4 * (m * k // 128 + n * k // 32) // 4 + 2 * m * n,
+               {"weights": "e2m1, 1x32 UE8M0 scales"})
+        del fc, sfa, sfb, d
+
     # contiguous grouped: 8 experts, M_e ~ U[128, 4096] padded to 128
     for (n, k) in ((4096, 7168), (7168, 2048)):
         cc = inputs.contiguous_case(8, n, k, seed=3, device=dev)

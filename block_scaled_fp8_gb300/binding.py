@@ -30,6 +30,7 @@ DG_DEBUG_WIDE_PAIR = 8
 # Every symbol include/dg.h declares.
 EXPORTS = (
     "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn", "dg_fp8_gemm_tt",
+    "dg_fp8_fp4_gemm_nt",
     "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped", "dg_k_grouped_packed_sf_rows",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
@@ -71,6 +72,8 @@ def lib():
                 L.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes
             L.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [P, P, i32, P, P, i32, P, P, i32, i32,
                                                           i32, i32, i32, P, P]
+            L.dg_fp8_fp4_gemm_nt.argtypes = [P, i64, P, P, i64, P, P, i64, P, i64, i32, i32, i32, P, P]
+            L.dg_fp8_fp4_gemm_nt.restype = i32
             L.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [P, i64, P, P, i64, P, P, P, i32, i32, P, P, i32,
                                                               P, P]
             L.dg_transform_sf_k_grouped.argtypes = [P, i32, P, i32, P, P, P]
@@ -249,6 +252,21 @@ def dg_fp8_gemm_tn(a, sfa, b, sfb, d, c=None, status=None, stream=None):
 def dg_fp8_gemm_tt(a, sfa, b, sfb, d, c=None, status=None, stream=None):
     """D = C + A^T @ B^T: a [K, M] (M contiguous), b [N, K] (K contiguous)."""
     return _gemm_layout("dg_fp8_gemm_tt", True, False, a, sfa, b, sfb, d, c, status, stream)
+
+
+def dg_fp8_fp4_gemm_nt(a, sfa, b, sfb, d, c=None, status=None, stream=None):
+    """D = C + A @ B^T with FP8 A [M, K] (packed 1x128 scales) and FP4 B: b uint8
+    [N, K/2], two E2M1 codes per byte (even k in the low nibble), row stride =
+    stride(0) bytes; sfb packed int32 [K/128, align4(N)] (4 x 32 K per word)."""
+    M, K = a.shape
+    N = b.shape[0]
+    assert b.dtype == torch.uint8 and b.shape[1] * 2 == K and b.stride(1) == 1
+    assert a.stride(1) == 1 and d.stride(1) == 1 and d.dtype == torch.bfloat16
+    assert c is None or (c.dtype == torch.bfloat16 and c.stride(1) == 1)
+    _check("dg_fp8_fp4_gemm_nt", lib().dg_fp8_fp4_gemm_nt(
+        _p(a), a.stride(0), _p(sfa), _p(b), b.stride(0), _p(sfb), _p(c), 0 if c is None else c.stride(0), _p(d),
+        d.stride(0), M, N, K, _p(status), _stream(stream)))
+    return d
 
 
 def _ks_host(ks):

@@ -212,12 +212,12 @@ bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
 
 int cached_max_pairs(int bn, bool with_c, int mp, bool f32 = false, int lay = 0) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][2][4][513];
+    static int cache[kMaxDevices][2][2][2][8][513];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn <= 0 || bn > 512) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][lay & 3][bn];
-    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32, lay & 3);
+    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][lay & 7][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32, lay & 7);
     return v;
 }
 
@@ -334,7 +334,10 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
         else
             ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
                             a_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        if (lay & 2)   // a whole 128-byte atom per CTA, of which the MMA reads bn/2 columns
+        if (lay & 4)   // FP4 B, K-contiguous, two codes per byte: boxes of 128 codes x rows
+            ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 1, o.b, k, o.b_rows, o.ldb, kBlockK,
+                            b1_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        else if (lay & 2)   // a whole 128-byte atom per CTA, of which the MMA reads bn/2 columns
             ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, o.b_rows, k, o.ldb, 128, k_rows,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         else
@@ -763,6 +766,69 @@ dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fm
                          void *d, int64_t ldd, int m, int n, int k, int32_t *status_dev, void *stream) {
     return gemm_mn_layout(1, a, lda, sfa, sfa_fmt, b, ldb, sfb, sfb_fmt, c, ldc, d, ldd, m, n, k, status_dev,
                           stream);
+}
+
+// FP8 x FP4: 256-row CTA pairs; the column count that fills the SMs best, of
+// 128 and 256 without C (one accumulator at 256) and 128 and 192 with C.
+static int choose_fp4_block_n(int64_t m_units, int n, int num_sms, bool with_c) {
+    const int cands[2] = {128, with_c ? 192 : 256};
+    const int pairs = num_sms / 2;
+    double best = -1.0;
+    int best_bn = 128;
+    for (int bn : cands) {
+        const int64_t tiles = m_units * cdiv64(n, bn);
+        const int64_t waves = cdiv64(tiles, pairs);
+        const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * pairs);
+        const double pad_eff = static_cast<double>(n) / static_cast<double>(cdiv64(n, bn) * bn);
+        const double tile_eff = static_cast<double>(bn) / (bn + 64.0);
+        const double score = wave_eff * pad_eff * tile_eff;
+        if (score > best + 1e-9) {
+            best = score;
+            best_bn = bn;
+        }
+    }
+    return best_bn;
+}
+
+dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const void *b, int64_t ldb,
+                             const void *sfb, const void *c, int64_t ldc, void *d, int64_t ldd, int m, int n,
+                             int k, int32_t *status_dev, void *stream) {
+    if (m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) return DG_OK;
+    if (d == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || ldd < n || ldd % 8 != 0 || n % 8 != 0) return DG_ERR_ALIGNMENT;
+    if (c != nullptr && (!aligned16(c) || ldc < n || ldc % 8 != 0)) return DG_ERR_ALIGNMENT;
+    int sms = 0;
+    if (k == 0) {
+        dg_status st = check_device(&sms);
+        if (st != DG_OK) return st;
+        dg_fill_d_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint16_t *>(c), ldc, static_cast<uint16_t *>(d), ldd, m, n);
+        g_last_config[5] = 1;
+        return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    }
+    if (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    // the FP4 loads: K a multiple of 128, rows 32-byte aligned
+    if (k % kBlockK != 0) return DG_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(b) & 31u) != 0 || ldb % 32 != 0) return DG_ERR_ALIGNMENT;
+    if (lda < k || ldb < k / 2) return DG_ERR_INVALID_ARG;
+    if (lda % 16 != 0) return DG_ERR_ALIGNMENT;
+    dg_status st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeDense, m, n, k, status_dev);
+    p.c = static_cast<const uint16_t *>(c);
+    p.ldc = ldc;
+    p.layout = 4;
+    const int64_t psf_a = cdiv64(cdiv64(k, kGran), 4);   // 4 x 128 K per A word
+    const int64_t psf_b = k / kBlockK;                     // 4 x 32 K per B word
+    BsOperands o{a,   lda, static_cast<uint64_t>(m), b,   ldb, static_cast<uint64_t>(n),
+                 sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(psf_a),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_b),
+                 d,   ldd, static_cast<uint64_t>(m)};
+    const int64_t units = cdiv64(m, 2 * kBlockM);
+    const int bn = choose_fp4_block_n(units, n, sms, c != nullptr);
+    return launch_pair(p, o, 256, bn, units, sms, static_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,

@@ -41,7 +41,10 @@ namespace dg {
 // B_ATOM: B is MN-major ([K][N]); each CTA's B region per K-block is one whole
 // 128-byte swizzle atom wide (128 N-bytes x 128 K-rows) however many of its
 // columns (BN/2 <= 128) the MMA reads.
-template <int BN, int MP = 256, bool B_ATOM = false>
+// B4: B is FP4 (E2M1) with one scale per 32 K: its stages take the same shared
+// memory as FP8 (the loads leave 8 empty bytes after every 8 bytes of codes),
+// and a scale group holds one B word per column for each of its 4 K-blocks.
+template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false>
 struct Bs2Config {
     // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
     // with MP=128 each half of N is whole 16-column epilogue chunks
@@ -66,7 +69,9 @@ struct Bs2Config {
     // B scale words: MP=256 copies each 128-column chunk to all four lane quadrants;
     // MP=128 copies the two halves of N to quadrants {0,1} and {2,3} (one 64-row copy)
     static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
-    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4);
+    static constexpr int kSfbKb = B4 ? 4 : 1;                    // B words per column per group
+    static_assert(!B4 || (MP == 256 && BN <= 256), "FP4 B: 256-row pair tiles, one MMA");
+    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks * kSfbKb : 4);
     // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
     // destination, already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what
     // the MMA reads).  A scale warp loads a group up to kSfLookahead groups before
@@ -85,8 +90,10 @@ struct Bs2Config {
     static constexpr int kB2Bytes = kB2Rows * kBlockK;
     static constexpr int kBBytes = kB1Bytes + kB2Bytes;         // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
+    // bytes a K-block's loads deliver (FP4 B: the packed codes, half its stage)
+    static constexpr int kTxBytes = kABytes + (B4 ? kBBytes / 2 : kBBytes);
     static constexpr int kSfaBytes = 512;
-    static constexpr int kSfbBytes = 512 * kSfbChunks;
+    static constexpr int kSfbBytes = 512 * kSfbChunks * kSfbKb;
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
     static constexpr int kEpiChunk = 16;
     static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
@@ -397,8 +404,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_b2,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
-    constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0;
-    using Cfg = Bs2Config<BN, MP, B_MN>;
+    constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0;
+    static_assert(!B4 || (!A_MN && !B_MN && !F32), "FP4 B: K-major operands, bf16 D");
+    using Cfg = Bs2Config<BN, MP, B_MN, B4>;
     static_assert(LAY == 0 || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
@@ -501,7 +509,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     drop = false;  // diagnostic: leave this slot empty
                 } else {
                     const uint32_t fb = leader_full + slot * 8;
-                    if constexpr (LAY != 0) {
+                    if constexpr (A_MN || B_MN) {
                         // an MN-major operand: one box of 128 MN-bytes x G*128 K-rows fills the
                         // slot; the K-major one: G boxes (K-blocks past K are out of bounds,
                         // zero-filled, and still count their bytes)
@@ -539,7 +547,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         }
                     } else if (elect_one()) {
                         // the leader expects both CTAs' bytes; each CTA's loads count there
-                        if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kStageBytes);
+                        if (leader) mbar_arrive_expect_tx(&full_bar[slot], 2 * nk * Cfg::kTxBytes);
                         // a slot's B: the G K-blocks of the first MMA's rows, then the G
                         // K-blocks of the second's
                         auto load_kb = [&](int j) {
@@ -586,8 +594,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                               : make_desc_kmajor_sw128(smem_u32(smem_b));
             // a 32-K step: 32 bytes along a K-major row, 32 rows (4096 bytes) of an MN-major tile
             constexpr uint64_t kStepA = A_MN ? (4096 >> 4) : 2, kStepB = B_MN ? (4096 >> 4) : 2;
+            // (B format 5: E2M1)
             constexpr uint32_t idesc_base = make_idesc_mxf8(MMA_M, Cfg::kBN1, 0, 0) | (A_MN ? 1u << 15 : 0u) |
-                                            (B_MN ? 1u << 16 : 0u);
+                                            (B_MN ? 1u << 16 : 0u) | (B4 ? 5u << 10 : 0u);
             constexpr uint32_t idesc2_base = make_idesc_mxf8(MMA_M, Cfg::kBN2 > 0 ? Cfg::kBN2 : 16, 0, 0);
             for (int t = pair_id; t < num_tiles; t += num_pairs) {
                 // the tile's 128-K blocks (K-grouped: its group's; none for an empty group,
@@ -622,10 +631,15 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
                             const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
                             const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kB1Bytes >> 4));
+                            // FP4 B: this K-block's B cells, whose byte k scales the k-th 32 K
+                            const uint32_t sfb_tmem =
+                                sfa_tmem + 4 + (B4 ? static_cast<uint32_t>((kb & 3) * 4 * Cfg::kSfbChunks) : 0u);
 #pragma unroll
                             for (int k = 0; k < kBlockK / 32; ++k) {
-                                tc_mma_mxf8_pair(d_tmem, a_desc + kStepA * k, b_desc + kStepB * k, idesc, sfa_tmem,
-                                                 sfa_tmem + 4, (kb | k) != 0);
+                                const uint32_t idesc_k =
+                                    B4 ? (idesc_base | (static_cast<uint32_t>(k) << 4) | (sf << 29)) : idesc;
+                                tc_mma_mxf8_pair(d_tmem, a_desc + kStepA * k, b_desc + kStepB * k, idesc_k, sfa_tmem,
+                                                 sfb_tmem, (kb | k) != 0);
                                 if constexpr (Cfg::kBN2 > 0) {
                                     // columns [kBN1, BN): their accumulator columns, B rows and
                                     // B scale cells (column x at lane x % 32, cell x / 32)
@@ -732,13 +746,17 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     copy_word(p.sfa_words, p.sfa_ld, p.sfa_slices, st.sfa_x + 32 * q + static_cast<int>(lane), ya,
                               4 * lane + q);
                 if constexpr (MP == 256) {
+                    // FP4 B: one packed row per K-block, the group's 4 rows in 4 regions
 #pragma unroll
-                    for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                    for (int jj = 0; jj < Cfg::kSfbKb; ++jj)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
-                                      st.n0 + 128 * c + 32 * q + static_cast<int>(lane), yb,
-                                      128 + 128 * c + 4 * lane + q);
+                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
+                                          st.n0 + 128 * c + 32 * q + static_cast<int>(lane),
+                                          B4 ? 4 * yb + jj : yb,
+                                          128 + 128 * (jj * Cfg::kSfbChunks + c) + 4 * lane + q);
                 } else {
                     constexpr int kHalf = BN / 2;
 #pragma unroll
@@ -784,7 +802,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
                     if constexpr (MP == 256) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::kSfbChunks; ++c)
+                        for (int c = 0; c < Cfg::kSfbKb * Cfg::kSfbChunks; ++c)
                             tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
                                                       make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
                     } else {
@@ -1084,7 +1102,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
     cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
@@ -1106,7 +1124,7 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
 
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 int max_active_pairs_impl() {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
     if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
@@ -1128,7 +1146,7 @@ int max_active_pairs_impl() {
 
 template <int BN, int MP, int LAY = 0>
 void fill_bs2_info(KernelInfo *info) {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0>;
+    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
     info->block_n = BN;
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;

@@ -1,7 +1,8 @@
 // The compiled instantiations of the CTA-pair kernel: (BLOCK_N, with C, rows per
-// pair tile, FP32 D, operand layouts: bit 0 A MN-major, bit 1 B MN-major).  The
-// bf16-output NT ones are instantiated in gemm_bs2_inst.cu, the FP32-output ones
-// in gemm_bs2_inst_f32.cu, the NN/TN/TT ones in gemm_bs2_inst_mn.cu.
+// pair tile, FP32 D, operand layouts: bit 0 A MN-major, bit 1 B MN-major, bit 2
+// B FP4).  The bf16-output NT ones are instantiated in gemm_bs2_inst.cu, the
+// FP32-output ones in gemm_bs2_inst_f32.cu, the NN/TN/TT and K-grouped ones in
+// gemm_bs2_inst_mn.cu, the FP8 x FP4 ones in gemm_bs2_inst_fp4.cu.
 #pragma once
 
 #define DG_BS2_LIST_BF16(X)                                                                        \
@@ -22,4 +23,10 @@
     X(224, true, 256, false, 3) X(256, false, 256, false, 1) X(224, true, 256, false, 1)           \
     X(224, true, 256, true, 3)
 
-#define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X) DG_BS2_LIST_MN(X)
+// FP8 x FP4 (layout bit 2: B is E2M1 with one scale per 32 K): 128 or 256 columns
+// without C, 128 or 192 (two accumulators) with C
+#define DG_BS2_LIST_FP4(X)                                                                         \
+    X(256, false, 256, false, 4) X(128, false, 256, false, 4) X(128, true, 256, false, 4)          \
+    X(192, true, 256, false, 4)
+
+#define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X) DG_BS2_LIST_MN(X) DG_BS2_LIST_FP4(X)

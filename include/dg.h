@@ -172,6 +172,29 @@ dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fm
                          int m, int n, int k, int32_t *status_dev, void *stream);
 
 /*
+ * dg_fp8_fp4_gemm_nt -- FP8 activations x FP4 weights ("DeepSeek V4 源码剖析
+ * 第13章" §13.1 reason 2 and §13.5: E2M1 weights whose scales run along K, one
+ * per 32 elements; the tensor cores take the mixed operands directly):
+ *
+ *   D[m,n] = C[m,n] + sum_k A[m,k] sa(m, k/128) * B[n,k] sb(n, k/32)
+ *
+ *   a    E4M3 [m, lda], K contiguous; sfa packed UE8M0 int32 [ceil(k/512)][align4(m)]
+ *        (as for dg_fp8_gemm_nt: 4 x 128 K per word).
+ *   b    E2M1 codes packed two per byte, row n at b + n*ldb BYTES: element k is
+ *        byte k/2, low nibble for even k; b 32-byte aligned, ldb >= k/2 and a
+ *        multiple of 32 (else DG_ERR_ALIGNMENT / DG_ERR_INVALID_ARG).
+ *   sfb  packed UE8M0 int32 [k/128][align4(n)]: byte j of word (p, i) is the
+ *        scale of row i for K elements 128p + 32j .. 128p + 32j + 31; build it
+ *        with dg_transform_sf(sfb_fp32 [n][k/32], 1, n, k/32, 1, n, ...).
+ *   c    bf16 [m, ldc] or NULL (may equal d); d bf16 [m, ldd].
+ *   k a multiple of 128 (DG_ERR_ALIGNMENT otherwise); k == 0 gives D = C.
+ *   n, ldc, ldd multiples of 8.  Runs on 256-row CTA pairs.
+ */
+dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const void *b, int64_t ldb,
+                             const void *sfb, const void *c, int64_t ldc, void *d, int64_t ldd, int m, int n,
+                             int k, int32_t *status_dev, void *stream);
+
+/*
  * dg_m_grouped_fp8_gemm_nt_contiguous -- MoE GEMM grouped along M only
  * (PaperTrace §5.1; "DeepSeek V4 源码剖析 第13章" §13.6): the rows of all
  * experts are concatenated along M, each expert's segment starting on a

@@ -1,0 +1,92 @@
+"""FP8 x FP4 GEMM ("DeepSeek V4 源码剖析 第13章" §13.1 reason 2, §13.5: E2M1
+weights with one scale per 32 K, the mixed operands fed to the tensor cores)
+against the oracle, and bit for bit against the FP8 GEMM when the weights'
+32-K scales are equal within each 128-K block (the E2M1 codes re-encoded as
+E4M3, exactly): the same products in the same order."""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_gb300 import binding, inputs
+from tests._util import assert_close, bf16_bits, u8
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = "cuda"
+E2M1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def _b_device(b: torch.Tensor, pad: int = 0) -> torch.Tensor:
+    """Packed codes [N, K/2] on the device, rows 32-byte aligned (+ pad bytes)."""
+    n, kb = b.shape
+    ld = (kb + 31) // 32 * 32 + pad
+    wide = torch.zeros(n, ld, dtype=torch.uint8)
+    wide[:, :kb] = b
+    return wide.to(DEV)[:, :kb]
+
+
+def _run(case, c=None, pad=0):
+    M, N, K = case.shape
+    sfa = binding.transform_sf(case.sfa.to(DEV), 1, M)
+    sfb = binding.transform_sf(case.sfb.to(DEV), 1, N)     # [N, K/32] -> [K/128, align4(N)]
+    d = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.dg_fp8_fp4_gemm_nt(case.a.to(DEV), sfa, _b_device(case.b, pad), sfb, d, c=c, status=status)
+    cfg = binding.last_config()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return d, cfg
+
+
+@pytest.mark.parametrize("M,N,K,with_c,pad", [(256, 256, 512, False, 0), (300, 1000, 384, True, 32),
+                                              (17, 96, 128, False, 0), (1000, 2048, 1536, True, 0),
+                                              (513, 264, 896, False, 64), (128, 7168, 2048, False, 0)])
+def test_fp4_matches_oracle(orc, M, N, K, with_c, pad):
+    case = inputs.fp4_case(M, N, K, seed=M + N + K, with_c=with_c)
+    c = case.c.to(DEV) if with_c else None
+    d, cfg = _run(case, c=c, pad=pad)
+    assert cfg["kind"] == 2 and cfg["block_m"] == 256, cfg
+    ref = orc.gemm_fp8_fp4_nt(u8(case.a), case.sfa.double().numpy(), case.b.numpy(), case.sfb.double().numpy(),
+                              c=None if c is None else bf16_bits(case.c))
+    assert_close(bf16_bits(d), ref, f"fp4 {M}x{N}x{K}")
+
+
+def test_fp4_equals_fp8_gemm_on_the_same_values():
+    M, N, K = 512, 768, 1024
+    case = inputs.fp4_case(M, N, K, seed=91)
+    # one scale per 128-K block of each row, repeated over its four 32-K blocks
+    s128 = case.sfb[:, ::4].contiguous()
+    case.sfb = s128.repeat_interleave(4, dim=1).contiguous()
+    d4, _ = _run(case)
+    codes = torch.stack([case.b & 0xF, case.b >> 4], dim=-1).reshape(N, K).long()
+    b8 = E2M1[codes].to(torch.float8_e4m3fn)
+    assert torch.equal(b8.float(), E2M1[codes])
+    d8 = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    binding.dg_fp8_gemm_nt(case.a.to(DEV), binding.transform_sf(case.sfa.to(DEV), 1, M), b8.to(DEV),
+                           binding.transform_sf(s128.to(DEV), 1, N), d8)
+    torch.cuda.synchronize()
+    assert torch.equal(d4, d8)
+
+
+def test_fp4_workload_sampled(orc):
+    """4096 x 7168 x 16384 (the largest V3-like shape with FP4 weights) on sampled outputs."""
+    M, N, K = 4096, 7168, 16384
+    case = inputs.fp4_case(M, N, K, seed=92)
+    d, _ = _run(case)
+    rng = np.random.default_rng(7)
+    rows, cols = rng.integers(0, M, 3000), rng.integers(0, N, 3000)
+    ref = orc.gemm_fp8_fp4_nt_sampled(u8(case.a), case.sfa.double().numpy(), case.b.numpy(),
+                                      case.sfb.double().numpy(), rows, cols)
+    assert_close(bf16_bits(d)[rows, cols], ref, "fp4 workload")
+
+
+def test_fp4_rejects_k_not_multiple_of_128():
+    lib = binding.lib()
+    P = binding._p
+    a = torch.empty(128, 192, dtype=torch.float8_e4m3fn, device=DEV)
+    b = torch.empty(128, 96, dtype=torch.uint8, device=DEV)
+    sf = torch.empty(64, dtype=torch.int32, device=DEV)
+    d = torch.empty(128, 128, dtype=torch.bfloat16, device=DEV)
+    st = lib.dg_fp8_fp4_gemm_nt(P(a), 192, P(sf), P(b), 96, P(sf), None, 0, P(d), 128, 128, 128, 192, None, None)
+    assert st == 2   # DG_ERR_ALIGNMENT
