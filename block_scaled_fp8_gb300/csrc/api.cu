@@ -826,6 +826,17 @@ dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const 
                  sfa, static_cast<uint64_t>(m), static_cast<uint64_t>(psf_a),
                  sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(psf_b),
                  d,   ldd, static_cast<uint64_t>(m)};
+    if (m <= kBlockM && c == nullptr) {
+        // M <= 128: 128-row pairs (each CTA loads 64 rows of A), the widest tile that
+        // still gives most pairs a tile, as the weight stream from HBM sets the time
+        int bn = 32;
+        for (int cand : {128, 96, 64})
+            if (cdiv64(n, cand) * 10 >= static_cast<int64_t>(sms / 2) * 9) {
+                bn = cand;
+                break;
+            }
+        return launch_pair(p, o, 128, bn, 1, sms, static_cast<cudaStream_t>(stream));
+    }
     const int64_t units = cdiv64(m, 2 * kBlockM);
     const int bn = choose_fp4_block_n(units, n, sms, c != nullptr);
     return launch_pair(p, o, 256, bn, units, sms, static_cast<cudaStream_t>(stream));

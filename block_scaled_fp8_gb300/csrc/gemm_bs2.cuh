@@ -70,8 +70,8 @@ struct Bs2Config {
     // MP=128 copies the two halves of N to quadrants {0,1} and {2,3} (one 64-row copy)
     static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
     static constexpr int kSfbKb = B4 ? 4 : 1;                    // B words per column per group
-    static_assert(!B4 || (MP == 256 && BN <= 256), "FP4 B: 256-row pair tiles, one MMA");
-    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks * kSfbKb : 4);
+    static_assert(!B4 || BN <= 256, "FP4 B: one MMA per K step");
+    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4) * kSfbKb;
     // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
     // destination, already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what
     // the MMA reads).  A scale warp loads a group up to kSfLookahead groups before
@@ -407,11 +407,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0;
     static_assert(!B4 || (!A_MN && !B_MN && !F32), "FP4 B: K-major operands, bf16 D");
     using Cfg = Bs2Config<BN, MP, B_MN, B4>;
-    static_assert(LAY == 0 || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
+    static_assert(!(A_MN || B_MN) || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
     constexpr int G = Cfg::kGroupKb;
-    static_assert(LAY == 0 || G * kBlockK <= 256, "an MN-major box holds at most 256 K rows");
+    static_assert(!(A_MN || B_MN) || G * kBlockK <= 256, "an MN-major box holds at most 256 K rows");
     constexpr int NUM_ACC = Cfg::kNumAcc;
     constexpr int NSF = Cfg::kSfSlots;       // shared-memory scale slots
     constexpr int NTS = Cfg::kSfTmemSlots;   // TMEM scale slots
@@ -632,8 +632,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
                             const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kB1Bytes >> 4));
                             // FP4 B: this K-block's B cells, whose byte k scales the k-th 32 K
+                            constexpr int kSfbRegionCols = MP == 256 ? 4 * Cfg::kSfbChunks : 4;
                             const uint32_t sfb_tmem =
-                                sfa_tmem + 4 + (B4 ? static_cast<uint32_t>((kb & 3) * 4 * Cfg::kSfbChunks) : 0u);
+                                sfa_tmem + 4 + (B4 ? static_cast<uint32_t>((kb & 3) * kSfbRegionCols) : 0u);
 #pragma unroll
                             for (int k = 0; k < kBlockK / 32; ++k) {
                                 const uint32_t idesc_k =
@@ -760,13 +761,15 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 } else {
                     constexpr int kHalf = BN / 2;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int jj = 0; jj < Cfg::kSfbKb; ++jj)
 #pragma unroll
-                        for (int q = 0; q < (kHalf + 31) / 32; ++q)
-                            if (32 * q + static_cast<int>(lane) < kHalf)
-                                copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
-                                          st.n0 + h * kHalf + 32 * q + static_cast<int>(lane), yb,
-                                          128 + 4 * (32 * h + lane) + q);
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < (kHalf + 31) / 32; ++q)
+                                if (32 * q + static_cast<int>(lane) < kHalf)
+                                    copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
+                                              st.n0 + h * kHalf + 32 * q + static_cast<int>(lane),
+                                              B4 ? 4 * yb + jj : yb, 128 + 256 * jj + 4 * (32 * h + lane) + q);
                 }
                 lj += NW;
                 settle();
@@ -806,7 +809,10 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
                                                       make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
                     } else {
-                        tc_cp_64x128b_warpx2_01_23_pair(sfa_tmem + 4, make_desc_sf_32x128b(smem_u32(sfb_buf)));
+#pragma unroll
+                        for (int jj = 0; jj < Cfg::kSfbKb; ++jj)
+                            tc_cp_64x128b_warpx2_01_23_pair(sfa_tmem + 4 + 4 * jj,
+                                                            make_desc_sf_32x128b(smem_u32(sfb_buf + 256 * jj)));
                     }
                     tc_commit_pair(&sf_ready_bar[tslot], 0x1);
                     tc_commit_pair(&sf_sfree_bar[slot], 0x3);   // both CTAs may refill the slot

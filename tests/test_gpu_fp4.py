@@ -41,12 +41,15 @@ def _run(case, c=None, pad=0):
 
 @pytest.mark.parametrize("M,N,K,with_c,pad", [(256, 256, 512, False, 0), (300, 1000, 384, True, 32),
                                               (17, 96, 128, False, 0), (1000, 2048, 1536, True, 0),
-                                              (513, 264, 896, False, 64), (128, 7168, 2048, False, 0)])
+                                              (513, 264, 896, False, 64), (128, 7168, 2048, False, 0),
+                                              (64, 2112, 1024, False, 0), (100, 24576, 384, False, 32),
+                                              (128, 520, 640, True, 0)])
 def test_fp4_matches_oracle(orc, M, N, K, with_c, pad):
     case = inputs.fp4_case(M, N, K, seed=M + N + K, with_c=with_c)
     c = case.c.to(DEV) if with_c else None
     d, cfg = _run(case, c=c, pad=pad)
-    assert cfg["kind"] == 2 and cfg["block_m"] == 256, cfg
+    # M <= 128 without C: 128-row pairs; otherwise 256-row pairs
+    assert cfg["kind"] == 2 and cfg["block_m"] == (128 if M <= 128 and not with_c else 256), cfg
     ref = orc.gemm_fp8_fp4_nt(u8(case.a), case.sfa.double().numpy(), case.b.numpy(), case.sfb.double().numpy(),
                               c=None if c is None else bf16_bits(case.c))
     assert_close(bf16_bits(d), ref, f"fp4 {M}x{N}x{K}")
