@@ -676,32 +676,39 @@ def run_case(args):
     build.build()
     m, n, k = (int(x) for x in args.case.split(","))
     dev = torch.device("cuda", 0)
-    case = inputs.dense_case(m, n, k, seed=0, with_c=args.with_c)
+    if args.fp4:
+        case = inputs.fp4_case(m, n, k, seed=0, with_c=args.with_c, device=dev)
+        sfb = binding.transform_sf(case.sfb.contiguous(), 1, n)
+        gemm = binding.dg_fp8_fp4_gemm_nt
+    else:
+        case = inputs.dense_case(m, n, k, seed=0, with_c=args.with_c)
+        sfb = binding.transform_sf(case.sfb.to(dev), 128, n)
+        gemm = binding.dg_fp8_gemm_nt
     a, b = case.a.to(dev), case.b.to(dev)
     sfa = binding.transform_sf(case.sfa.to(dev), 1, m)
-    sfb = binding.transform_sf(case.sfb.to(dev), 128, n)
     c = case.c.to(dev) if args.with_c else None
     d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(args.warmup):
-        binding.dg_fp8_gemm_nt(a, sfa, b, sfb, d, c=c, status=status)
+        gemm(a, sfa, b, sfb, d, c=c, status=status)
     torch.cuda.synchronize()
     times = []
     for i in range(args.steps):
         flush.fill_(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        binding.dg_fp8_gemm_nt(a, sfa, b, sfb, d, c=c, status=status)
+        gemm(a, sfa, b, sfb, d, c=c, status=status)
         e1.record()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     assert int(status.item()) == 0, int(status.item())
     us = statistics.median(times) * 1e3
     cfg = binding.last_config()
-    print(json.dumps({"case": [m, n, k], "with_c": args.with_c, "median_us": round(us, 2),
+    print(json.dumps({"case": [m, n, k], "with_c": args.with_c, "fp4": args.fp4, "median_us": round(us, 2),
                       "tflops": round(flops(m, n, k) / (us * 1e-6) / 1e12, 1),
-                      "gbs": round(gemm_bytes(m, n, k) / (us * 1e-6) / 1e9, 1), "config": cfg}))
+                      "gbs": round((m * k + n * k // 2 + 2 * m * n if args.fp4 else gemm_bytes(m, n, k))
+                                   / (us * 1e-6) / 1e9, 1), "config": cfg}))
 
 
 def e2e_pipelined(probs, steps, status, stream):
@@ -766,6 +773,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None, help="M,N,K: time one dense GEMM shape only")
     ap.add_argument("--with-c", action="store_true")
+    ap.add_argument("--fp4", action="store_true", help="with --case: FP4 (E2M1) weights, dg_fp8_fp4_gemm_nt")
     ap.add_argument("--case-k-grouped", default=None,
                     help="E,M,N,K: time one K-grouped GEMM (E groups of K rows each, C = D in place)")
     ap.add_argument("--gpus", type=int, default=1)
