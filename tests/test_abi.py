@@ -106,3 +106,29 @@ def test_k_grouped_host_validation_without_gpu(lib):
     assert call(m=-4) == 1
     assert lib.dg_transform_sf_k_grouped(P(16), 6, ks, 4, P(16), None, None) == 3
     assert lib.dg_transform_sf_k_grouped(P(16), 8, bad, 2, P(16), None, None) == 1
+
+
+def test_fp4_and_layout_host_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+
+    def fp4(a=32, lda=256, sfa=16, b=32, ldb=128, sfb=16, c=None, ldc=0, d=16, ldd=64, m=8, n=64, k=256):
+        return lib.dg_fp8_fp4_gemm_nt(P(a), lda, P(sfa), P(b), ldb, P(sfb), P(c), ldc, P(d), ldd, m, n, k,
+                                      None, None)
+    assert fp4(m=-1) == 1
+    assert fp4(m=0) == 0
+    assert fp4(k=192, lda=256) == 2          # K % 128 != 0 (the 4-bit loads' rule)
+    assert fp4(b=48) == 2                    # B not 32-byte aligned
+    assert fp4(ldb=112) == 2                 # B row stride not a multiple of 32 bytes
+    assert fp4(ldb=96, k=256) == 1           # ldb < k/2
+    assert fp4(n=60, ldd=64) == 2            # N % 8 != 0
+    assert fp4(sfb=0) == 1
+
+    def lay(fn, a=16, lda=64, b=16, ldb=64, m=64, n=64, k=128):
+        return getattr(lib, fn)(P(a), lda, P(16), 1, P(b), ldb, P(16), 1, None, 0, P(16), 64, m, n, k, None, None)
+    # nn: A [m][k] K-contiguous, B [k][n]; tn: A [k][m], B [k][n]; tt: A [k][m], B [n][k]
+    assert lay("dg_fp8_gemm_nn", lda=128, ldb=48) == 1    # N-contiguous B: ldb < n
+    assert lay("dg_fp8_gemm_nn", lda=112, ldb=64) == 1    # K-contiguous A: lda < k
+    assert lay("dg_fp8_gemm_tn", lda=48, ldb=64) == 1     # M-contiguous A: lda < m
+    assert lay("dg_fp8_gemm_tt", lda=72, ldb=128) == 2    # lda % 16 != 0
+    assert lay("dg_fp8_gemm_nn", lda=128, ldb=64, k=120) == 2   # K-contiguous A: K % 16 != 0
+    assert lay("dg_fp8_gemm_tt", m=0) == 0
