@@ -286,6 +286,40 @@ def gemm_fp8_fp4_nt_sampled(a, sa, b, sb, rows, cols, nthreads: int = 0) -> np.n
     return out
 
 
+def m_grouped_fp8_fp4_contiguous(a, sa, b, sb, grouped_layout, d_init=None, nthreads: int = 0):
+    """Contiguous M-grouped FP8 x FP4 GEMM ("DeepSeek V4 源码剖析 第13章" §13.6;
+    PaperTrace DeepGEMM §5.1): row m of A uses expert grouped_layout[m]'s
+    weights; a row marked -1 keeps d_init.  a [M, K] E4M3, sa [M, K/128];
+    b [E, N, K/2] packed E2M1, sb [E, N, K/32].  Each expert's rows are the
+    dense FP8 x FP4 GEMM of those rows with that expert's weights."""
+    a = _u8(a)
+    layout = np.asarray(grouped_layout)
+    E, N = b.shape[0], b.shape[1]
+    d = (np.zeros((a.shape[0], N), dtype=np.uint16) if d_init is None
+         else np.ascontiguousarray(d_init).view(np.uint16).copy())
+    for e in range(E):
+        rows = np.nonzero(layout == e)[0]
+        if len(rows):
+            d[rows] = gemm_fp8_fp4_nt(a[rows], np.asarray(sa)[rows], b[e], sb[e], nthreads=nthreads)
+    return d
+
+
+def m_grouped_fp8_fp4_masked(a, sa, b, sb, masked_m, d_init=None, nthreads: int = 0):
+    """Masked M-grouped FP8 x FP4 GEMM (PaperTrace DeepGEMM §5.2): expert e
+    computes its first masked_m[e] rows of a [E, max_m, K]; the other rows keep
+    d_init.  sa [E, max_m, K/128]; b [E, N, K/2]; sb [E, N, K/32]."""
+    a = _u8(a)
+    E, max_m = a.shape[0], a.shape[1]
+    N = b.shape[1]
+    d = (np.zeros((E, max_m, N), dtype=np.uint16) if d_init is None
+         else np.ascontiguousarray(d_init).view(np.uint16).copy())
+    for e in range(E):
+        m = int(masked_m[e])
+        if m:
+            d[e, :m] = gemm_fp8_fp4_nt(a[e, :m], np.asarray(sa)[e, :m], b[e], sb[e], nthreads=nthreads)
+    return d
+
+
 def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarray,
                 c: np.ndarray | None = None, nthreads: int = 0) -> np.ndarray:
     """D = C + A @ B^T as gemm_nt, with FP32 C (or none) and FP32 D: the fp64

@@ -728,3 +728,39 @@ def test_fp8_fp4_reduces_to_fp8_nt(orc):
     got = orc.gemm_fp8_fp4_nt(a, sa, b, sb)
     want = orc.gemm_nt(a, sa, b8, s128)
     assert np.array_equal(got, want)
+
+
+def test_m_grouped_fp4_oracles_bruteforce(orc):
+    """The grouped FP8 x FP4 oracles against the packed-storage brute force on a
+    few elements of every expert: the expert's own weights and scales, and
+    untouched rows outside the groups."""
+    E, N, K = 3, 6, 128
+    cases = [inputs.fp4_case(8, N, K, seed=83 + e) for e in range(E)]
+    b = np.stack([c.b.numpy() for c in cases])
+    sb = np.stack([c.sfb.double().numpy() for c in cases])
+    a_all = torch.cat([c.a for c in cases]).view(torch.uint8).numpy()[:20]
+    sa_all = torch.cat([c.sfa for c in cases]).double().numpy()[:20]
+    layout = np.array([0] * 5 + [-1] * 3 + [2] * 7 + [1] * 5)
+    init = np.full((20, N), 0x7FC1, dtype=np.uint16)
+    d = orc.m_grouped_fp8_fp4_contiguous(a_all, sa_all, b, sb, layout, d_init=init)
+    A = _decode_codes_torch(torch.from_numpy(a_all))
+    for m in range(20):
+        e = layout[m]
+        for n in range(N):
+            if e < 0:
+                assert d[m, n] == 0x7FC1
+                continue
+            codes = _nibbles(b[e, n], K)
+            s = Fraction(0)
+            for k in range(K):
+                if A[m, k] and codes[k] & 7:
+                    s += (Fraction(float(A[m, k])) * Fraction(float(sa_all[m, k // 128])) *
+                          Fraction(E2M1_TEXTBOOK[codes[k]]) * Fraction(float(sb[e, n, k // 32])))
+            assert d[m, n] == _bf16_nearest_bruteforce(s), (m, n)
+    # masked: the same rows as experts' first rows
+    am = np.stack([a_all[0:5], a_all[8:13], a_all[15:20]])
+    sam = np.stack([sa_all[0:5], sa_all[8:13], sa_all[15:20]])
+    dm = orc.m_grouped_fp8_fp4_masked(am, sam, b[[0, 2, 1]], sb[[0, 2, 1]], [5, 3, 0],
+                                      d_init=np.full((3, 5, N), 0x7FC1, dtype=np.uint16))
+    assert np.array_equal(dm[0], d[0:5]) and np.array_equal(dm[1, :3], d[8:11])
+    assert np.all(dm[1, 3:] == 0x7FC1) and np.all(dm[2] == 0x7FC1)
