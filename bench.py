@@ -244,6 +244,18 @@ def measure_other_workloads(dev, flush, reps, stream):
                                                                             status=status),
                    flops(valid, n, k), valid * k + used * n * k + 2 * mt * n,
                    {"valid_rows": valid, "rows": mt})
+        if n == 4096:
+            # the same experts with FP4 (E2M1) weights, one scale per 32 K
+            fb = [inputs.fp4_case(1, n, k, seed=40 + e, device=dev) for e in range(8)]
+            b4 = torch.stack([f.b for f in fb])
+            sfb4 = binding.transform_sf(torch.stack([f.sfb for f in fb]).contiguous(), 1, n)
+            del fb
+            record(f"m-grouped contiguous FP8 x FP4 8 experts N={n} K={k}",
+                   lambda: binding.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(cc.a, sfa, b4, sfb4, d, cc.grouped_layout,
+                                                                           status=status),
+                   flops(valid, n, k), valid * k + used * n * k // 2 + 2 * valid * n,
+                   {"valid_rows": valid, "rows": mt, "weights": "e2m1"})
+            del b4, sfb4
         del cc, sfa, sfb, d
 
     # K-grouped weight gradient of the contiguous MoE layer (8 experts, N=4096 x K=7168
@@ -273,7 +285,17 @@ def measure_other_workloads(dev, flush, reps, stream):
                                                            mc.expected_m, status=status),
            flops(valid, n, k), valid * k + used * n * k + 2 * valid * n,
            {"valid_rows": valid, "bound": "hbm"})
-    del mc, sfa, sfb, d
+    # the same decode with FP4 (E2M1) expert weights: half the weight bytes
+    fb = [inputs.fp4_case(1, n, k, seed=80 + i, device=dev) for i in range(e)]
+    b4 = torch.stack([f.b for f in fb])
+    sfb4 = binding.transform_sf(torch.stack([f.sfb for f in fb]).contiguous(), 1, n)
+    del fb
+    record(f"m-grouped masked FP8 x FP4 {e} experts max_m={max_m} N={n} K={k}",
+           lambda: binding.dg_m_grouped_fp8_fp4_gemm_nt_masked(mc.a, sfa, b4, sfb4, d, mc.masked_m, mc.expected_m,
+                                                               status=status),
+           flops(valid, n, k), valid * k + used * n * k // 2 + 2 * valid * n,
+           {"valid_rows": valid, "bound": "hbm", "weights": "e2m1"})
+    del mc, sfa, sfb, d, b4, sfb4
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the other workloads")

@@ -30,7 +30,7 @@ DG_DEBUG_WIDE_PAIR = 8
 # Every symbol include/dg.h declares.
 EXPORTS = (
     "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn", "dg_fp8_gemm_tt",
-    "dg_fp8_fp4_gemm_nt",
+    "dg_fp8_fp4_gemm_nt", "dg_m_grouped_fp8_fp4_gemm_nt_contiguous", "dg_m_grouped_fp8_fp4_gemm_nt_masked",
     "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped", "dg_k_grouped_packed_sf_rows",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
@@ -74,6 +74,11 @@ def lib():
                                                           i32, i32, i32, P, P]
             L.dg_fp8_fp4_gemm_nt.argtypes = [P, i64, P, P, i64, P, P, i64, P, i64, i32, i32, i32, P, P]
             L.dg_fp8_fp4_gemm_nt.restype = i32
+            L.dg_m_grouped_fp8_fp4_gemm_nt_contiguous.argtypes = [P, i64, P, P, i64, P, P, i64, P, i32, i32, i32,
+                                                                  i32, P, P]
+            L.dg_m_grouped_fp8_fp4_gemm_nt_masked.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
+            for f in ("dg_m_grouped_fp8_fp4_gemm_nt_contiguous", "dg_m_grouped_fp8_fp4_gemm_nt_masked"):
+                getattr(L, f).restype = i32
             L.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [P, i64, P, P, i64, P, P, P, i32, i32, P, P, i32,
                                                               P, P]
             L.dg_transform_sf_k_grouped.argtypes = [P, i32, P, i32, P, P, P]
@@ -266,6 +271,32 @@ def dg_fp8_fp4_gemm_nt(a, sfa, b, sfb, d, c=None, status=None, stream=None):
     _check("dg_fp8_fp4_gemm_nt", lib().dg_fp8_fp4_gemm_nt(
         _p(a), a.stride(0), _p(sfa), _p(b), b.stride(0), _p(sfb), _p(c), 0 if c is None else c.stride(0), _p(d),
         d.stride(0), M, N, K, _p(status), _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, d, grouped_layout, status=None, stream=None):
+    """a [M_total, K] E4M3; b uint8 [E, N, K/2] packed E2M1 (row stride = stride(1)
+    bytes, expert stride N * stride(1)); sfa packed [ceil(K/512), align4(M_total)];
+    sfb packed [E, K/128, align4(N)]; d bf16 [M_total, N]; grouped_layout int32 [M_total]."""
+    M, K = a.shape
+    E, N, _ = b.shape
+    assert b.dtype == torch.uint8 and b.stride(0) == N * b.stride(1) and b.stride(2) == 1
+    assert a.stride(1) == 1 and d.stride(1) == 1
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_contiguous", lib().dg_m_grouped_fp8_fp4_gemm_nt_contiguous(
+        _p(a), a.stride(0), _p(sfa), _p(b), b.stride(1), _p(sfb), _p(d), d.stride(0), _p(grouped_layout), M, N, K,
+        E, _p(status), _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, expected_m, status=None, stream=None):
+    """a [E, max_m, K] E4M3 contiguous; b uint8 [E, N, K/2] contiguous; sfa packed
+    [E, ceil(K/512), align4(max_m)]; sfb packed [E, K/128, align4(N)]; d bf16 [E, max_m, N]."""
+    E, max_m, K = a.shape
+    N = b.shape[1]
+    assert a.is_contiguous() and b.is_contiguous() and d.is_contiguous() and b.dtype == torch.uint8
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_masked", lib().dg_m_grouped_fp8_fp4_gemm_nt_masked(
+        _p(a), _p(sfa), _p(b), _p(sfb), _p(d), _p(masked_m), E, max_m, int(expected_m), N, K, _p(status),
+        _stream(stream)))
     return d
 
 

@@ -842,6 +842,83 @@ dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const 
     return launch_pair(p, o, 256, bn, units, sms, static_cast<cudaStream_t>(stream));
 }
 
+// Operand rules of the FP4 weights: K a multiple of 128, rows 32-byte aligned.
+static dg_status check_fp4_operands(const void *a, int64_t lda, const void *b, int64_t ldb, int n, int k) {
+    if (a == nullptr || b == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(a) || (reinterpret_cast<uintptr_t>(b) & 31u) != 0) return DG_ERR_ALIGNMENT;
+    if (k % kBlockK != 0 || n % 8 != 0 || ldb % 32 != 0 || lda % 16 != 0) return DG_ERR_ALIGNMENT;
+    if (lda < k || ldb < k / 2) return DG_ERR_INVALID_ARG;
+    return DG_OK;
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
+                                                  int64_t ldb, const void *sfb, void *d, int64_t ldd,
+                                                  const int32_t *grouped_layout, int m_total, int n, int k,
+                                                  int num_groups, int32_t *status_dev, void *stream) {
+    if (m_total < 0 || n < 0 || k < 0 || num_groups < 1) return DG_ERR_INVALID_ARG;
+    if (m_total % kBlockM != 0) return DG_ERR_LAYOUT;
+    if (m_total == 0 || n == 0) return DG_OK;
+    if (k == 0) return DG_ERR_UNSUPPORTED;
+    dg_status st = check_fp4_operands(a, lda, b, ldb, n, k);
+    if (st != DG_OK) return st;
+    if (d == nullptr || sfa == nullptr || sfb == nullptr || grouped_layout == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || !aligned16(sfa) || !aligned16(sfb) || ldd < n || ldd % 8 != 0) return DG_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(num_groups) * n > INT32_MAX || cdiv64(m_total, 2 * kBlockM) > kMaxPairPrefix ||
+        num_groups >= 32768)
+        return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeContiguous, m_total, n, k, status_dev);
+    p.num_groups = num_groups;
+    p.grouped_layout = grouped_layout;
+    p.layout = 4;
+    const int64_t psf_a = cdiv64(cdiv64(k, kGran), 4);
+    const int64_t kb = k / kBlockK;
+    BsOperands o{a,   lda, static_cast<uint64_t>(m_total),
+                 b,   ldb, static_cast<uint64_t>(num_groups) * n,
+                 sfa, static_cast<uint64_t>(m_total), static_cast<uint64_t>(psf_a),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(kb * num_groups),
+                 d,   ldd, static_cast<uint64_t>(m_total)};
+    const int64_t blocks = m_total / kBlockM;
+    const int bn = choose_fp4_block_n(cdiv64(blocks, 2), n, sms, false);
+    return launch_pair(p, o, 256, bn, blocks, sms, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void *a, const void *sfa, const void *b, const void *sfb,
+                                              void *d, const int32_t *masked_m, int num_groups, int max_m,
+                                              int expected_m, int n, int k, int32_t *status_dev, void *stream) {
+    if (num_groups < 1 || max_m < 0 || n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+    if (num_groups > kMaxPairPrefix) return DG_ERR_UNSUPPORTED;
+    if (max_m == 0 || n == 0) return DG_OK;
+    if (k == 0) return DG_ERR_UNSUPPORTED;
+    dg_status st = check_fp4_operands(a, k, b, k / 2, n, k);
+    if (st != DG_OK) return st;
+    if (d == nullptr || sfa == nullptr || sfb == nullptr || masked_m == nullptr) return DG_ERR_INVALID_ARG;
+    if (!aligned16(d) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(num_groups) * max_m > INT32_MAX || static_cast<int64_t>(num_groups) * n > INT32_MAX)
+        return DG_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != DG_OK) return st;
+    GemmParams p = base_params(kModeMasked, max_m, n, k, status_dev);
+    p.num_groups = num_groups;
+    p.masked_m = masked_m;
+    p.layout = 4;
+    p.num_m_blocks = static_cast<int>(cdiv64(max_m, kBlockM));
+    const int64_t psf_a = cdiv64(cdiv64(k, kGran), 4);
+    const int64_t kb = k / kBlockK;
+    BsOperands o{a,   k,     static_cast<uint64_t>(num_groups) * max_m,
+                 b,   k / 2, static_cast<uint64_t>(num_groups) * n,
+                 sfa, static_cast<uint64_t>(max_m), static_cast<uint64_t>(psf_a * num_groups),
+                 sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(kb * num_groups),
+                 d,   n,     static_cast<uint64_t>(num_groups) * max_m};
+    const int exp_m = expected_m > 0 ? (expected_m < max_m ? expected_m : max_m) : max_m;
+    const int bn = choose_fp4_block_n(static_cast<int64_t>(num_groups) * cdiv64(exp_m, 2 * kBlockM), n, sms, false);
+    return launch_pair(p, o, 256, bn, static_cast<int64_t>(num_groups) * p.num_m_blocks, sms,
+                       static_cast<cudaStream_t>(stream));
+}
+
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa,
                                               int sfa_fmt, const void *b, int64_t ldb,
                                               const void *sfb, int sfb_fmt, void *d, int64_t ldd,

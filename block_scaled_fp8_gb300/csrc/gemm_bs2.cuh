@@ -387,7 +387,8 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
     }
     tile.b_row0 = group * p.n + tile.n0 + rank * Bs2Config<BN, MP>::kB1Rows;
     tile.b2_row0 = group * p.n + tile.n0 + Bs2Config<BN, MP>::kBN1 + rank * Bs2Config<BN, MP>::kB2Rows;
-    tile.sfb_y0 = p.mode == kModeKGrouped ? tile.sfa_y0 : group * psf_k;
+    // (FP4 B: one packed scale row per K-block, so an expert's rows start at e * K-blocks)
+    tile.sfb_y0 = p.mode == kModeKGrouped ? tile.sfa_y0 : group * ((p.layout & 4) ? p.num_k_blocks : psf_k);
     if (p.mode != kModeKGrouped) tile.d_row0 = tile.a_row0;
 }
 
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             for (int q = 0; q < 4; ++q)
                                 copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
                                           st.n0 + 128 * c + 32 * q + static_cast<int>(lane),
-                                          B4 ? 4 * yb + jj : yb,
+                                          B4 ? st.sfb_y0 + 4 * lj + jj : yb,
                                           128 + 128 * (jj * Cfg::kSfbChunks + c) + 4 * lane + q);
                 } else {
                     constexpr int kHalf = BN / 2;
@@ -769,7 +770,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                 if (32 * q + static_cast<int>(lane) < kHalf)
                                     copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
                                               st.n0 + h * kHalf + 32 * q + static_cast<int>(lane),
-                                              B4 ? 4 * yb + jj : yb, 128 + 256 * jj + 4 * (32 * h + lane) + q);
+                                              B4 ? st.sfb_y0 + 4 * lj + jj : yb, 128 + 256 * jj + 4 * (32 * h + lane) + q);
                 }
                 lj += NW;
                 settle();

@@ -195,6 +195,30 @@ dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const 
                              int k, int32_t *status_dev, void *stream);
 
 /*
+ * dg_m_grouped_fp8_fp4_gemm_nt_contiguous / _masked -- the MoE GEMMs grouped
+ * along M with FP4 expert weights ("DeepSeek V4 源码剖析 第13章" §13.6: the
+ * routed experts run FP8 activations x FP4 weights through
+ * m_grouped_fp8_fp4_gemm_nt_{contiguous,masked}).  Layouts, grouped_layout,
+ * masked_m and expected_m as for the FP8 calls below; B and its scales as for
+ * dg_fp8_fp4_gemm_nt, per expert:
+ *   b    E2M1 packed [num_groups][n][ldb bytes] (masked: ldb = k/2), expert
+ *        stride n*ldb; 32-byte aligned, ldb a multiple of 32.
+ *   sfb  packed int32 [num_groups][k/128][align4(n)] (dg_transform_sf on FP32
+ *        [num_groups][n][k/32] with gran_mn 1 and batch num_groups).
+ *   sfa  packed as for the FP8 calls ([ceil(k/512)][align4(m_total)], masked:
+ *        [num_groups][ceil(k/512)][align4(max_m)]).
+ *   k a multiple of 128.  Runs on 256-row CTA pairs only: the contiguous form
+ *   takes m_total <= 131072, the masked one at most 512 experts.
+ */
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
+                                                  int64_t ldb, const void *sfb, void *d, int64_t ldd,
+                                                  const int32_t *grouped_layout, int m_total, int n, int k,
+                                                  int num_groups, int32_t *status_dev, void *stream);
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void *a, const void *sfa, const void *b, const void *sfb,
+                                              void *d, const int32_t *masked_m, int num_groups, int max_m,
+                                              int expected_m, int n, int k, int32_t *status_dev, void *stream);
+
+/*
  * dg_m_grouped_fp8_gemm_nt_contiguous -- MoE GEMM grouped along M only
  * (PaperTrace §5.1; "DeepSeek V4 源码剖析 第13章" §13.6): the rows of all
  * experts are concatenated along M, each expert's segment starting on a

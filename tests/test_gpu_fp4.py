@@ -93,3 +93,73 @@ def test_fp4_rejects_k_not_multiple_of_128():
     d = torch.empty(128, 128, dtype=torch.bfloat16, device=DEV)
     st = lib.dg_fp8_fp4_gemm_nt(P(a), 192, P(sf), P(b), 96, P(sf), None, 0, P(d), 128, 128, 128, 192, None, None)
     assert st == 2   # DG_ERR_ALIGNMENT
+
+
+def _experts(E, N, K, seed):
+    cases = [inputs.fp4_case(1, N, K, seed=seed + e) for e in range(E)]
+    return torch.stack([c.b for c in cases]), torch.stack([c.sfb for c in cases])
+
+
+@pytest.mark.parametrize("m_per_expert,N,K", [([5, 130, 0, 256, 300], 264, 512), ([128] * 4, 7168, 2048),
+                                              ([1000, 17], 520, 1152)])
+def test_fp4_contiguous_matches_oracle(orc, m_per_expert, N, K):
+    E = len(m_per_expert)
+    base = inputs.contiguous_case(E, 8, K, seed=sum(m_per_expert), m_per_expert=m_per_expert)
+    b, sfb = _experts(E, N, K, seed=95)
+    M = base.a.shape[0]
+    sfa_p = binding.transform_sf(base.sfa.to(DEV), 1, M)
+    sfb_p = binding.transform_sf(sfb.contiguous().to(DEV), 1, N)
+    d = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(base.a.to(DEV), sfa_p, b.to(DEV), sfb_p, d,
+                                                    base.grouped_layout.to(DEV), status=status)
+    cfg = binding.last_config()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and cfg["kind"] == 2 and cfg["block_m"] == 256, cfg
+    init = bf16_bits(torch.full((M, N), 7.0, dtype=torch.bfloat16))
+    ref = orc.m_grouped_fp8_fp4_contiguous(u8(base.a), base.sfa.double().numpy(), b.numpy(),
+                                           sfb.double().numpy(), base.grouped_layout.numpy(), d_init=init)
+    got = bf16_bits(d)
+    valid = base.grouped_layout.numpy() >= 0
+    if valid.any():
+        assert_close(got[valid], ref[valid], f"fp4 contiguous {m_per_expert}")
+    assert np.array_equal(got[~valid], ref[~valid])
+    # each expert's rows equal the dense FP8 x FP4 GEMM of those rows, bit for bit
+    for e in range(E):
+        rows = np.nonzero(base.grouped_layout.numpy() == e)[0]
+        if len(rows) == 0:
+            continue
+        ae = base.a[torch.from_numpy(rows)]
+        de = torch.empty(len(rows), N, dtype=torch.bfloat16, device=DEV)
+        binding.dg_fp8_fp4_gemm_nt(ae.to(DEV), binding.transform_sf(base.sfa[torch.from_numpy(rows)].to(DEV), 1,
+                                                                    len(rows)),
+                                   b[e].to(DEV), binding.transform_sf(sfb[e].contiguous().to(DEV), 1, N), de)
+        torch.cuda.synchronize()
+        if binding.last_config()["block_m"] == 256:
+            assert torch.equal(de, d[torch.from_numpy(rows).to(DEV)]), e
+
+
+@pytest.mark.parametrize("masked_m,max_m,N,K", [([0, 256, 17, 300], 320, 264, 512), ([5, 128, 64], 128, 7168, 1024)])
+def test_fp4_masked_matches_oracle(orc, masked_m, max_m, N, K):
+    E = len(masked_m)
+    base = inputs.masked_case(E, max_m, 8, K, seed=sum(masked_m), masked_m=masked_m)
+    b, sfb = _experts(E, N, K, seed=97)
+    sfa_p = binding.transform_sf(base.sfa.to(DEV), 1, max_m)
+    sfb_p = binding.transform_sf(sfb.contiguous().to(DEV), 1, N)
+    d = torch.full((E, max_m, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.dg_m_grouped_fp8_fp4_gemm_nt_masked(base.a.to(DEV), sfa_p, b.to(DEV), sfb_p, d,
+                                                base.masked_m.to(DEV), base.expected_m, status=status)
+    torch.cuda.synchronize()
+    clamped = [min(m, max_m) for m in masked_m]
+    flag = binding.DG_DEV_BAD_GROUP if any(m > max_m for m in masked_m) else 0
+    assert int(status.item()) == flag
+    init = bf16_bits(torch.full((E, max_m, N), 7.0, dtype=torch.bfloat16))
+    ref = orc.m_grouped_fp8_fp4_masked(u8(base.a), base.sfa.double().numpy(), b.numpy(), sfb.double().numpy(),
+                                       clamped, d_init=init)
+    got = bf16_bits(d)
+    for e in range(E):
+        m = clamped[e]
+        if m:
+            assert_close(got[e, :m], ref[e, :m], f"fp4 masked expert {e}")
+        assert np.array_equal(got[e, m:], ref[e, m:])
