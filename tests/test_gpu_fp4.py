@@ -120,10 +120,15 @@ def test_fp4_contiguous_matches_oracle(orc, m_per_expert, N, K):
     ref = orc.m_grouped_fp8_fp4_contiguous(u8(base.a), base.sfa.double().numpy(), b.numpy(),
                                            sfb.double().numpy(), base.grouped_layout.numpy(), d_init=init)
     got = bf16_bits(d)
-    valid = base.grouped_layout.numpy() >= 0
+    layout = base.grouped_layout.numpy()
+    valid = layout >= 0
     if valid.any():
         assert_close(got[valid], ref[valid], f"fp4 contiguous {m_per_expert}")
-    assert np.array_equal(got[~valid], ref[~valid])
+    # 128-row blocks that start with padding are left untouched (as in the FP8 layout;
+    # padding rows inside an expert's block are computed from their A rows)
+    for mb in range(len(layout) // 128):
+        if layout[mb * 128] < 0:
+            assert np.array_equal(got[mb * 128:(mb + 1) * 128], init[mb * 128:(mb + 1) * 128])
     # each expert's rows equal the dense FP8 x FP4 GEMM of those rows, bit for bit
     for e in range(E):
         rows = np.nonzero(base.grouped_layout.numpy() == e)[0]
