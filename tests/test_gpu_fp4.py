@@ -134,7 +134,7 @@ def test_fp4_contiguous_matches_oracle(orc, m_per_expert, N, K):
         rows = np.nonzero(base.grouped_layout.numpy() == e)[0]
         if len(rows) == 0:
             continue
-        ae = base.a[torch.from_numpy(rows)]
+        ae = base.a.view(torch.uint8)[torch.from_numpy(rows)].view(torch.float8_e4m3fn)
         de = torch.empty(len(rows), N, dtype=torch.bfloat16, device=DEV)
         binding.dg_fp8_fp4_gemm_nt(ae.to(DEV), binding.transform_sf(base.sfa[torch.from_numpy(rows)].to(DEV), 1,
                                                                     len(rows)),
