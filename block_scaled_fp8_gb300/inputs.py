@@ -6,7 +6,7 @@ plays the upstream quantiser that the pages leave to the caller ("DeepGEMM
 does not cast; it consumes already-quantised FP8 tensors and their scales",
 PaperTrace DeepGEMM §1.1), on CPU with a seeded ``torch.Generator``.
 
-Quantisation recipe (one reading, stated in the design notes):
+Quantisation recipe (one reading of the pages):
   * activations: one FP32 scale per 1x128 K-group of each row; weights: one
     per 128x128 block (PaperTrace DeepGEMM §1.1);
   * scale s = 2^ceil(log2(amax/448)), i.e. absmax/448 rounded up to a power of

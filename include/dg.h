@@ -53,7 +53,7 @@ typedef enum {
     DG_ERR_INVALID_ARG = 1,   /* a size, pointer or enum value is out of range */
     DG_ERR_ALIGNMENT = 2,     /* a pointer or leading dimension breaks the 16-byte rules */
     DG_ERR_LAYOUT = 3,        /* a scale layout does not match the contract */
-    DG_ERR_UNSUPPORTED = 4,   /* valid request outside what this build implements */
+    DG_ERR_UNSUPPORTED = 4,   /* valid request outside what the library implements */
     DG_ERR_CUDA = 5,          /* a CUDA runtime call failed (launch, attribute, device) */
     DG_ERR_TIMEOUT = 6,       /* used by helpers that read back the device status */
     DG_ERR_INEXACT_SCALE = 7, /* idem */

@@ -21,7 +21,7 @@
  * D = C + A @ B^T with 1x128 (A) and 128x128 (B) scales [P1 1.1, P2 13.3,
  * P3]; the two-level promotion of [P1 2.2] is the same sum regrouped.
  *
- * Readings of points the pages leave open (each listed in the design notes):
+ * Readings of points the pages leave open:
  *   - "FP8 e4m3" is the OCP E4M3 "fn" flavour (no infinities, S.1111.111 = NaN,
  *     max 448), the torch.float8_e4m3fn type the pages' example code uses [P2 13.11].
  *   - scale groups are fixed at 128 along K and, for B, 128 along N; the group
@@ -226,7 +226,7 @@ static double dot_element(int K, const uint8_t *arow, const double *sarow, const
 }
 
 /*
- * Full GEMM with FP32 C and D (the survey's FP32-output row; same sum as
+ * Full GEMM with FP32 C and D (the FP32-output form; same sum as
  * orc_gemm_nt): D[m][n] = fp32_rne(C[m][n] + sum), the sum in fp64 starting
  * from C (0 if C is NULL), one rounding to FP32 (C's double -> float
  * conversion rounds to nearest even).
