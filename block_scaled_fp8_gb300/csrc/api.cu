@@ -305,7 +305,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     // FP32 D: the caller sets d_f32 (and c_f32 for an FP32 C) before the call
     const bool f32 = p.d_f32 != nullptr;
     const bool with_c = f32 ? p.c_f32 != nullptr : p.c != nullptr;
-    const int lay = p.layout;   // MN-major operands: bit 0 A, bit 1 B
+    const int lay = p.layout;   // bit 0 A MN-major, bit 1 B MN-major, bit 2 B FP4
     KernelInfo info;
     if (bn == 0 || !get_bs2_kernel_info(bn, with_c, mp, &info, f32, lay)) return DG_ERR_UNSUPPORTED;
     const int pairs = usable_pairs(bn, with_c, mp, num_sms, f32, lay);

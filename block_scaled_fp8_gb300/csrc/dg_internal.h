@@ -47,7 +47,8 @@ struct GemmParams {
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
-    int layout;          // operand layouts: bit 0 A MN-major ([K][M]), bit 1 B MN-major ([K][N])
+    int layout;          // operand layouts: bit 0 A MN-major ([K][M]), bit 1 B MN-major ([K][N]),
+                         // bit 2 B FP4 (E2M1, one scale per 32 K)
     // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the
     // block-scaled kernels' scale warps read them with cp.async
     const uint32_t *sfa_words;

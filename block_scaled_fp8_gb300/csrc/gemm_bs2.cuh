@@ -1,5 +1,6 @@
 // Block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2): dense, contiguous
-// grouped and masked grouped layouts.
+// grouped (per-row expert ids or PSUM offsets), masked grouped and K-grouped
+// layouts; K-major or M/N-major operands; FP8 or FP4 (E2M1) B; bf16 or FP32 D.
 //
 // Same method as the single-CTA kernel (gemm_bs.cuh; "02 · DeepGEMM 技术解析"
 // §2-§4, "DeepSeek V4 源码剖析 第13章" §13.3): per output tile the block-scaled
@@ -393,7 +394,8 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
 }
 
 // LAY: operand layouts, bit 0 = A MN-major (stored [K][M]), bit 1 = B MN-major
-// (stored [K][N]); 0 is the NT layout (both K-major).  An MN-major operand's
+// (stored [K][N]), bit 2 = B is FP4 (E2M1, K-major, one scale per 32 K); 0 is
+// the NT layout (both K-major FP8).  An MN-major operand's
 // stage is a TMA box of 128 MN-bytes x 128 K-rows with 128-byte swizzle: one
 // swizzle atom along MN (MP=256; an MN-major B half of BN/2 <= 128 columns,
 // the rest of the atom unread), 8-row groups 1024 bytes apart, and a 32-K step
