@@ -32,9 +32,11 @@
  *    laid out MN-major: word (row i, slice p) at p*align4(mn) + i, batch
  *    stride psf_k*align4(mn) (PaperTrace §3.1).  B's packed scales are one row
  *    per N index (the 128x128 block scale broadcast along N, §3.2).
- *  - Operand preconditions: 16-byte aligned base pointers; K % 16 == 0;
- *    lda, ldb (in elements = bytes) multiples of 16; N % 8 == 0 and ldc, ldd
- *    (bf16 elements) multiples of 8.
+ *  - Operand preconditions, unless a call states its own: 16-byte aligned
+ *    base pointers; K % 16 == 0; lda, ldb (in elements = bytes) multiples of
+ *    16; N % 8 == 0 and ldc, ldd (bf16 elements) multiples of 8.  (FP4
+ *    weights, M/N-contiguous operands and FP32 outputs have their own rules,
+ *    given with their calls.)
  *  - No split-K: each output element is reduced by one CTA in a fixed K
  *    order, so a row's result does not depend on M or on the other rows of
  *    the batch (batch invariance, §13.1).
