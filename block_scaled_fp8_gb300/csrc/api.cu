@@ -768,10 +768,11 @@ dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fm
                           stream);
 }
 
-// FP8 x FP4: 256-row CTA pairs; the column count that fills the SMs best, of
-// 128 and 256 without C (one accumulator at 256) and 128 and 192 with C.
+// FP8 x FP4: 256-row CTA pairs; without C the column count that fills the SMs
+// best, of 128 and 256 (one accumulator at 256); with C, 128.
 static int choose_fp4_block_n(int64_t m_units, int n, int num_sms, bool with_c) {
-    const int cands[2] = {128, with_c ? 192 : 256};
+    if (with_c) return 128;
+    const int cands[2] = {128, 256};
     const int pairs = num_sms / 2;
     double best = -1.0;
     int best_bn = 128;
@@ -830,7 +831,7 @@ dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const 
         // M <= 128: 128-row pairs (each CTA loads 64 rows of A), the widest tile that
         // still gives most pairs a tile, as the weight stream from HBM sets the time
         int bn = 32;
-        for (int cand : {128, 96, 64})
+        for (int cand : {128, 96})
             if (cdiv64(n, cand) * 10 >= static_cast<int64_t>(sms / 2) * 9) {
                 bn = cand;
                 break;

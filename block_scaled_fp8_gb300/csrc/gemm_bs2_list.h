@@ -24,11 +24,10 @@
     X(224, true, 256, true, 3)
 
 // FP8 x FP4 (layout bit 2: B is E2M1 with one scale per 32 K): 256-row pairs with
-// 128 or 256 columns without C, 128 or 192 (two accumulators) with C; 128-row pairs
-// (M <= 128, no C) with 32 to 128 columns
+// 128 or 256 columns without C, 128 with C; 128-row pairs (M <= 128, no C) with 32,
+// 96 or 128 columns
 #define DG_BS2_LIST_FP4(X)                                                                         \
     X(256, false, 256, false, 4) X(128, false, 256, false, 4) X(128, true, 256, false, 4)          \
-    X(192, true, 256, false, 4) X(32, false, 128, false, 4) X(64, false, 128, false, 4)            \
-    X(96, false, 128, false, 4) X(128, false, 128, false, 4)
+    X(32, false, 128, false, 4) X(96, false, 128, false, 4) X(128, false, 128, false, 4)
 
 #define DG_BS2_LIST(X) DG_BS2_LIST_BF16(X) DG_BS2_LIST_F32(X) DG_BS2_LIST_MN(X) DG_BS2_LIST_FP4(X)
