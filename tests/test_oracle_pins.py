@@ -764,3 +764,44 @@ def test_m_grouped_fp4_oracles_bruteforce(orc):
                                       d_init=np.full((3, 5, N), 0x7FC1, dtype=np.uint16))
     assert np.array_equal(dm[0], d[0:5]) and np.array_equal(dm[1, :3], d[8:11])
     assert np.all(dm[1, 3:] == 0x7FC1) and np.all(dm[2] == 0x7FC1)
+
+
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt"])
+def test_gemm_layouts_integer_exact_matmul(orc, layout):
+    """Integer codes and power-of-two scales make every sum exact: the layout
+    oracle must equal bf16_rne of the float64 matmul op(A) op(B) of the decoded
+    stored operands, at a size (96 x 160 x 384) that spans several scale blocks."""
+    M, N, K = 96, 160, 384
+    case = inputs.integer_exact_case(M, N, K, seed=84)
+    a_mk = case.a.view(torch.uint8).numpy()
+    b_nk = case.b.view(torch.uint8).numpy()
+    a = np.ascontiguousarray(a_mk.T) if layout[0] == "t" else a_mk
+    b = np.ascontiguousarray(b_nk.T) if layout[1] == "n" else b_nk
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(N) // 128]
+    A = _decode_codes_torch(torch.from_numpy(a))
+    B = _decode_codes_torch(torch.from_numpy(b))
+    A_mk = (A.T if layout[0] == "t" else A) * np.repeat(sa, 128, axis=1)[:, :K]
+    B_kn = (B if layout[1] == "n" else B.T) * np.repeat(sb_rows, 128, axis=1)[:, :K].T
+    exact = A_mk @ B_kn
+    got = orc.gemm(layout, a, sa, b, sb_rows)
+    want = np.array([[_bf16_nearest_bruteforce(Fraction(float(v))) for v in row] for row in exact],
+                    dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_fp8_fp4_matches_float64_matmul(orc):
+    """At 64 x 96 x 512 the decoded products of the seeded case span under 40
+    bits, so any order of fp64 summation is exact: the FP4 oracle must equal
+    bf16_rne of numpy's float64 matmul of the scale-expanded operands."""
+    M, N, K = 64, 96, 512
+    case = inputs.fp4_case(M, N, K, seed=85)
+    a = case.a.view(torch.uint8).numpy()
+    A = _decode_codes_torch(case.a.view(torch.uint8)) * np.repeat(case.sfa.double().numpy(), 128, axis=1)
+    codes = np.stack([case.b.numpy() & 0xF, case.b.numpy() >> 4], axis=-1).reshape(N, K)
+    B = np.array(E2M1_TEXTBOOK)[codes] * np.repeat(case.sfb.double().numpy(), 32, axis=1)
+    exact = A @ B.T
+    got = orc.gemm_fp8_fp4_nt(a, case.sfa.double().numpy(), case.b.numpy(), case.sfb.double().numpy())
+    want = np.array([[_bf16_nearest_bruteforce(Fraction(float(v))) for v in row] for row in exact],
+                    dtype=np.uint16)
+    assert np.array_equal(got, want)
