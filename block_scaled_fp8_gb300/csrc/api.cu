@@ -169,32 +169,6 @@ struct BsOperands {
     void *d;        int64_t ldd;  uint64_t d_rows;
 };
 
-// Co-resident clusters per (BLOCK_N, C, cluster size), cached per device.
-int cached_max_clusters(int bn, bool with_c, int cluster) {
-    static std::mutex mu;
-    static int cache[kMaxDevices][2][257][9];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn > 256 ||
-        cluster > 8)
-        return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][bn][cluster];
-    if (v == 0) v = bs_max_active_clusters(bn, with_c, cluster);
-    return v;
-}
-
-// CTAs per cluster sharing the A tile.  DG_CLUSTER_SIZE (1, 2, 4 or 8)
-// overrides the default of 1 (A is loaded by every CTA).
-int choose_cluster(int64_t num_n_blocks) {
-    static const int env = [] {
-        const char *e = std::getenv("DG_CLUSTER_SIZE");
-        return e ? std::atoi(e) : 0;
-    }();
-    int c = (env == 1 || env == 2 || env == 4 || env == 8) ? env : 1;
-    while (c > 1 && num_n_blocks < c) c >>= 1;
-    return c;
-}
-
 // 256-row CTA pairs (cta_group::2) unless DG_DEBUG_SINGLE_CTA is set: dense
 // problems with more than one 128-row block; contiguous layouts of at most
 // kMaxPairPrefix m-pairs (and fewer than 2^15 experts); masked layouts of at
@@ -362,8 +336,6 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     if (p.mode == kModeDense || p.mode == kModeContiguous) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
-    p.cluster = 2;
-    p.num_n_groups = p.num_n_blocks;
     p.group_m = 8;
     if (f32) p.d_f32 = static_cast<float *>(o.d);
     else p.d = static_cast<uint16_t *>(o.d);
@@ -406,29 +378,18 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     }
     KernelInfo info;
     if (!get_bs_kernel_info(bn, with_c, &info)) return DG_ERR_UNSUPPORTED;
-    int cluster = choose_cluster(cdiv64(p.n, bn));
-    int max_clusters = num_sms;
-    if (cluster > 1) {
-        max_clusters = cached_max_clusters(bn, with_c, cluster);
-        if (max_clusters <= 0) {
-            cluster = 1;
-            max_clusters = num_sms;
-        }
-        if (max_clusters * cluster > num_sms) max_clusters = num_sms / cluster;
-    }
     TensorMaps maps;
     const int k = p.k;
     bool ok = true;
-    // K a multiple of 128 and no A multicast: one 3-D load per operand fills a ring slot
-    p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1 && cluster == 1) ? 1 : 0;
+    // K a multiple of 128: one 3-D load per operand fills a ring slot
+    p.ab_3d = (k % kBlockK == 0 && info.group_kb > 1) ? 1 : 0;
     if (p.ab_3d) {
         const uint64_t kblocks = static_cast<uint64_t>(k / kBlockK);
         ok &= encode_kblocked_3d(&maps.a, o.a, o.a_rows, o.lda, kblocks, kBlockM, info.group_kb);
         ok &= encode_kblocked_3d(&maps.b, o.b, o.b_rows, o.ldb, kblocks, bn, info.group_kb);
     } else {
-        // each CTA of a cluster loads (and multicasts) kBlockM / cluster rows of A
         ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.a, k, o.a_rows, o.lda, kBlockK,
-                        kBlockM / cluster, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                        kBlockM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         ok &= encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, o.b, k, o.b_rows, o.ldb, kBlockK, bn,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
@@ -438,8 +399,6 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     set_scale_words(p, o);
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(k, kBlockK));
-    p.cluster = cluster;
-    p.num_n_groups = static_cast<int>(cdiv64(p.num_n_blocks, cluster));
     p.group_m = 8;
     p.d = static_cast<uint16_t *>(o.d);
     p.ldd = o.ldd;
@@ -447,13 +406,11 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
     uint32_t dbg = g_debug_flags.load();
     if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));
     p.debug_flags = dbg;
-    const int64_t cluster_tiles = max_tiles_per_n_block * p.num_n_groups;
-    const int64_t clusters = cluster_tiles < max_clusters ? (cluster_tiles < 1 ? 1 : cluster_tiles)
-                                                          : max_clusters;
-    const int grid = static_cast<int>(clusters * cluster);
+    const int64_t tiles = max_tiles_per_n_block * p.num_n_blocks;
+    const int grid = static_cast<int>(tiles < num_sms ? (tiles < 1 ? 1 : tiles) : num_sms);
     if ((dbg & DG_DEBUG_PRINT_CONFIGS) || std::getenv("DG_PRINT_CONFIGS"))
-        std::fprintf(stderr, "[dg] mode=%d rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d cluster=%d grid=%d\n",
-                     p.mode, p.rows, p.n, k, kBlockM, bn, info.stages, info.smem_bytes, cluster, grid);
+        std::fprintf(stderr, "[dg] mode=%d rows=%d n=%d k=%d -> BLOCK_M=%d BLOCK_N=%d stages=%d smem=%d grid=%d\n",
+                     p.mode, p.rows, p.n, k, kBlockM, bn, info.stages, info.smem_bytes, grid);
     g_last_config[0] = kBlockM;
     g_last_config[1] = bn;
     g_last_config[2] = info.stages;
@@ -495,8 +452,6 @@ dg_status launch_promotion(GemmParams &p, const void *a, int64_t lda, const void
     p.num_m_blocks = static_cast<int>(m_blocks);
     p.num_n_blocks = static_cast<int>(cdiv64(p.n, bn));
     p.num_k_blocks = static_cast<int>(cdiv64(p.k, kBlockK));
-    p.cluster = 1;
-    p.num_n_groups = p.num_n_blocks;
     p.group_m = 8;
     p.d = static_cast<uint16_t *>(d);
     p.ldd = ldd;

@@ -28,8 +28,6 @@ struct GemmParams {
     int num_m_blocks;    // blocks of 128 rows (dense/contiguous: over all rows; masked: per expert, max)
     int num_n_blocks;
     int num_k_blocks;
-    int cluster;         // CTAs per cluster along N (they share the A tile by TMA multicast)
-    int num_n_groups;    // ceil(num_n_blocks / cluster): n-block groups, one per cluster tile
     int num_groups;
     int group_m;         // tile-order group size along M (L2 reuse)
     const int32_t *grouped_layout;  // contiguous: expert id per row
@@ -81,8 +79,6 @@ struct KernelInfo {
 bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info);
 cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream);
-// Largest number of co-resident clusters of `cluster` CTAs for that kernel (0 on error).
-int bs_max_active_clusters(int block_n, bool with_c, int cluster);
 
 // CTA-pair (cta_group::2) block-scaled kernel family (the instantiations are
 // listed in gemm_bs2_list.h).  mp = rows of a pair tile: 256 or 128; f32 picks

@@ -90,28 +90,28 @@ struct BsConfig {
     static_assert(kNumBars * 8 + 16 <= 512, "barrier region");
 };
 
-// Walks the (tile, 4-K-block group) sequence of one cluster in scheduler order,
+// Walks the (tile, 4-K-block group) sequence of one CTA in scheduler order,
 // skipping tiles with nothing to compute; the scale warps run one to load and one
 // to copy.
 template <int BN>
 struct GroupCursor {
     const GemmParams *p;
     const int *prefix;
-    int t, j, num_tiles, num_clusters, rank, psf_k, groups_per_tile;
+    int t, j, num_tiles, num_ctas, psf_k, groups_per_tile;
     bool valid;
     Tile tile;
-    __device__ __forceinline__ void start(const GemmParams &params, const int *pre, int cluster_id,
-                                          int nclusters, int r, int ntiles, int psf) {
-        p = &params; prefix = pre; num_clusters = nclusters; rank = r; num_tiles = ntiles;
+    __device__ __forceinline__ void start(const GemmParams &params, const int *pre, int cta, int nctas,
+                                          int ntiles, int psf) {
+        p = &params; prefix = pre; num_ctas = nctas; num_tiles = ntiles;
         psf_k = psf; groups_per_tile = (params.num_k_blocks + 3) >> 2;
-        t = cluster_id - nclusters;
+        t = cta - nctas;
         next_tile();
     }
     __device__ __forceinline__ void next_tile() {
         j = 0;
         valid = false;
-        for (t += num_clusters; t < num_tiles; t += num_clusters)
-            if (get_tile<BN>(*p, prefix, t, rank, psf_k, tile, false)) { valid = true; return; }
+        for (t += num_ctas; t < num_tiles; t += num_ctas)
+            if (get_tile<BN>(*p, prefix, t, psf_k, tile, false)) { valid = true; return; }
     }
     __device__ __forceinline__ void next() {
         if (++j == groups_per_tile) next_tile();
@@ -155,24 +155,17 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     const uint32_t lane = threadIdx.x & 31;
     const int psf_k = (p.num_k_blocks + 3) >> 2;
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    // 1-D clusters along x: the CTAs of a cluster are consecutive blockIdx.x.
-    const int csize = p.cluster;
-    const int rank = csize > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int cluster_id = blockIdx.x / csize;
-    const int num_clusters = gridDim.x / csize;
-    const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
+    const int cta_id = blockIdx.x;
+    const int num_ctas = gridDim.x;
 
     if (warp == 0) {
         // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
-        // initialise them, each fencing its own inits.  Every CTA of a cluster frees
-        // an empty slot; both epilogue halves drain an accumulator.
+        // initialise them, each fencing its own inits.  Both epilogue halves drain an
+        // accumulator.
         const int num_bars = static_cast<int>(drain_bar + 1 + Cfg::kSfWarps - bars);  // <= Cfg::kNumBars
         for (int i = static_cast<int>(lane); i < num_bars; i += 32) {
             uint64_t *b = bars + i;
-            uint32_t count = 1;
-            if (b >= empty_bar && b < empty_bar + R) count = csize;
-            if (b >= tempty_bar && b < tempty_bar + NUM_ACC) count = Cfg::kEpiWarps;
-            mbar_init(b, count);
+            mbar_init(b, b >= tempty_bar && b < tempty_bar + NUM_ACC ? Cfg::kEpiWarps : 1);
         }
         if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
@@ -192,16 +185,15 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
     grid_launch_dependents();
     grid_dependency_wait();
     if (p.mode == kModeMasked) build_masked_prefix(p, prefix);
-    // Without a cluster the producer waits for nobody: it signals that the barriers
-    // are initialised and starts loading while the others wait for the TMEM
-    // allocation (and the masked prefix, which it then waits for too).
-    const bool producer_early = csize == 1 && p.mode != kModeMasked;
+    // The producer waits for nobody: it signals that the barriers are initialised
+    // and starts loading while the others wait for the TMEM allocation (and the
+    // masked prefix, which it then waits for too).
+    const bool producer_early = p.mode != kModeMasked;
     if (producer_early && warp == 0) {
         named_bar_arrive(1, Cfg::kThreads);
     } else {
         tc_fence_before_sync();
         named_bar_sync(1, Cfg::kThreads);
-        if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast
         tc_fence_after_sync();
     }
     const uint32_t tmem_base = warp != 0 ? *tmem_holder : 0u;
@@ -214,9 +206,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued = 0;
         bool drop = (p.debug_flags & DG_DEBUG_DROP_ONE_LOAD) && blockIdx.x == 0;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        for (int t = cta_id; t < num_tiles; t += num_ctas) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, lane == 0)) continue;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, lane == 0)) continue;
             for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += G) {
                 const int nk = p.num_k_blocks - kb0 < G ? p.num_k_blocks - kb0 : G;
                 if (!mbar_wait_warp(&empty_bar[slot], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
@@ -238,16 +230,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                         auto load_kb = [&](int j) {
                             const int kb = kb0 + j;
                             const int stage = slot * G + j;
-                            if (csize == 1) {
-                                tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[slot],
-                                            kb * kBlockK, tile.a_row0);
-                            } else {
-                                // this CTA's slice of the shared A tile, to every CTA of the cluster
-                                const int rows = kBlockM / csize;
-                                tma_load_2d_multicast(smem_a + stage * Cfg::kABytes + rank * rows * kBlockK,
-                                                      &tm_a, &full_bar[slot], kb * kBlockK,
-                                                      tile.a_row0 + rank * rows, cmask);
-                            }
+                            tma_load_2d(smem_a + stage * Cfg::kABytes, &tm_a, &full_bar[slot],
+                                        kb * kBlockK, tile.a_row0);
                             tma_load_2d(smem_b + stage * Cfg::kBBytes, &tm_b, &full_bar[slot],
                                         kb * kBlockK, tile.b_row0);
                         };
@@ -282,9 +266,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         const uint64_t a_desc_base = make_desc_kmajor_sw128(smem_u32(smem_a));
         const uint64_t b_desc_base = make_desc_kmajor_sw128(smem_u32(smem_b));
         constexpr uint32_t idesc_base = make_idesc_mxf8(kBlockM, BN, 0, 0);
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        for (int t = cta_id; t < num_tiles; t += num_ctas) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
             if (!mbar_wait_warp(&tempty_bar[acc], acc_phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto mma_done;
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + acc * BN;
@@ -323,8 +307,7 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
                     } else {
                         for (int j = 0; j < nk; ++j) mma_kb(j);
                     }
-                    if (csize == 1) tc_commit(&empty_bar[slot]);
-                    else tc_commit_multicast(&empty_bar[slot], cmask);
+                    tc_commit(&empty_bar[slot]);
                     // last K-block of the scale group: its TMEM slot is free once these MMAs finish
                     if (group_end) tc_commit(&sf_tfree_bar[tslot]);
                 }
@@ -356,8 +339,8 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         static_assert(NSF % NW == 0, "scale slots per warp");
         const int sw = static_cast<int>(warp) - Cfg::kSfWarp;
         GroupCursor<BN> lc, gc;   // next group to load, next group to copy
-        lc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
-        gc.start(p, prefix, cluster_id, num_clusters, rank, num_tiles, psf_k);
+        lc.start(p, prefix, cta_id, num_ctas, num_tiles, psf_k);
+        gc.start(p, prefix, cta_id, num_ctas, num_tiles, psf_k);
         for (int i = 0; i < sw; ++i) { lc.next(); gc.next(); }
         int gl = sw;              // index of lc's group
         // issues the loads of group gl, or an empty commit group past the last one;
@@ -438,9 +421,9 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
         uint32_t acc_phase = 0;
         uint32_t buf = 0;
         uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        for (int t = cta_id; t < num_tiles; t += num_ctas) {
             Tile tile;
-            if (!get_tile<BN>(p, prefix, t, rank, psf_k, tile, false)) continue;
+            if (!get_tile<BN>(p, prefix, t, psf_k, tile, false)) continue;
             const bool tile_has_columns = tile.n0 < p.n;  // false past the last n-block of a group
             const int local_row = quad * 32 + lane;
             const int row = tile.a_row0 + local_row;       // row in the 2-D view of D
@@ -545,8 +528,6 @@ __global__ void __launch_bounds__(BsConfig<BN>::kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    // no CTA may leave while a peer can still multicast into it or arrive on its barriers
-    if (csize > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
@@ -563,45 +544,18 @@ cudaError_t launch_bs_gemm_impl(const TensorMaps &maps, const GemmParams &p, int
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    // a programmatic dependent of the stream's previous grid; clusters along x for A multicast
+    // a programmatic dependent of the stream's previous grid
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = p.cluster > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.d, p);
-}
-
-// Largest number of clusters of `cluster` CTAs that can be resident at once.
-template <int BN, bool WITH_C>
-int max_active_clusters_impl(int cluster) {
-    using Cfg = BsConfig<BN>;
-    if (cudaFuncSetAttribute(dg_bs_gemm_kernel<BN, WITH_C>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
-        return 0;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(cluster);
-    cfg.blockDim = dim3(Cfg::kThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dg_bs_gemm_kernel<BN, WITH_C>, &cfg) != cudaSuccess) return 0;
-    return n;
+    return cudaLaunchKernelEx(&cfg, dg_bs_gemm_kernel<BN, WITH_C>, maps.a, maps.b, maps.d, p);
 }
 
 template <int BN>

@@ -3,19 +3,11 @@
 
 namespace dg {
 template cudaError_t launch_bs_gemm_impl<16, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<16, false>(int);
 template cudaError_t launch_bs_gemm_impl<16, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<16, true>(int);
 template cudaError_t launch_bs_gemm_impl<32, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<32, false>(int);
 template cudaError_t launch_bs_gemm_impl<32, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<32, true>(int);
 template cudaError_t launch_bs_gemm_impl<48, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<48, false>(int);
 template cudaError_t launch_bs_gemm_impl<48, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<48, true>(int);
 template cudaError_t launch_bs_gemm_impl<64, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<64, false>(int);
 template cudaError_t launch_bs_gemm_impl<64, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<64, true>(int);
 }  // namespace dg

@@ -3,15 +3,9 @@
 
 namespace dg {
 template cudaError_t launch_bs_gemm_impl<96, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<96, false>(int);
 template cudaError_t launch_bs_gemm_impl<96, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<96, true>(int);
 template cudaError_t launch_bs_gemm_impl<128, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<128, false>(int);
 template cudaError_t launch_bs_gemm_impl<128, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<128, true>(int);
 template cudaError_t launch_bs_gemm_impl<160, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<160, false>(int);
 template cudaError_t launch_bs_gemm_impl<160, true>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<160, true>(int);
 }  // namespace dg

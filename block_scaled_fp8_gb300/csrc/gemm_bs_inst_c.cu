@@ -3,7 +3,5 @@
 
 namespace dg {
 template cudaError_t launch_bs_gemm_impl<176, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<176, false>(int);
 template cudaError_t launch_bs_gemm_impl<192, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<192, false>(int);
 }  // namespace dg

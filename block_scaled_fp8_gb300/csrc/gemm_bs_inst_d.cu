@@ -3,7 +3,5 @@
 
 namespace dg {
 template cudaError_t launch_bs_gemm_impl<224, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<224, false>(int);
 template cudaError_t launch_bs_gemm_impl<256, false>(const TensorMaps &, const GemmParams &, int, cudaStream_t);
-template int max_active_clusters_impl<256, false>(int);
 }  // namespace dg

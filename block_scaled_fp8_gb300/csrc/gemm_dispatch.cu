@@ -74,32 +74,6 @@ bool get_bs_kernel_info(int block_n, bool with_c, KernelInfo *info) {
     }
 }
 
-#define DG_EXTERN(BN) \
-    extern template int max_active_clusters_impl<BN, false>(int);
-DG_BS_BLOCK_N_LIST(DG_EXTERN)
-#undef DG_EXTERN
-#define DG_EXTERN(BN) \
-    extern template int max_active_clusters_impl<BN, true>(int);
-DG_BS_BLOCK_N_LIST_C(DG_EXTERN)
-#undef DG_EXTERN
-
-int bs_max_active_clusters(int block_n, bool with_c, int cluster) {
-    if (with_c) {
-        switch (block_n) {
-#define DG_CASE(BN) case BN: return max_active_clusters_impl<BN, true>(cluster);
-            DG_BS_BLOCK_N_LIST_C(DG_CASE)
-#undef DG_CASE
-            default: return 0;
-        }
-    }
-    switch (block_n) {
-#define DG_CASE(BN) case BN: return max_active_clusters_impl<BN, false>(cluster);
-        DG_BS_BLOCK_N_LIST(DG_CASE)
-#undef DG_CASE
-        default: return 0;
-    }
-}
-
 cudaError_t launch_bs_gemm(int block_n, const TensorMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream) {
     if (p.c != nullptr) {

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(PromoteConfig<BN>::kThreads, 1)
             uint32_t issued = 0;
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
                 Tile tile;
-                get_tile<BN>(p, nullptr, t, 0, 0, tile, false);
+                get_tile<BN>(p, nullptr, t, 0, tile, false);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ctl, DG_DEV_TIMEOUT)) goto prod_done;
                     mbar_arrive_expect_tx(&full_bar[stage], Cfg::kTxBytes);
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(PromoteConfig<BN>::kThreads, 1)
         uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             Tile tile;
-            get_tile<BN>(p, nullptr, t, 0, 0, tile, false);
+            get_tile<BN>(p, nullptr, t, 0, tile, false);
             const int local_row = quad * 32 + lane;
             const int row = tile.a_row0 + local_row;
             const bool row_ok = row < p.rows;

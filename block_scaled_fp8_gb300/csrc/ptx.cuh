@@ -210,19 +210,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
-// The same box is written to the same shared-memory offset of every CTA in
-// `cta_mask` (cluster ranks), and completes bytes on the mbarrier at the same
-// offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cluster address `bar_cluster`).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
@@ -345,16 +332,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// As tc_commit, but arrives on the mbarrier at the same offset in every CTA of
-// `cta_mask` (cluster ranks).
-__device__ __forceinline__ void tc_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

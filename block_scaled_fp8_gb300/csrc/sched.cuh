@@ -1,16 +1,13 @@
-// Persistent tile scheduler shared by the GEMM kernels.
+// Persistent tile scheduler of the single-CTA GEMM kernels.
 //
-// Every cluster of `cluster` CTAs walks cluster-tile ids ct = cluster_id,
-// cluster_id + num_clusters, ... (the persistent loop of PaperTrace "02 ·
-// DeepGEMM 技术解析" §4.3).  A cluster tile is one 128-row m-block and a group of
-// `cluster` consecutive n-blocks; the CTA of rank r takes n-block
-// group*cluster + r, so the CTAs of a cluster share the A tile (loaded once
-// and multicast).  Cluster tiles map to (m-block, n-group) in groups of
-// `group_m` m-blocks so that clusters running at the same time share A and B
-// tiles through L2.  There is no split-K: one CTA owns every K-block of its
-// tile.  All roles of a CTA (and all CTAs of a cluster) call the scheduler with
-// the same ids and reach the same decisions, including skips, so they stay in
-// step without talking to each other.
+// Every CTA walks tile ids t = blockIdx.x, blockIdx.x + gridDim.x, ... (the
+// persistent loop of PaperTrace "02 · DeepGEMM 技术解析" §4.3).  A tile is one
+// 128-row m-block and one n-block.  Tiles map to (m-block, n-block) in groups of
+// `group_m` m-blocks so that CTAs running at the same time share A and B tiles
+// through L2.  There is no split-K: one CTA owns every K-block of its tile.  All
+// roles of a CTA call the scheduler with the same ids and reach the same
+// decisions, including skips, so they stay in step without talking to each
+// other.
 #pragma once
 
 #include "dg_internal.h"
@@ -42,7 +39,7 @@ __device__ __forceinline__ void build_masked_prefix(const GemmParams &p, int *pr
                 if (p.status) atomicOr(p.status, DG_DEV_BAD_GROUP);
                 mm = mm < 0 ? 0 : p.rows;
             }
-            acc += ceil_div_i(mm, kBlockM) * p.num_n_groups;
+            acc += ceil_div_i(mm, kBlockM) * p.num_n_blocks;
         }
         prefix[p.num_groups] = acc;
     }
@@ -50,17 +47,14 @@ __device__ __forceinline__ void build_masked_prefix(const GemmParams &p, int *pr
 
 __device__ __forceinline__ int total_tiles(const GemmParams &p, const int *prefix) {
     if (p.mode == kModeMasked) return prefix[p.num_groups];
-    return p.num_m_blocks * p.num_n_groups;
+    return p.num_m_blocks * p.num_n_blocks;
 }
 
-// Fills `tile` for cluster-tile id t (< total) and cluster rank `rank`.
-// Returns false when the tile is skipped (contiguous layout: a padding block
-// or an out-of-range expert); all CTAs of a cluster skip together.  The
-// n-block may lie past the last one (a partial final group): its loads read
-// zeros and nothing is stored.
+// Fills `tile` for tile id t (< total).  Returns false when the tile is skipped
+// (contiguous layout: a padding block or an out-of-range expert).
 template <int BN>
-__device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix, int t, int rank,
-                                         int psf_k, Tile &tile, bool report) {
+__device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix, int t, int psf_k,
+                                         Tile &tile, bool report) {
     int mb, ng, group = 0;
     if (p.mode == kModeMasked) {
         // find the expert: largest e with prefix[e] <= t
@@ -82,7 +76,7 @@ __device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix,
         int v = mm - mb * kBlockM;
         tile.valid_rows = v < kBlockM ? v : kBlockM;
     } else {
-        const int per_group = p.group_m * p.num_n_groups;
+        const int per_group = p.group_m * p.num_n_blocks;
         const int g = t / per_group;
         const int first_m = g * p.group_m;
         const int rem_m = p.num_m_blocks - first_m;
@@ -103,7 +97,7 @@ __device__ __forceinline__ bool get_tile(const GemmParams &p, const int *prefix,
             }
         }
     }
-    const int nb = ng * p.cluster + rank;
+    const int nb = ng;
     tile.group = group;
     tile.n0 = nb * BN;
     tile.b_row0 = group * p.n + nb * BN;

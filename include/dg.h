@@ -190,7 +190,10 @@ dg_status dg_fp8_gemm_tt(const void *a, int64_t lda, const void *sfa, int sfa_fm
  *        with dg_transform_sf(sfb_fp32 [n][k/32], 1, n, k/32, 1, n, ...).
  *   c    bf16 [m, ldc] or NULL (may equal d); d bf16 [m, ldd].
  *   k a multiple of 128 (DG_ERR_ALIGNMENT otherwise); k == 0 gives D = C.
- *   n, ldc, ldd multiples of 8.  Runs on 256-row CTA pairs.
+ *   n, ldc, ldd multiples of 8.  Runs on 256-row CTA pairs; with m <= 128 and
+ *   no C, on 128-row CTA pairs (BLOCK_N 32, 96 or 128) instead.  Row i of D is
+ *   the same bit for bit whatever m the call has (both tile forms sum each
+ *   element's K-blocks in the same order).
  */
 dg_status dg_fp8_fp4_gemm_nt(const void *a, int64_t lda, const void *sfa, const void *b, int64_t ldb,
                              const void *sfb, const void *c, int64_t ldc, void *d, int64_t ldd, int m, int n,
@@ -378,9 +381,7 @@ void dg_set_wait_timeout_ms(int ms);
 enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2, DG_DEBUG_SINGLE_CTA = 4, DG_DEBUG_WIDE_PAIR = 8 };
 /* Environment, read once per process (tuning and diagnostics only; results are
  * the same for every choice): DG_BLOCK_N forces the single-CTA kernel's tile
- * width, DG_PAIR_BLOCK_N the 256-row pair kernel's, DG_CLUSTER_SIZE (2, 4 or 8)
- * shares the A tile of single-CTA GEMMs across a cluster by TMA multicast, and
- * DG_PRINT_CONFIGS prints each GEMM's tile configuration to stderr.  A
+ * width, DG_PAIR_BLOCK_N the 256-row pair kernel's, and DG_PRINT_CONFIGS prints each GEMM's tile configuration to stderr.  A
  * DG_PAIR_BLOCK_N width that is not compiled in makes pair launches return
  * DG_ERR_UNSUPPORTED; a DG_BLOCK_N width that is not compiled in is ignored
  * (128 is used). */
