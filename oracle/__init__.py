@@ -340,6 +340,19 @@ def gemm_nt_f32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb_rows: np.ndarra
     return d
 
 
+def gemm_nt_f32_sampled(a, sa, b, sb_rows, rows, cols, c=None, nthreads: int = 0) -> np.ndarray:
+    """The elements (rows[i], cols[i]) of gemm_nt_f32, one by one, in its order:
+    the fp64 product sum (gemm_nt_sampled, summed from 0 in increasing k), then
+    the FP32 C added in fp64 (0 if c is None), rounded once to FP32.  Equals
+    gemm_nt_f32 at those elements bit for bit."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    _, pre = gemm_nt_sampled(a, sa, b, sb_rows, rows, cols, want_pre=True, nthreads=nthreads)
+    cv = (np.zeros(len(rows)) if c is None
+          else np.asarray(c, dtype=np.float32)[rows, cols].astype(np.float64))
+    return (cv + pre).astype(np.float32)
+
+
 def k_grouped_pack_sf(sf: np.ndarray, ks) -> np.ndarray:
     """Packed scales of the K-grouped GEMM (PaperTrace DeepGEMM §3.3).
 
@@ -380,7 +393,8 @@ def k_grouped_gemm_tn(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarr
     [K_total, N] (N contiguous, the "n" operand); sa: fp64 [K_total/128, M];
     sb: fp64 [K_total/128, N]; ks: group sizes, multiples of 128 (0 allowed);
     c: FP32 [E, M, N] (required, as the pages make C mandatory here).
-    fp64 sum started from C, rounded once to FP32.  Returns FP32 [E, M, N].
+    C plus the group's fp64 product sum (the products summed from 0 in increasing
+    k, then C added), rounded once to FP32.  Returns FP32 [E, M, N].
     """
     a, b = _u8(a), _u8(b)
     M, N = a.shape[1], b.shape[1]
@@ -403,11 +417,11 @@ def k_grouped_gemm_tn(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarr
 
 
 def k_grouped_gemm_tn_sampled(a, sa, b, sb, ks, c, es, ms, ns, nthreads: int = 0) -> np.ndarray:
-    """The elements (es[i], ms[i], ns[i]) of k_grouped_gemm_tn, one by one: the
-    group's fp64 sum (gemm_nt_sampled on the group's transposed slices), plus
-    C in fp64, rounded once to FP32.  (C is added after the products here, so
-    the fp64 rounding order differs from the full function's; the FP32 result
-    is the same except within an fp64 rounding of an FP32 tie.)"""
+    """The elements (es[i], ms[i], ns[i]) of k_grouped_gemm_tn, one by one, in
+    the full function's order: the group's fp64 product sum (gemm_nt_sampled on
+    the group's transposed slices, summed from 0 in increasing k), then C added
+    in fp64, rounded once to FP32.  The result equals the full function's bit
+    for bit."""
     a, b = _u8(a), _u8(b)
     es, ms, ns = (np.asarray(x, dtype=np.int64) for x in (es, ms, ns))
     out = np.empty(len(es), dtype=np.float32)
@@ -423,7 +437,7 @@ def k_grouped_gemm_tn_sampled(a, sa, b, sb, ks, c, es, ms, ns, nthreads: int = 0
                 _, pre = gemm_nt_sampled(np.ascontiguousarray(a[k0:k0 + k].T), np.ascontiguousarray(sa[s0:s1].T),
                                          np.ascontiguousarray(b[k0:k0 + k].T), np.ascontiguousarray(sb[s0:s1].T),
                                          ms[sel], ns[sel], want_pre=True, nthreads=nthreads)
-                out[sel] = (pre + cv).astype(np.float32)
+                out[sel] = (cv + pre).astype(np.float32)
         k0 += k
     return out
 

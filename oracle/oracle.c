@@ -227,9 +227,9 @@ static double dot_element(int K, const uint8_t *arow, const double *sarow, const
 
 /*
  * Full GEMM with FP32 C and D (the FP32-output form; same sum as
- * orc_gemm_nt): D[m][n] = fp32_rne(C[m][n] + sum), the sum in fp64 starting
- * from C (0 if C is NULL), one rounding to FP32 (C's double -> float
- * conversion rounds to nearest even).
+ * orc_gemm_nt): D[m][n] = fp32_rne(C[m][n] + sum), the products summed in
+ * fp64 from 0 in increasing k, then C added (0 if C is NULL), one rounding to
+ * FP32 (C's double -> float conversion rounds to nearest even).
  */
 void orc_gemm_nt_f32(int M, int N, int K, const uint8_t *A, int64_t lda, const double *sa,
                      const uint8_t *B, int64_t ldb, const double *sb, const float *C, int64_t ldc,

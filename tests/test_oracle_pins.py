@@ -541,6 +541,24 @@ def test_gemm_f32_rounds_once_to_fp32(orc):
     assert np.array_equal(got, pre.astype(np.float32))
 
 
+def test_gemm_f32_sampled_equals_full(orc):
+    """The sampled FP32 form takes the same fp64 steps in the same order as the
+    full one, so the same FP32 bits at every sampled element (with and without
+    C, over a ragged N that spans two 128-row B scale blocks)."""
+    case = inputs.dense_case(37, 200, 384, seed=12, b_scale_exp_range=(-8, 4))
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa = case.sfa.double().numpy()
+    sb_rows = case.sfb.double().numpy()[np.arange(200) // 128]
+    c = torch.randn(37, 200, generator=torch.Generator().manual_seed(8)).numpy()
+    rng = np.random.default_rng(1)
+    rows, cols = rng.integers(0, 37, 400), rng.integers(0, 200, 400)
+    for cc in (None, c):
+        full = orc.gemm_nt_f32(a, sa, b, sb_rows, c=cc)
+        got = orc.gemm_nt_f32_sampled(a, sa, b, sb_rows, rows, cols, c=cc)
+        assert np.array_equal(got.view(np.uint32), full[rows, cols].view(np.uint32))
+
+
 # ---------------------------------------------------------------- NN / TN / TT layouts
 
 @pytest.mark.parametrize("layout", ["nn", "tn", "tt", "nt"])
@@ -662,7 +680,8 @@ def test_k_grouped_sampled_equals_full(orc):
     es, ms, ns = rng.integers(0, 3, 300), rng.integers(0, 40, 300), rng.integers(0, 24, 300)
     got = orc.k_grouped_gemm_tn_sampled(a, sa, b, sb, case.ks, c, es, ms, ns)
     ref = full[es, ms, ns]
-    assert np.all(np.abs(got.astype(np.float64) - ref) <= 2.0 ** -23 * np.abs(ref))
+    # same fp64 order (products from 0, then C), so the same FP32 bits
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
 # ---------------------------------------------------------------- FP8 x FP4
