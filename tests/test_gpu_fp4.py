@@ -55,6 +55,28 @@ def test_fp4_matches_oracle(orc, M, N, K, with_c, pad):
     assert_close(bf16_bits(d), ref, f"fp4 {M}x{N}x{K}")
 
 
+def test_fp4_batch_invariance_bitwise():
+    """Rows [0, m) of a call with m rows equal the same rows of the m=4096 call
+    bit for bit, across the 128-row pair tiles (m <= 128) and the 256-row ones."""
+    M, N, K = 4096, 2112, 1536
+    case = inputs.fp4_case(M, N, K, seed=77)
+    a = case.a.to(DEV)
+    b = _b_device(case.b)
+    sfb = binding.transform_sf(case.sfb.to(DEV), 1, N)
+    d_full = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    binding.dg_fp8_fp4_gemm_nt(a, binding.transform_sf(case.sfa.to(DEV), 1, M), b, sfb, d_full)
+    seen = set()
+    for m in [1, 17, 128, 129, 1000]:
+        d = torch.empty(m, N, dtype=torch.bfloat16, device=DEV)
+        binding.dg_fp8_fp4_gemm_nt(a[:m], binding.transform_sf(case.sfa[:m].contiguous().to(DEV), 1, m), b,
+                                   sfb, d)
+        cfg = binding.last_config()
+        seen.add((cfg["block_m"], cfg["block_n"]))
+        torch.cuda.synchronize()
+        assert torch.equal(d, d_full[:m]), f"rows differ at m={m} ({cfg})"
+    assert {bm for bm, _ in seen} == {128, 256}, seen
+
+
 def test_fp4_equals_fp8_gemm_on_the_same_values():
     M, N, K = 512, 768, 1024
     case = inputs.fp4_case(M, N, K, seed=91)
