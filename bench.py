@@ -73,6 +73,60 @@ def load_traffic():
         return None
 
 
+def read_ncu_csv(path):
+    """Launches of an ncu --csv metrics log: a list of {"kernel": name, metric:
+    value in bytes / ns}, in capture order (ncu's own lines before the header
+    are skipped)."""
+    import csv
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9,
+             "ns": 1, "nsecond": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}
+    with open(path) as f:
+        lines = f.read().splitlines()
+    start = next(i for i, ln in enumerate(lines) if ln.startswith('"ID"'))
+    launches = {}
+    for row in csv.DictReader(lines[start:]):
+        rec = launches.setdefault(row["ID"], {"kernel": row["Kernel Name"]})
+        val = float(row["Metric Value"].replace(",", ""))
+        rec[row["Metric Name"]] = val * scale.get(row["Metric Unit"], 1)
+    return [launches[k] for k in sorted(launches, key=int)]
+
+
+def record_traffic(capture_dir, out_path, command):
+    """Writes the per-launch DRAM traffic record of the benchmark's six GEMMs
+    from one ncu capture per GEMM (capture_dir/traffic_M,N,K.csv, the captured
+    launch of `bench.py --case M,N,K`), stamped with the digest of the kernel
+    sources this tree holds (the tree that was captured)."""
+    from block_scaled_fp8_gb300.build import source_digest
+    per = {}
+    for (m, n, k) in SHAPES:
+        launches = read_ncu_csv(os.path.join(capture_dir, f"traffic_{m},{n},{k}.csv"))
+        if len(launches) != 1:
+            raise RuntimeError(f"{m}x{n}x{k}: expected one captured launch, got {len(launches)}")
+        x = launches[0]
+        per[f"{m}x{n}x{k}"] = {"kernel": x["kernel"].split("(")[0].replace("void ", ""),
+                               "bytes": int(x["dram__bytes_read.sum"] + x["dram__bytes_write.sum"]),
+                               "read": int(x["dram__bytes_read.sum"]), "write": int(x["dram__bytes_write.sum"]),
+                               "ncu_us": round(x["gpu__time_duration.sum"] / 1e3, 2),
+                               "algorithmic_bytes": gemm_bytes(m, n, k)}
+    mean = lambda keys: int(round(statistics.mean(per[k]["bytes"] for k in keys)))
+    big = [f"{m}x{n}x{k}" for (m, n, k) in SHAPES if m > 128]
+    small = [f"{m}x{n}x{k}" for (m, n, k) in SHAPES if m <= 128]
+    rec = {"what": "dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu capture per GEMM "
+                   "of the benchmark step",
+           "command": command,
+           "source_digest": source_digest(),
+           "m4096_mean_bytes_per_launch": mean(big),
+           "m128_mean_bytes_per_launch": mean(small),
+           "per_gemm": per,
+           "note": "m4096: the 256-row pair kernel's three launches; m128: the three M=128 GEMMs. "
+                   "Writes of D still in L2 when the kernel ends are not counted. The digest is "
+                   "computed by this writer from the comment-stripped kernel sources."}
+    with open(out_path, "w") as f:
+        json.dump(rec, f, indent=2)
+        f.write("\n")
+    return rec
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 10 ms; stop(t0, t1)
     keeps the samples whose nvidia-smi timestamp lies in the host wall-clock
@@ -500,6 +554,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_steps = min(20, max(3, args.steps // 2))
     e2e_ms, e2e_host_ms = e2e_pipelined(probs, e2e_steps, status, stream)
+    raw_copy = measure_pinned_copies(dev, stream)
 
     # ---------------- reductions over ranks (max time)
     total_ms, e2e_total_ms, total_t_ms = reduce_job_times([local_ms, e2e_ms, local_t_ms], world, dev)
@@ -572,7 +627,15 @@ def run_ours(args, rank, world, local_rank):
                     "pipeline": "per GEMM: copy A and packed scales in, dg_fp8_gemm_nt, copy D out; "
                                 "D out in two row halves on two streams; two device buffer sets",
                     "host_enqueue_ms_per_step": round(e2e_host_ms / e2e_steps, 3),
-                    "host_cpus": host_cpus or "unbound"},
+                    "host_cpus": host_cpus or "unbound",
+                    "raw_pinned_copy_gbs": raw_copy,
+                    "copy_bound_value": (round(step_flops / (max(h2d / raw_copy["h2d_concurrent"],
+                                                                  d2h / raw_copy["d2h_concurrent"]) / 1e9)
+                                               / 1e12, 2) if raw_copy else None),
+                    "copy_bound_note": "the TFLOP/s the step would reach if its copies in and out, "
+                                       "overlapped as in the pipeline, were the only cost: "
+                                       "flops / max(h2d bytes / H2D rate, d2h bytes / D2H rate) "
+                                       "at the concurrent rates measured in this run"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
@@ -733,6 +796,51 @@ def run_case(args):
                                    / (us * 1e-6) / 1e9, 1), "config": cfg}))
 
 
+def measure_pinned_copies(dev, stream, nbytes=256 * 1024 * 1024, reps=5):
+    """Raw copy rates (GB/s, best of `reps`) between pinned host memory and the
+    device in this process: host to device alone, device to host alone (two
+    halves on two streams, as the e2e pipeline copies D out), and both
+    directions at once (all three streams)."""
+    import torch
+    try:
+        h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        d_out = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        s_in, s_o = torch.cuda.Stream(), [torch.cuda.Stream(), torch.cuda.Stream()]
+        h = nbytes // 2
+
+        def timed(do_in, do_out):
+            best = None
+            for _ in range(reps):
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for s_ in [s_in] + s_o:
+                    s_.wait_event(e0)
+                if do_in:
+                    with torch.cuda.stream(s_in):
+                        d_in.copy_(h_in, non_blocking=True)
+                if do_out:
+                    for j, s_ in enumerate(s_o):
+                        with torch.cuda.stream(s_):
+                            h_out[j * h:(j + 1) * h].copy_(d_out[j * h:(j + 1) * h], non_blocking=True)
+                for s_ in [s_in] + s_o:
+                    stream.wait_stream(s_)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+            return nbytes / (best * 1e-3) / 1e9
+        h2d = timed(True, False)
+        d2h = timed(False, True)
+        both = timed(True, True)   # each direction moved nbytes in that time
+        return {"h2d": round(h2d, 1), "d2h": round(d2h, 1), "h2d_concurrent": round(both, 1),
+                "d2h_concurrent": round(both, 1), "bytes": nbytes}
+    except Exception:
+        return None
+
+
 def e2e_pipelined(probs, steps, status, stream):
     """End-to-end steps through the public API: every GEMM of every step copies
     its activations and their packed scales in from pinned host memory, runs,
@@ -803,7 +911,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-traffic", default=None, metavar="DIR",
+                    help="write the DRAM traffic record from DIR/traffic_M,N,K.csv (one ncu capture per "
+                         "GEMM of the step) to --traffic-out, stamped with this tree's source digest")
+    ap.add_argument("--traffic-out", default=os.path.join(ROOT, "profiles", "gemm_dram_traffic.json"))
+    ap.add_argument("--traffic-command", default="", help="the capture command, stored in the record")
     args = ap.parse_args()
+    if args.record_traffic:
+        rec = record_traffic(args.record_traffic, args.traffic_out, args.traffic_command)
+        print(json.dumps({"traffic_record": args.traffic_out, "source_digest": rec["source_digest"]}))
+        return
     if args.warmup < 3 and not (args.case or args.case_k_grouped):
         ap.error("--warmup must be >= 3")
 

@@ -37,16 +37,52 @@ def _deps():
         os.path.join(CSRC, "*.h")) + [os.path.join(HERE, "..", "include", "dg.h"), __file__]
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, with runs of blanks outside
+    literals collapsed to one, trailing blanks and blank lines dropped: what the
+    compiler sees, for digests that a comment-only edit leaves unchanged.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(src)
+
+    def blank():
+        if out and out[-1] not in (" ", "\n"):
+            out.append(" ")
+    while i < n:
+        ch = src[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and src[j] != ch:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            blank()
+            i = n if j < 0 else j + 2
+        elif ch in " \t":
+            blank()
+            i += 1
+        else:
+            out.append(ch)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).split("\n"))
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_digest() -> str:
-    """sha256 over the kernel and ABI sources (identifies the compiled kernels)."""
+    """sha256 over the kernel and ABI sources with their comments stripped
+    (identifies the compiled kernels; comment-only edits keep it)."""
     import hashlib
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                    + glob.glob(os.path.join(CSRC, "*.h")))
     for f in files + [os.path.join(HERE, "..", "include", "dg.h")]:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
