@@ -331,6 +331,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
                         32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (!ok) return DG_ERR_CUDA;
     set_scale_words(p, o);
+    p.c_v8 = (p.c != nullptr && (reinterpret_cast<uintptr_t>(p.c) & 31u) == 0 && p.ldc % 16 == 0) ? 1 : 0;
     // dense and contiguous: the pair kernel counts mp-row m-units (masked: unused;
     // K-grouped: the caller sets the m-units of one group)
     if (p.mode == kModeDense || p.mode == kModeContiguous) p.num_m_blocks = static_cast<int>(cdiv64(p.rows, mp));

@@ -99,10 +99,22 @@ struct Bs2Config {
     static constexpr int kEpiChunk = 16;
     static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
-    static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * kEpiChunk * 2;
     static constexpr int kSmemLimit = 232448;
     static constexpr int kPrefixBytes = (2 * kMaxPairPrefix + 1) * 4;  // grouped-layout unit prefix + info
-    static constexpr int kFixedBytes = 1024 + kStagingBytes + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
+    // Output staging: kStageBufs buffers of one 32-row x 32-byte store box per
+    // epilogue warp.  A buffer is rewritten once the TMA store issued from it
+    // kStageBufs chunks earlier has read it; the stores queue behind the operand
+    // loads in the TMA unit, so more buffers keep more stores in flight.  As many
+    // as fit (up to 4) without costing an operand stage.
+    static constexpr int kStageBufBytes = 32 * kEpiChunk * 2;
+    static constexpr int fixed_bytes(int bufs) {
+        return 1024 + kEpiWarps * bufs * kStageBufBytes + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
+    }
+    static constexpr int stages_by_smem(int bufs) { return (kSmemLimit - fixed_bytes(bufs)) / kStageBytes; }
+    static constexpr int stages_cap(int bufs) { return stages_by_smem(bufs) > 12 ? 12 : stages_by_smem(bufs); }
+    static constexpr int kStageBufs = stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2);
+    static constexpr int kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
+    static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
     static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
@@ -843,12 +855,16 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t buf = 0;
-        uint8_t *stage_out = smem_stage_out + ew * 2 * (32 * Cfg::kEpiChunk * 2);
+        uint8_t *stage_out = smem_stage_out + ew * Cfg::kStageBufs * Cfg::kStageBufBytes;
         // C (bf16) of one chunk of this thread's row; zero outside [rows, n)
         auto load_c = [&](const PairTile &tl, int j, uint32_t (&dst)[8]) {
             const int c = 2 * j + half;
             const int row = tl.d_row0 + row_off + lane;
             const int col0 = tl.n0 + col_off + c * Cfg::kEpiChunk;
+            if (p.c_v8 && c < Cfg::kNumChunks && row < p.rows && col0 + 16 <= p.n) {
+                ld_global_cg_v8(p.c + static_cast<int64_t>(row) * p.ldc + col0, dst);
+                return;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint4 cv = make_uint4(0u, 0u, 0u, 0u);
@@ -861,9 +877,21 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 dst[4 * h + 3] = cv.w;
             }
         };
-        // With C, each chunk's registers are refilled with the next tile's C as soon
-        // as this tile's chunk is stored, so the C loads run a whole tile ahead.
+        // bf16 C: a tile's C rows are fetched into L2 a tile ahead, one bulk prefetch
+        // of the whole row segment per row (long, contiguous DRAM reads), and loaded
+        // into registers from L2 just before the tile's epilogue.  Loading a whole
+        // tile ahead into registers instead kept thousands of scattered row loads in
+        // flight during the stores, which then queued behind them.
         uint32_t cpk[(WITH_C && !F32) ? Cfg::kChunksPerWarp : 1][8];
+        auto prefetch_c = [&](const PairTile &tl) {
+            if (half != 0 || tl.valid_rows == 0) return;
+            const int row = tl.d_row0 + row_off + static_cast<int>(lane);
+            const int cols = p.n - (tl.n0 + col_off) < (MP == 256 ? BN : BN / 2) ? p.n - (tl.n0 + col_off)
+                                                                                  : (MP == 256 ? BN : BN / 2);
+            if (row < p.rows && cols > 0)
+                prefetch_l2_bulk(p.c + static_cast<int64_t>(row) * p.ldc + tl.n0 + col_off,
+                                 static_cast<uint32_t>(cols) * 2u);
+        };
         // FP32 C: a ring of kCDepth chunks of this thread's row; chunk j of every tile
         // lives in slot j % kCDepth.  Once chunk j is added, its slot is refilled with
         // chunk j + kCDepth of the tile, or, past the tile's last chunk, with chunk
@@ -886,10 +914,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         PairTile tile;
         if (pair_id < num_tiles) {
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
-            if constexpr (WITH_C && !F32) {
-#pragma unroll
-                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
-            }
+            if constexpr (WITH_C && !F32) prefetch_c(tile);
             if constexpr (WITH_C && F32) {
 #pragma unroll
                 for (int j = 0; j < kCDepth; ++j) load_c32(tile, j, cring[j]);
@@ -921,8 +946,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     }
                     return;
                 }
-                uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
-                if (lane == 0) bulk_wait_group_read<1>();
+                uint8_t *sbuf = stage_out + buf * Cfg::kStageBufBytes;
+                if (lane == 0) bulk_wait_group_read<Cfg::kStageBufs - 1>();
                 __syncwarp();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -935,10 +960,25 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     tma_store_2d(&tm_d, sbuf, col0, tile.d_row0 + row_off);
                     bulk_commit_group();
                 }
-                buf ^= 1;
+                buf = buf + 1 == Cfg::kStageBufs ? 0 : buf + 1;
             };
+            // bf16 C of this tile into registers (the first tile's once its accumulator is
+            // complete, so that its loads do not compete with the first operand loads)
+            if constexpr (WITH_C && !F32) {
+                if (t != pair_id) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
+                }
+            }
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
             tc_fence_after_sync();
+            if constexpr (WITH_C && !F32) {
+                if (t == pair_id) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
+                }
+                if (has_next) prefetch_c(next_tile);
+            }
             if constexpr (F32) {
                 // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> two
                 // 8-column FP32 boxes through the staging buffers; the accumulator is
@@ -998,8 +1038,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         if (col0 + 8 * part >= p.n) break;
-                        uint8_t *sbuf = stage_out + buf * (32 * Cfg::kEpiChunk * 2);
-                        if (lane == 0) bulk_wait_group_read<1>();
+                        uint8_t *sbuf = stage_out + buf * Cfg::kStageBufBytes;
+                        if (lane == 0) bulk_wait_group_read<Cfg::kStageBufs - 1>();
                         __syncwarp();
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -1014,7 +1054,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
                             bulk_commit_group();
                         }
-                        buf ^= 1;
+                        buf = buf + 1 == Cfg::kStageBufs ? 0 : buf + 1;
                     }
                 }
                 tc_fence_before_sync();
@@ -1022,9 +1062,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
             } else if constexpr (WITH_C) {
-                // C is held as bf16 (prefetched above), so the FP32 accumulator stays in
-                // TMEM until each chunk is converted and stored; the other accumulator
-                // keeps the MMAs busy meanwhile
+                // each chunk's bf16(acc + C) overwrites that chunk's C registers; the
+                // accumulator is released once every chunk is read (the MMAs of the tile
+                // after next need it), and only then are the chunks stored
 #pragma unroll
                 for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
                     uint32_t v[2][16];
@@ -1041,22 +1081,24 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         const int c = 2 * j + half;
                         if (j >= Cfg::kChunksPerWarp || c >= Cfg::kNumChunks) continue;
                         reg_fence16(v[u]);
-                        uint32_t o[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float lo = __uint_as_float(v[u][2 * i]) + __uint_as_float(cpk[j][i] << 16);
                             const float hi = __uint_as_float(v[u][2 * i + 1]) + __uint_as_float(cpk[j][i] & 0xFFFF0000u);
                             __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                            o[i] = *reinterpret_cast<uint32_t *>(&b2);
+                            cpk[j][i] = *reinterpret_cast<uint32_t *>(&b2);
                         }
-                        store_chunk(o, c);
-                        if (has_next) load_c(next_tile, j, cpk[j]);
                     }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+#pragma unroll
+                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
+                    const int c = 2 * j + half;
+                    if (c < Cfg::kNumChunks) store_chunk(cpk[j], c);
+                }
             } else {
                 // the whole row segment to registers, release the accumulator, then store
                 uint32_t out[Cfg::kChunksPerWarp][8];

@@ -197,6 +197,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ----------------------------------------------------------------- TMA
 
+// Fetch [p, p + bytes) from global memory into L2 (no data returned; p and bytes
+// multiples of 16).  One request for a whole row segment keeps the DRAM reads
+// long and contiguous.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
+// 32-byte global load (p 32-byte aligned), cached at L2 only.
+__device__ __forceinline__ void ld_global_cg_v8(const void *p, uint32_t (&r)[8]) {
+    asm volatile("ld.global.cg.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
