@@ -245,6 +245,12 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
 // max(bytes a CTA loads / 60, MMA cycles) times the waves of tiles.  Returns
 // the pair kernel's BLOCK_N, or 0 to keep the single-CTA kernel.
 int choose_skinny_pair_block_n(const GemmParams &p, int bn1, int num_sms) {
+    static const int forced = [] {
+        const char *e = std::getenv("DG_SKINNY_PAIR_BLOCK_N");
+        return e ? std::atoi(e) : 0;
+    }();
+    if (forced < 0) return 0;
+    if (forced > 0) return usable_pairs(forced, false, 128, num_sms) > 0 ? forced : 0;
     auto cost = [](int64_t waves, double bytes, double mma) {
         return static_cast<double>(waves) * (bytes / 60.0 > mma ? bytes / 60.0 : mma);
     };

@@ -100,7 +100,14 @@ struct Bs2Config {
     static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
     static constexpr int kSmemLimit = 232448;
-    static constexpr int kPrefixBytes = (2 * kMaxPairPrefix + 1) * 4;  // grouped-layout unit prefix + info
+    // grouped-layout unit prefix + info (the 128-row pairs run dense problems only)
+    static constexpr int kPrefixBytes = MP == 256 ? (2 * kMaxPairPrefix + 1) * 4 : 0;
+    // Operand stages: 256-row pairs keep up to 12 (slots of 4, 2 or 1 K-blocks, so
+    // the MMA warp waits and commits once per slot).  128-row pairs stream B from
+    // DRAM at a few bytes per MMA cycle, so what bounds them is the bytes in flight:
+    // up to 20 stages in slots of 2 K-blocks (a slot frees as soon as its two
+    // K-blocks' MMAs complete).
+    static constexpr int kMaxStages = MP == 256 ? 12 : 20;
     // Output staging: kStageBufs buffers of one 32-row x 32-byte store box per
     // epilogue warp.  A buffer is rewritten once the TMA store issued from it
     // kStageBufs chunks earlier has read it; the stores queue behind the operand
@@ -111,13 +118,16 @@ struct Bs2Config {
         return 1024 + kEpiWarps * bufs * kStageBufBytes + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
     }
     static constexpr int stages_by_smem(int bufs) { return (kSmemLimit - fixed_bytes(bufs)) / kStageBytes; }
-    static constexpr int stages_cap(int bufs) { return stages_by_smem(bufs) > 12 ? 12 : stages_by_smem(bufs); }
-    static constexpr int kStageBufs = stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2);
+    static constexpr int stages_cap(int bufs) {
+        return stages_by_smem(bufs) > kMaxStages ? kMaxStages : stages_by_smem(bufs);
+    }
+    static constexpr int kStageBufs =
+        MP == 128 ? 2 : (stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2));
     static constexpr int kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
     static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
-    static constexpr int kStagesCap = kStagesBySmem > 12 ? 12 : kStagesBySmem;
-    static constexpr int kGroupKb = kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1);
+    static constexpr int kStagesCap = kStagesBySmem > kMaxStages ? kMaxStages : kStagesBySmem;
+    static constexpr int kGroupKb = MP == 128 ? 2 : (kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1));
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;
     static constexpr int kNumAcc = (2 * kAccCols + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
@@ -488,7 +498,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     grid_launch_dependents();
     grid_dependency_wait();
     // (the scale ring is free until the roles start: PSUM segments go there)
-    if (p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo, reinterpret_cast<int *>(smem_sf));
+    if (MP == 256 && p.mode != kModeDense) build_pair_prefix(p, prefix, pinfo, reinterpret_cast<int *>(smem_sf));
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     if (warp == 1) {
@@ -503,7 +513,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     }
     const uint32_t tmem_base = warp != 0 ? *tmem_holder : 0u;
     const uint32_t sf_col0 = NUM_ACC * ACC;
-    const int num_units = pair_units(p, prefix);
+    const int num_units = MP == 128 ? p.num_m_blocks : pair_units(p, prefix);
     const int num_tiles = num_units * p.num_n_blocks;
 
     if (warp == 0) {

@@ -381,10 +381,13 @@ void dg_set_wait_timeout_ms(int ms);
 enum { DG_DEBUG_DROP_ONE_LOAD = 1, DG_DEBUG_PRINT_CONFIGS = 2, DG_DEBUG_SINGLE_CTA = 4, DG_DEBUG_WIDE_PAIR = 8 };
 /* Environment, read once per process (tuning and diagnostics only; results are
  * the same for every choice): DG_BLOCK_N forces the single-CTA kernel's tile
- * width, DG_PAIR_BLOCK_N the 256-row pair kernel's, and DG_PRINT_CONFIGS prints each GEMM's tile configuration to stderr.  A
- * DG_PAIR_BLOCK_N width that is not compiled in makes pair launches return
- * DG_ERR_UNSUPPORTED; a DG_BLOCK_N width that is not compiled in is ignored
- * (128 is used). */
+ * width, DG_PAIR_BLOCK_N the 256-row pair kernel's, DG_SKINNY_PAIR_BLOCK_N the
+ * 128-row pair kernel's for dense GEMMs with m <= 128 and no C (32, 64, 96 or
+ * 128; a negative value keeps them on single CTAs), and DG_PRINT_CONFIGS
+ * prints each GEMM's tile configuration to stderr.  A DG_PAIR_BLOCK_N width
+ * that is not compiled in makes pair launches return DG_ERR_UNSUPPORTED; a
+ * DG_BLOCK_N width that is not compiled in is ignored (128 is used), and so
+ * is a DG_SKINNY_PAIR_BLOCK_N width (the single-CTA kernel is used). */
 void dg_set_debug_flags(uint32_t flags);
 
 /* Human-readable name of a dg_status value. */
