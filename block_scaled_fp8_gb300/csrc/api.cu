@@ -347,6 +347,7 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     if (f32) p.d_f32 = static_cast<float *>(o.d);
     else p.d = static_cast<uint16_t *>(o.d);
     p.ldd = o.ldd;
+    p.c_in_place = (f32 && p.c_f32 != nullptr && p.c_f32 == p.d_f32 && p.ldc == p.ldd) ? 1 : 0;
     p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
     uint32_t dbg = g_debug_flags.load();
     if (dbg & DG_DEBUG_DROP_ONE_LOAD) g_debug_flags.fetch_and(~static_cast<uint32_t>(DG_DEBUG_DROP_ONE_LOAD));

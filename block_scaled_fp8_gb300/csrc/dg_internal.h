@@ -46,6 +46,7 @@ struct GemmParams {
     uint32_t debug_flags;
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
     int c_v8;            // bf16 C rows are 32-byte aligned (base and ldc): 16 columns in one load
+    int c_in_place;      // FP32 C is D itself (same pointer and stride): D is accumulated into at L2
     int layout;          // operand layouts: bit 0 A MN-major ([K][M]), bit 1 B MN-major ([K][N]),
                          // bit 2 B FP4 (E2M1, one scale per 32 K)
     // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the

@@ -45,7 +45,9 @@ namespace dg {
 // B4: B is FP4 (E2M1) with one scale per 32 K: its stages take the same shared
 // memory as FP8 (the loads leave 8 empty bytes after every 8 bytes of codes),
 // and a scale group holds one B word per column for each of its 4 K-blocks.
-template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false>
+// SB: output staging buffers per epilogue warp, 0 for as many as fit (up to 4)
+// without costing an operand stage.
+template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false, int SB = 0>
 struct Bs2Config {
     // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
     // with MP=128 each half of N is whole 16-column epilogue chunks
@@ -122,7 +124,8 @@ struct Bs2Config {
         return stages_by_smem(bufs) > kMaxStages ? kMaxStages : stages_by_smem(bufs);
     }
     static constexpr int kStageBufs =
-        MP == 128 ? 2 : (stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2));
+        SB > 0 ? SB
+               : (MP == 128 ? 2 : (stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2)));
     static constexpr int kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
     static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
@@ -143,6 +146,13 @@ struct Bs2Config {
     static_assert(kNumBars * 8 + 8 <= 512, "barrier region");
     static_assert(kSfSlots * kSfSlotBytes >= 2 * (kMaxPsumGroups + 1) * 4, "PSUM segments fit the scale ring");
 };
+
+// Output staging of the FP32-output epilogue: four buffers per warp, one operand
+// stage fewer where that is their price (that epilogue, not the MMAs, sets the pace
+// of the FP32-output GEMMs).
+constexpr int kF32StageBufs = 4;
+template <int BN, int MP, int LAY, bool F32>
+using Bs2Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0, F32 ? kF32StageBufs : 0>;
 
 struct PairTile {
     int a_row0;      // this CTA's first row in the 2-D view of A (and D)
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
     constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0;
     static_assert(!B4 || (!A_MN && !B_MN && !F32), "FP4 B: K-major operands, bf16 D");
-    using Cfg = Bs2Config<BN, MP, B_MN, B4>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
     static_assert(!(A_MN || B_MN) || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
@@ -910,6 +920,22 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         constexpr int kCDepth = Cfg::kChunksPerWarp < 4 ? Cfg::kChunksPerWarp : 4;
         static_assert(!F32 || Cfg::kNumChunks % 2 == 0, "FP32 epilogue: both halves have every chunk");
         float4 cring[(WITH_C && F32) ? kCDepth : 1][4];
+        // FP32 C that is D itself: no C is loaded; each chunk is added to D at L2 by a
+        // TMA reduce, and the tile's D rows are prefetched into L2 a tile ahead (one
+        // bulk request per row) so that those additions find their lines there
+        // (C in a buffer of its own: its rows are prefetched the same way, then loaded
+        // chunk by chunk through the ring below)
+        auto prefetch_d32 = [&](const PairTile &tl) {
+            if (half != 0 || tl.valid_rows == 0 || (p.c_in_place && tl.nkb == 0)) return;
+            const int row = tl.d_row0 + row_off + static_cast<int>(lane);
+            const int cols = p.n - (tl.n0 + col_off) < (MP == 256 ? BN : BN / 2) ? p.n - (tl.n0 + col_off)
+                                                                                  : (MP == 256 ? BN : BN / 2);
+            const float *src = p.c_in_place ? p.d_f32 : p.c_f32;
+            const int64_t ld = p.c_in_place ? p.ldd : p.ldc;
+            if (row < p.rows && cols > 0)
+                prefetch_l2_bulk(src + static_cast<int64_t>(row) * ld + tl.n0 + col_off,
+                                 static_cast<uint32_t>(cols) * 4u);
+        };
         auto load_c32 = [&](const PairTile &tl, int j, float4 (&dst)[4]) {
             const int row = tl.d_row0 + row_off + static_cast<int>(lane);
             const int col0 = tl.n0 + col_off + (2 * j + static_cast<int>(half)) * Cfg::kEpiChunk;
@@ -926,8 +952,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
             if constexpr (WITH_C && !F32) prefetch_c(tile);
             if constexpr (WITH_C && F32) {
+                prefetch_d32(tile);
+                if (!p.c_in_place) {
 #pragma unroll
-                for (int j = 0; j < kCDepth; ++j) load_c32(tile, j, cring[j]);
+                    for (int j = 0; j < kCDepth; ++j) load_c32(tile, j, cring[j]);
+                }
             }
         }
         for (int t = pair_id; t < num_tiles; t += num_pairs) {
@@ -994,13 +1023,17 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 // 8-column FP32 boxes through the staging buffers; the accumulator is
                 // released after its last chunk is read
                 const int row = tile.d_row0 + row_off + static_cast<int>(lane);
+                // D = C in place: an empty group leaves D as it is; the next tile's rows go to L2
+                const bool in_place = WITH_C && p.c_in_place;
+                if (WITH_C && has_next) prefetch_d32(next_tile);
+                const bool skip_tile = in_place && tile.nkb == 0;
                 // chunks in runs of kCDepth, so that a chunk's ring slot is a constant
 #pragma unroll 1
                 for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += kCDepth)
 #pragma unroll
                 for (int u = 0; u < kCDepth; ++u) {
                     const int j = j0 + u;
-                    if (j >= Cfg::kChunksPerWarp) break;
+                    if (j >= Cfg::kChunksPerWarp || skip_tile) break;
                     const int c = 2 * j + half;
                     const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
                     float f[16];
@@ -1017,18 +1050,20 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         for (int i = 0; i < 16; ++i) f[i] = 0.f;
                     }
                     if constexpr (WITH_C) {
+                        if (!in_place) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            f[4 * q + 0] += cring[u][q].x;
-                            f[4 * q + 1] += cring[u][q].y;
-                            f[4 * q + 2] += cring[u][q].z;
-                            f[4 * q + 3] += cring[u][q].w;
+                            for (int q = 0; q < 4; ++q) {
+                                f[4 * q + 0] += cring[u][q].x;
+                                f[4 * q + 1] += cring[u][q].y;
+                                f[4 * q + 2] += cring[u][q].z;
+                                f[4 * q + 3] += cring[u][q].w;
+                            }
+                            // refill the slot: chunk j + kCDepth of this tile, or chunk u of the next
+                            if (j + kCDepth < Cfg::kChunksPerWarp)
+                                load_c32(tile, j + kCDepth, cring[u]);
+                            else if (has_next)
+                                load_c32(next_tile, u, cring[u]);
                         }
-                        // refill the slot: chunk j + kCDepth of this tile, or chunk u of the next
-                        if (j + kCDepth < Cfg::kChunksPerWarp)
-                            load_c32(tile, j + kCDepth, cring[u]);
-                        else if (has_next)
-                            load_c32(next_tile, u, cring[u]);
                     }
                     if (tile.valid_rows == 0 || col0 >= p.n) continue;
                     if (tile.valid_rows < MP / 2) {
@@ -1038,10 +1073,16 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             float *drow = p.d_f32 + static_cast<int64_t>(row) * p.ldd + col0;
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                if (col0 + 4 * q < p.n)
-                                    *reinterpret_cast<float4 *>(drow + 4 * q) =
-                                        value ? make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3])
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (col0 + 4 * q < p.n) {
+                                    float4 o4 = value ? make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3])
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    if (in_place && value) {
+                                        // this thread owns these elements: D += sum, one FP32 add each
+                                        const float4 d4 = *reinterpret_cast<const float4 *>(drow + 4 * q);
+                                        o4 = make_float4(d4.x + o4.x, d4.y + o4.y, d4.z + o4.z, d4.w + o4.w);
+                                    }
+                                    *reinterpret_cast<float4 *>(drow + 4 * q) = o4;
+                                }
                         }
                         continue;
                     }
@@ -1061,7 +1102,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
+                            if (in_place) tma_reduce_add_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
+                            else tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
                             bulk_commit_group();
                         }
                         buf = buf + 1 == Cfg::kStageBufs ? 0 : buf + 1;
@@ -1163,7 +1205,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
     cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
@@ -1185,7 +1227,7 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
 
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 int max_active_pairs_impl() {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
     if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
@@ -1205,9 +1247,9 @@ int max_active_pairs_impl() {
     return n;
 }
 
-template <int BN, int MP, int LAY = 0>
+template <int BN, int MP, int LAY = 0, bool F32 = false>
 void fill_bs2_info(KernelInfo *info) {
-    using Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
     info->block_n = BN;
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;

@@ -268,6 +268,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
         : "memory");
 }
 
+// TMA reduce: the box in shared memory is added element-wise to the tensor in
+// global memory (the addition is done at L2, in the tensor map's type; FP32
+// adds round to nearest even).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const void *smem_src, int32_t x,
+                                                  int32_t y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(smem_u32(smem_src))
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -63,6 +63,21 @@ def test_f32_rounds_to_the_bf16_gemm():
     assert torch.equal(d32.to(torch.bfloat16), d16)
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 1000, 384), (4096, 7168, 2048)])
+def test_f32_in_place_equals_separate(M, N, K):
+    """c = d (accumulated into D at L2 by TMA reduce-add) gives the same bits
+    as C in its own buffer (added in registers)."""
+    case = inputs.dense_case(M, N, K, seed=M + K, b_scale_exp_range=(-8, 4))
+    a, sfa, b, sfb = _packed(case)
+    c0 = torch.randn(M, N, generator=torch.Generator().manual_seed(M)).to(DEV)
+    d_sep = torch.full((M, N), 7.0, dtype=torch.float32, device=DEV)
+    binding.dg_fp8_gemm_nt_f32(a, sfa, b, sfb, d_sep, c=c0)
+    d_in = c0.clone()
+    binding.dg_fp8_gemm_nt_f32(a, sfa, b, sfb, d_in, c=d_in)
+    torch.cuda.synchronize()
+    assert torch.equal(d_sep, d_in)
+
+
 def test_f32_in_place_accumulation_and_k_zero(orc):
     """c aliasing d accumulates in place; K = 0 gives D = C."""
     M, N, K = 256, 512, 768

@@ -83,6 +83,21 @@ def test_k_grouped_in_place(orc):
     _close_f32(d.cpu().numpy(), ref, "in place")
 
 
+@pytest.mark.parametrize("E,M,N,ks", [(4, 320, 264, [256, 0, 384, 128]), (2, 1000, 520, [1152, 128])])
+def test_k_grouped_in_place_equals_separate(E, M, N, ks):
+    """C passed as D itself is accumulated into D at L2 (TMA reduce-add; rows at
+    the M edge by the owning thread); C in a buffer of its own is added in
+    registers.  Both are one FP32 addition of C and the same sum: the same bits."""
+    case = inputs.k_grouped_case(E, M, N, seed=E * M + N, ks=ks)
+    d_sep, _, _, st_sep, _ = _run(case)
+    d_in, _, _, st_in, _ = _run(case, in_place=True)
+    assert st_sep == 0 and st_in == 0
+    assert torch.equal(d_sep, d_in)
+    for e, k in enumerate(ks):
+        if k == 0:
+            assert torch.equal(d_in[e].cpu(), case.c[e]), f"empty group {e}: D must stay C"
+
+
 def test_k_grouped_equals_tn_per_group():
     ks = [256, 384, 128]
     E, M, N = 3, 512, 768
