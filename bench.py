@@ -752,6 +752,61 @@ def run_case_k_grouped(args):
                       "gbs": round(by / (us * 1e-6) / 1e9, 1), "config": binding.last_config()}))
 
 
+def run_case_grouped(args):
+    """One M-grouped GEMM of the MoE workloads, `warmup` + `steps` launches (for ncu
+    captures): `contiguous` (8 experts, M_e ~ U[128, 4096] padded to 128, N=4096,
+    K=7168) or `masked` (32 experts, max_m 256, N=4096, K=7168); prints the median
+    per-launch device time."""
+    import torch
+
+    from block_scaled_fp8_gb300 import binding, build, inputs
+    build.build()
+    dev = torch.device("cuda", 0)
+    n, k = 4096, 7168
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.case_grouped == "contiguous":
+        cc = inputs.contiguous_case(8, n, k, seed=3, device=dev)
+        mt = cc.a.shape[0]
+        sfa = binding.transform_sf(cc.sfa, 1, mt)
+        sfb = binding.transform_sf(cc.sfb, 128, n)
+        d = torch.empty(mt, n, dtype=torch.bfloat16, device=dev)
+        valid = sum(cc.m_per_expert)
+        used = sum(1 for v in cc.m_per_expert if v)
+
+        def call():
+            binding.dg_m_grouped_fp8_gemm_nt_contiguous(cc.a, sfa, cc.b, sfb, d, cc.grouped_layout, status=status)
+    else:
+        mc = inputs.masked_case(32, 256, n, k, seed=4, device=dev)
+        sfa = binding.transform_sf(mc.sfa, 1, 256)
+        sfb = binding.transform_sf(mc.sfb, 128, n)
+        d = torch.empty(32, 256, n, dtype=torch.bfloat16, device=dev)
+        valid = int(mc.masked_m.sum())
+        used = int((mc.masked_m > 0).sum())
+
+        def call():
+            binding.dg_m_grouped_fp8_gemm_nt_masked(mc.a, sfa, mc.b, sfb, d, mc.masked_m, mc.expected_m,
+                                                    status=status)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert int(status.item()) == 0, int(status.item())
+    us = statistics.median(times) * 1e3
+    by = valid * k + used * n * k + 2 * valid * n
+    print(json.dumps({"case_grouped": args.case_grouped, "valid_rows": valid, "median_us": round(us, 2),
+                      "tflops": round(flops(valid, n, k) / (us * 1e-6) / 1e12, 1),
+                      "gbs": round(by / (us * 1e-6) / 1e9, 1), "config": binding.last_config()}))
+
+
 def run_case(args):
     """One dense GEMM shape, `warmup` + `steps` launches (for ncu captures and
     per-shape timing); prints per-launch device time."""
@@ -766,8 +821,8 @@ def run_case(args):
         sfb = binding.transform_sf(case.sfb.contiguous(), 1, n)
         gemm = binding.dg_fp8_fp4_gemm_nt
     else:
-        case = inputs.dense_case(m, n, k, seed=0, with_c=args.with_c)
-        sfb = binding.transform_sf(case.sfb.to(dev), 128, n)
+        case = inputs.dense_case(m, n, k, seed=0, with_c=args.with_c, device=dev)
+        sfb = binding.transform_sf(case.sfb, 128, n)
         gemm = binding.dg_fp8_gemm_nt
     a, b = case.a.to(dev), case.b.to(dev)
     sfa = binding.transform_sf(case.sfa.to(dev), 1, m)
@@ -906,6 +961,8 @@ def main():
     ap.add_argument("--fp4", action="store_true", help="with --case: FP4 (E2M1) weights, dg_fp8_fp4_gemm_nt")
     ap.add_argument("--case-k-grouped", default=None,
                     help="E,M,N,K: time one K-grouped GEMM (E groups of K rows each, C = D in place)")
+    ap.add_argument("--case-grouped", choices=["contiguous", "masked"], default=None,
+                    help="time one M-grouped MoE GEMM: contiguous (8 experts) or masked (32 experts)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
@@ -921,7 +978,7 @@ def main():
         rec = record_traffic(args.record_traffic, args.traffic_out, args.traffic_command)
         print(json.dumps({"traffic_record": args.traffic_out, "source_digest": rec["source_digest"]}))
         return
-    if args.warmup < 3 and not (args.case or args.case_k_grouped):
+    if args.warmup < 3 and not (args.case or args.case_k_grouped or args.case_grouped):
         ap.error("--warmup must be >= 3")
 
     rank = int(os.environ.get("RANK", "0"))
@@ -935,6 +992,9 @@ def main():
         return
     if args.case_k_grouped:
         run_case_k_grouped(args)
+        return
+    if args.case_grouped:
+        run_case_grouped(args)
         return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
