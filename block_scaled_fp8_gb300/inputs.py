@@ -229,22 +229,33 @@ V3_M = [128, 4096]
 class KGroupedCase:
     """K-grouped weight-gradient inputs (PaperTrace DeepGEMM §3.3, §5.2): the
     groups' K rows are concatenated; group e owns rows [K_e, K_e + ks[e]) of A
-    and B and scale rows [K_e/128, (K_e + ks[e])/128)."""
+    and B and scale rows [K_e/gran_k, (K_e + ks[e])/gran_k), gran_k = 128 or 32."""
     a: torch.Tensor      # float8 [K_total, M] (M contiguous)
-    sfa: torch.Tensor    # fp32 [K_total/128, M], one scale per (128-K block, m)
+    sfa: torch.Tensor    # fp32 [K_total/gran_k, M], one scale per (gran_k-row K block, m)
     b: torch.Tensor      # float8 [K_total, N] (N contiguous)
-    sfb: torch.Tensor    # fp32 [K_total/128, N]
+    sfb: torch.Tensor    # fp32 [K_total/gran_k, N]
     c: torch.Tensor      # fp32 [E, M, N]
     ks: list[int]
     meta: dict = field(default_factory=dict)
 
 
+def quantize_1xg(x: torch.Tensor, gran: int):
+    """x fp32 [R, K] with K % gran == 0 -> (codes float8_e4m3fn [R, K], scales
+    fp32 [R, K/gran]): the 1x128 recipe with groups of `gran` elements."""
+    R, K = x.shape
+    xg = x.view(R, K // gran, gran)
+    s = pow2_scale(xg.abs().amax(-1))
+    return (xg / s[..., None]).view(R, K).to(torch.float8_e4m3fn), s
+
+
 def k_grouped_case(num_groups: int, M: int, N: int, seed: int = 0, ks: list[int] | None = None,
-                   k_lo: int = 128, k_hi: int = 4096, align: int = 128, device="cpu") -> KGroupedCase:
+                   k_lo: int = 128, k_hi: int = 4096, align: int = 128, device="cpu",
+                   gran_k: int = 128) -> KGroupedCase:
     """Group sizes uniform in [k_lo, k_hi] rounded up to `align` (the token
     counts per expert of the MoE shapes, stored padded), unless given.  Each
-    group's A and B come from N(0,1), quantised with one scale per 128 rows of
-    K and per column (the 1x128 recipe applied along K)."""
+    group's A and B come from N(0,1), quantised with one scale per gran_k rows
+    of K (128, or 32 for the pages' pre-packed form) and per column (the 1x128
+    recipe applied along K); sfa, sfb are then [K_total/gran_k, M or N]."""
     g = generator(seed, device)
     if ks is None:
         ks = [cdiv(int(v), align) * align
@@ -253,19 +264,20 @@ def k_grouped_case(num_groups: int, M: int, N: int, seed: int = 0, ks: list[int]
     k_total = sum(ks)
     a = torch.empty(k_total, M, dtype=torch.float8_e4m3fn, device=device)
     b = torch.empty(k_total, N, dtype=torch.float8_e4m3fn, device=device)
-    sfa = torch.empty(k_total // GRAN, M, dtype=torch.float32, device=device)
-    sfb = torch.empty(k_total // GRAN, N, dtype=torch.float32, device=device)
+    sfa = torch.empty(k_total // gran_k, M, dtype=torch.float32, device=device)
+    sfb = torch.empty(k_total // gran_k, N, dtype=torch.float32, device=device)
     k0 = 0
     for k in ks:
         if k:
             for x_out, s_out, mn in ((a, sfa, M), (b, sfb, N)):
-                q, s = quantize_1x128(torch.randn(mn, k, generator=g, dtype=torch.float32, device=device))
+                x = torch.randn(mn, k, generator=g, dtype=torch.float32, device=device)
+                q, s = quantize_1x128(x) if gran_k == GRAN else quantize_1xg(x, gran_k)
                 x_out[k0:k0 + k] = q.t()
-                s_out[k0 // GRAN:(k0 + k) // GRAN] = s.t()
+                s_out[k0 // gran_k:(k0 + k) // gran_k] = s.t()
         k0 += k
     c = torch.randn(num_groups, M, N, generator=g, dtype=torch.float32, device=device)
     return KGroupedCase(a, sfa, b, sfb, c, list(ks),
-                        {"E": num_groups, "M": M, "N": N, "K_total": k_total, "seed": seed})
+                        {"E": num_groups, "M": M, "N": N, "K_total": k_total, "seed": seed, "gran_k": gran_k})
 
 
 # E2M1 magnitudes by code (low 3 bits) and the midpoints between neighbours

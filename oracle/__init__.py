@@ -87,6 +87,10 @@ def _get():
             lib.orc_gemm_fp8_fp4_nt.argtypes = [i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, P, i32]
             lib.orc_gemm_fp8_fp4_nt_sampled.restype = None
             lib.orc_gemm_fp8_fp4_nt_sampled.argtypes = [i32, P, i64, P, P, i64, P, i64, P, P, P, i32]
+            lib.orc_gemm_nt_f32_gk.restype = None
+            lib.orc_gemm_nt_f32_gk.argtypes = [i32, i32, i32, i32, P, i64, P, P, i64, P, P, i64, P, i64, i32]
+            lib.orc_gemm_nt_gk_pre_sampled.restype = None
+            lib.orc_gemm_nt_gk_pre_sampled.argtypes = [i32, i32, P, i64, P, P, i64, P, i64, P, P, P, i32]
             lib.orc_max_threads.restype = i32
             _lib = lib
     return _lib
@@ -353,19 +357,20 @@ def gemm_nt_f32_sampled(a, sa, b, sb_rows, rows, cols, c=None, nthreads: int = 0
     return (cv + pre).astype(np.float32)
 
 
-def k_grouped_pack_sf(sf: np.ndarray, ks) -> np.ndarray:
+def k_grouped_pack_sf(sf: np.ndarray, ks, gran_k: int = 128) -> np.ndarray:
     """Packed scales of the K-grouped GEMM (PaperTrace DeepGEMM §3.3).
 
-    sf: FP32 [sum_k ks/128, mn], one row per 128-K block of the concatenated
-    groups, mn contiguous, mn % 4 == 0.  Each group is packed on its own and
-    the results are concatenated: packed row q of group e holds in byte j the
-    UE8M0 byte (the exponent bits, >> 23) of the group's scale row 4q + j, and 0
-    where the group has no such row.  Returns int32 [sum_e ceil(ks[e]/512), mn].
+    sf: FP32 [sum_k ks/gran_k, mn], one row per gran_k-row K block (128, or 32
+    for the pages' pre-packed form) of the concatenated groups, mn contiguous,
+    mn % 4 == 0.  Each group is packed on its own and the results are
+    concatenated: packed row q of group e holds in byte j the UE8M0 byte (the
+    exponent bits, >> 23) of the group's scale row 4q + j, and 0 where the group
+    has no such row.  Returns int32 [sum_e ceil(ks[e] / (4 gran_k)), mn].
     """
     sf = np.ascontiguousarray(sf, dtype=np.float32)
     mn = sf.shape[1]
     assert mn % 4 == 0
-    rows = [k // 128 for k in ks]
+    rows = [k // gran_k for k in ks]
     assert all(k % 128 == 0 and k >= 0 for k in ks) and sum(rows) == sf.shape[0]
     exp = ((sf.view(np.uint32) >> 23) & 0xFF).astype(np.uint32)
     out = []
@@ -414,6 +419,71 @@ def k_grouped_gemm_tn(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarr
                                c=c[e], nthreads=nthreads)
         k0 += k
     return d
+
+
+def k_grouped_gemm_tn_k32(a: np.ndarray, sa: np.ndarray, b: np.ndarray, sb: np.ndarray, ks,
+                          c: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """The K-grouped GEMM with scales at a K granularity of 32 (PaperTrace
+    DeepGEMM §3.3: the layout's pre-packed scales come at gran_k = 32): for each
+    group e
+
+        D_e[m, n] = C_e[m, n] + sum over group e's k of A[k, m] sa(k/32, m) B[k, n] sb(k/32, n)
+
+    a, b as for k_grouped_gemm_tn; sa: fp64 [K_total/32, M]; sb: fp64
+    [K_total/32, N]; C plus the group's fp64 product sum (from 0, increasing k),
+    rounded once to FP32.  Returns FP32 [E, M, N]."""
+    a, b = _u8(a), _u8(b)
+    M, N = a.shape[1], b.shape[1]
+    c = np.ascontiguousarray(c, dtype=np.float32)
+    E = len(ks)
+    assert c.shape == (E, M, N) and a.shape[0] == b.shape[0] == sum(ks)
+    assert sa.shape == (sum(ks) // 32, M) and sb.shape == (sum(ks) // 32, N)
+    d = np.empty((E, M, N), dtype=np.float32)
+    k0 = 0
+    for e, k in enumerate(ks):
+        assert k % 128 == 0 and k >= 0
+        if k == 0:
+            d[e] = c[e]
+        else:
+            s0, s1 = k0 // 32, (k0 + k) // 32
+            at = np.ascontiguousarray(a[k0:k0 + k].T)
+            bt = np.ascontiguousarray(b[k0:k0 + k].T)
+            sat = np.ascontiguousarray(sa[s0:s1].T, dtype=np.float64)
+            sbt = np.ascontiguousarray(sb[s0:s1].T, dtype=np.float64)
+            ce = np.ascontiguousarray(c[e])
+            _get().orc_gemm_nt_f32_gk(M, N, k, 32, _ptr(at), k, _ptr(sat), _ptr(bt), k, _ptr(sbt), _ptr(ce), N,
+                                      _ptr(d[e]), N, nthreads)
+        k0 += k
+    return d
+
+
+def k_grouped_gemm_tn_k32_sampled(a, sa, b, sb, ks, c, es, ms, ns, nthreads: int = 0) -> np.ndarray:
+    """The elements (es[i], ms[i], ns[i]) of k_grouped_gemm_tn_k32, one by one,
+    in its order (the fp64 product sum from 0, then C), rounded once to FP32."""
+    a, b = _u8(a), _u8(b)
+    es, ms, ns = (np.asarray(x, dtype=np.int64) for x in (es, ms, ns))
+    out = np.empty(len(es), dtype=np.float32)
+    k0 = 0
+    for e, k in enumerate(ks):
+        sel = np.nonzero(es == e)[0]
+        if len(sel):
+            cv = np.asarray(c[e], dtype=np.float32)[ms[sel], ns[sel]].astype(np.float64)
+            if k == 0:
+                out[sel] = cv.astype(np.float32)
+            else:
+                s0, s1 = k0 // 32, (k0 + k) // 32
+                at = np.ascontiguousarray(a[k0:k0 + k].T)
+                bt = np.ascontiguousarray(b[k0:k0 + k].T)
+                sat = np.ascontiguousarray(sa[s0:s1].T, dtype=np.float64)
+                sbt = np.ascontiguousarray(sb[s0:s1].T, dtype=np.float64)
+                rows = np.ascontiguousarray(ms[sel])
+                cols = np.ascontiguousarray(ns[sel])
+                pre = np.empty(len(sel), dtype=np.float64)
+                _get().orc_gemm_nt_gk_pre_sampled(k, 32, _ptr(at), k, _ptr(sat), _ptr(bt), k, _ptr(sbt),
+                                                  len(sel), _ptr(rows), _ptr(cols), _ptr(pre), nthreads)
+                out[sel] = (cv + pre).astype(np.float32)
+        k0 += k
+    return out
 
 
 def k_grouped_gemm_tn_sampled(a, sa, b, sb, ks, c, es, ms, ns, nthreads: int = 0) -> np.ndarray:

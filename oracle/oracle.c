@@ -250,6 +250,58 @@ void orc_gemm_nt_f32(int M, int N, int K, const uint8_t *A, int64_t lda, const d
 }
 
 /*
+ * The FP32-output GEMM with scales every gk elements of K instead of 128 (the
+ * K-grouped layout's scales at a K granularity of 32 [P1 3.3]): sa is
+ * [M][ceil(K/gk)] (row m, group k/gk), sb is [N][ceil(K/gk)].  Otherwise as
+ * orc_gemm_nt_f32: the products summed in fp64 from 0 in increasing k, then C
+ * added (0 if NULL), one rounding to FP32.
+ */
+static double dot_element_gk(int K, int gk, const uint8_t *arow, const double *sarow, const uint8_t *brow,
+                             const double *sbrow, double c) {
+    double s = 0.0;
+    for (int k = 0; k < K; k++) {
+        double a = orc_e4m3_decode(arow[k]) * sarow[k / gk];
+        double b = orc_e4m3_decode(brow[k]) * sbrow[k / gk];
+        s += a * b;
+    }
+    return c + s;
+}
+
+void orc_gemm_nt_f32_gk(int M, int N, int K, int gk, const uint8_t *A, int64_t lda, const double *sa,
+                        const uint8_t *B, int64_t ldb, const double *sb, const float *C, int64_t ldc,
+                        float *D, int64_t ldd, int nthreads) {
+    int sf_k = (K + gk - 1) / gk;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int m = 0; m < M; m++) {
+        for (int n = 0; n < N; n++) {
+            double c = C ? (double)C[(int64_t)m * ldc + n] : 0.0;
+            double v = dot_element_gk(K, gk, A + (int64_t)m * lda, sa + (int64_t)m * sf_k,
+                                      B + (int64_t)n * ldb, sb + (int64_t)n * sf_k, c);
+            D[(int64_t)m * ldd + n] = (float)v;
+        }
+    }
+}
+
+/* The fp64 product sums (no C, no rounding) of orc_gemm_nt_f32_gk at a list of
+ * (row, col) pairs. */
+void orc_gemm_nt_gk_pre_sampled(int K, int gk, const uint8_t *A, int64_t lda, const double *sa,
+                                const uint8_t *B, int64_t ldb, const double *sb, int64_t nsamples,
+                                const int64_t *rows, const int64_t *cols, double *pre, int nthreads) {
+    int sf_k = (K + gk - 1) / gk;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
+    for (int64_t i = 0; i < nsamples; i++) {
+        int64_t m = rows[i], n = cols[i];
+        pre[i] = dot_element_gk(K, gk, A + m * lda, sa + m * sf_k, B + n * ldb, sb + n * sf_k, 0.0);
+    }
+}
+
+/*
  * Full GEMM, NT layout [P2 13.3]: A [M][lda] (K contiguous), B [N][ldb] (K
  * contiguous), sa [M][sf_k], sb [N][sf_k] (per row), C bf16 [M][ldc] or NULL,
  * D bf16 [M][ldd].  pre (optional, [M][N]) receives the fp64 value before

@@ -670,6 +670,75 @@ def test_k_grouped_pack_hand_worked(orc):
     assert np.array_equal(got, want)
 
 
+def test_k_grouped_k32_bruteforce_from_storage(orc):
+    """PaperTrace DeepGEMM §3.3: the K-grouped layout's pre-packed scales come
+    at a K granularity of 32.  The brute force reads A[k, m], B[k, n] and the
+    scale rows k // 32 straight from storage; power-of-two scales keep every
+    term exact, so each FP32 output is the single rounding of the rational sum.
+    ks = [128, 0, 256] spans 4, 0 and 8 scale rows, so a scale row taken at the
+    128 granularity, a group offset or an operand swap changes the values."""
+    ks = [128, 0, 256]
+    M, N = 3, 5
+    case = inputs.k_grouped_case(3, M, N, seed=64, ks=ks, gran_k=32)
+    assert case.sfa.shape == (12, M) and case.sfb.shape == (12, N)
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    A = _decode_codes_torch(case.a.view(torch.uint8))
+    B = _decode_codes_torch(case.b.view(torch.uint8))
+    sa = case.sfa.double().numpy()
+    sb = case.sfb.double().numpy()
+    assert len(np.unique(sa)) > 1 and len(np.unique(sb)) > 1
+    c = case.c.numpy()
+    d = orc.k_grouped_gemm_tn_k32(a, sa, b, sb, ks, c)
+    assert np.array_equal(d[1], c[1])
+    k0 = 0
+    for e, k in enumerate(ks):
+        for m in range(M):
+            for n in range(N):
+                s = Fraction(float(c[e, m, n]))
+                for kk in range(k0, k0 + k):
+                    if A[kk, m] and B[kk, n]:
+                        s += (Fraction(float(A[kk, m])) * Fraction(float(sa[kk // 32, m])) *
+                              Fraction(float(B[kk, n])) * Fraction(float(sb[kk // 32, n])))
+                assert d[e, m, n] == np.float32(float(s)), (e, m, n)
+        k0 += k
+
+
+def test_k_grouped_k32_reduces_to_k128(orc):
+    """Scales at a K granularity of 32 whose four rows in every 128-row block are
+    equal give the 128-granularity GEMM bit for bit (the same terms in the same
+    order); the sampled form equals the full one bit for bit."""
+    ks = [256, 128, 0, 384]
+    case = inputs.k_grouped_case(4, 24, 40, seed=65, ks=ks)
+    a = case.a.view(torch.uint8).numpy()
+    b = case.b.view(torch.uint8).numpy()
+    sa, sb, c = case.sfa.double().numpy(), case.sfb.double().numpy(), case.c.numpy()
+    sa32, sb32 = np.repeat(sa, 4, axis=0), np.repeat(sb, 4, axis=0)
+    d128 = orc.k_grouped_gemm_tn(a, sa, b, sb, ks, c)
+    d32 = orc.k_grouped_gemm_tn_k32(a, sa32, b, sb32, ks, c)
+    assert np.array_equal(d32.view(np.uint32), d128.view(np.uint32))
+    rng = np.random.default_rng(2)
+    es, ms, ns = rng.integers(0, 4, 300), rng.integers(0, 24, 300), rng.integers(0, 40, 300)
+    got = orc.k_grouped_gemm_tn_k32_sampled(a, sa32, b, sb32, ks, c, es, ms, ns)
+    assert np.array_equal(got.view(np.uint32), d32[es, ms, ns].view(np.uint32))
+
+
+def test_k_grouped_pack_k32_hand_worked(orc):
+    """PaperTrace DeepGEMM §3.3 at gran_k = 32: ks = [128, 256, 0] gives 4, 8
+    and 0 scale rows, packed 4 per int32 per group: 1 + 2 + 0 packed rows.
+    Scale row r, column i is 2^(r - i) (UE8M0 byte 0x7F + r - i); byte j of a
+    word is row 4q + j of its group.  The words were worked out by hand."""
+    mn = 4
+    sf = np.array([[2.0 ** (r - i) for i in range(mn)] for r in range(12)], dtype=np.float32)
+    got = orc.k_grouped_pack_sf(sf, [128, 256, 0], gran_k=32).view(np.uint32)
+    want = np.array([
+        [0x8281807F, 0x81807F7E, 0x807F7E7D, 0x7F7E7D7C],   # group 0: rows 0..3
+        [0x86858483, 0x85848382, 0x84838281, 0x83828180],   # group 1: rows 4..7
+        [0x8A898887, 0x89888786, 0x88878685, 0x87868584],   # group 1: rows 8..11
+    ], dtype=np.uint32)
+    assert np.array_equal(got, want)
+
+
 def test_k_grouped_sampled_equals_full(orc):
     case = inputs.k_grouped_case(3, 40, 24, seed=63, ks=[256, 0, 384])
     a = case.a.view(torch.uint8).numpy()
