@@ -325,6 +325,18 @@ def measure_other_workloads(dev, flush, reps, stream):
            flops(4096, 7168, kt), kt * (4096 + 7168) + 2 * 4 * 8 * 4096 * 7168,
            {"d": "fp32, in place", "ks": kc.ks})
     del kc, sfa, sfb, ks_dev
+    # the same weight gradient with its scales every 32 rows of K (the pages' pre-packed form)
+    kc = inputs.k_grouped_case(8, 4096, 7168, seed=3, device=dev, gran_k=32)
+    sfa = binding.dg_transform_sf_k_grouped_k32(kc.sfa, kc.ks)
+    sfb = binding.dg_transform_sf_k_grouped_k32(kc.sfb, kc.ks)
+    ks_dev = torch.tensor(kc.ks, dtype=torch.int32, device=dev)
+    kt = sum(kc.ks)
+    record(f"k-grouped weight gradient 8 groups M=4096 N=7168 K_total={kt}, 32-row scales",
+           lambda: binding.dg_k_grouped_fp8_gemm_tn_contiguous_k32(kc.a, sfa, kc.b, sfb, kc.c, kc.ks, ks_dev=ks_dev,
+                                                                   c=kc.c, status=status),
+           flops(4096, 7168, kt), kt * (4096 + 7168) + 2 * 4 * 8 * 4096 * 7168,
+           {"d": "fp32, in place", "ks": kc.ks, "scales": "every 32 rows of K"})
+    del kc, sfa, sfb, ks_dev
 
     # masked grouped decode: 32 experts, max_m 256
     n, k, e, max_m = 4096, 7168, 32, 256

@@ -33,6 +33,7 @@ EXPORTS = (
     "dg_fp8_fp4_gemm_nt", "dg_m_grouped_fp8_fp4_gemm_nt_contiguous", "dg_m_grouped_fp8_fp4_gemm_nt_masked",
     "dg_transform_sf", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_contiguous_psum",
     "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped", "dg_k_grouped_packed_sf_rows",
+    "dg_k_grouped_fp8_gemm_tn_contiguous_k32", "dg_transform_sf_k_grouped_k32",
     "dg_m_grouped_fp8_gemm_nt_masked", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_get_tma_aligned_size", "dg_packed_sf_words", "dg_set_num_sms", "dg_get_num_sms",
     "dg_set_wait_timeout_ms", "dg_set_debug_flags", "dg_status_string", "dg_get_last_config",
@@ -82,9 +83,12 @@ def lib():
             L.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [P, i64, P, P, i64, P, P, P, i32, i32, P, P, i32,
                                                               P, P]
             L.dg_transform_sf_k_grouped.argtypes = [P, i32, P, i32, P, P, P]
+            L.dg_k_grouped_fp8_gemm_tn_contiguous_k32.argtypes = L.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes
+            L.dg_transform_sf_k_grouped_k32.argtypes = L.dg_transform_sf_k_grouped.argtypes
             L.dg_k_grouped_packed_sf_rows.restype = i64
             L.dg_k_grouped_packed_sf_rows.argtypes = [P, i32]
-            for f in ("dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped"):
+            for f in ("dg_k_grouped_fp8_gemm_tn_contiguous", "dg_transform_sf_k_grouped",
+                      "dg_k_grouped_fp8_gemm_tn_contiguous_k32", "dg_transform_sf_k_grouped_k32"):
                 getattr(L, f).restype = i32
             for f in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_tn",
                       "dg_fp8_gemm_tt", "dg_transform_sf",
@@ -320,6 +324,35 @@ def dg_transform_sf_k_grouped(sf: torch.Tensor, ks, out: torch.Tensor | None = N
     _check("dg_transform_sf_k_grouped", lib().dg_transform_sf_k_grouped(
         _p(sf), mn, _ks_host(ks), len(ks), _p(out), _p(status), _stream(stream)))
     return out
+
+
+def dg_transform_sf_k_grouped_k32(sf: torch.Tensor, ks, out: torch.Tensor | None = None,
+                                  status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """sf FP32 [sum(ks)/32, mn] (one scale row per 32 rows of K) -> packed int32
+    [sum(ks)/128, mn]."""
+    assert sf.dtype == torch.float32 and sf.is_contiguous()
+    mn = sf.shape[1]
+    if out is None:
+        out = torch.empty(sum(ks) // 128, mn, dtype=torch.int32, device=sf.device)
+    _check("dg_transform_sf_k_grouped_k32", lib().dg_transform_sf_k_grouped_k32(
+        _p(sf), mn, _ks_host(ks), len(ks), _p(out), _p(status), _stream(stream)))
+    return out
+
+
+def dg_k_grouped_fp8_gemm_tn_contiguous_k32(a, sfa, b, sfb, d, ks, ks_dev=None, c=None,
+                                            status: torch.Tensor | None = None, stream=None):
+    """As dg_k_grouped_fp8_gemm_tn_contiguous with scales every 32 rows of K:
+    sfa/sfb packed int32 [sum(ks)/128, M] / [sum(ks)/128, N]."""
+    K, M = a.shape
+    N = b.shape[1]
+    assert a.stride(1) == 1 and b.stride(1) == 1 and d.is_contiguous() and d.dtype == torch.float32
+    assert c is not None and c.is_contiguous() and c.dtype == torch.float32
+    if ks_dev is None:
+        ks_dev = torch.tensor(list(ks), dtype=torch.int32, device=d.device)
+    _check("dg_k_grouped_fp8_gemm_tn_contiguous_k32", lib().dg_k_grouped_fp8_gemm_tn_contiguous_k32(
+        _p(a), a.stride(0), _p(sfa), _p(b), b.stride(0), _p(sfb), _p(c), _p(d), M, N, _ks_host(ks),
+        _p(ks_dev), len(ks), _p(status), _stream(stream)))
+    return d
 
 
 def dg_k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, d, ks, ks_dev=None, c=None,

@@ -186,12 +186,12 @@ bool use_pair_kernel(const GemmParams &p, int64_t m_blocks_hint) {
 
 int cached_max_pairs(int bn, bool with_c, int mp, bool f32 = false, int lay = 0) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][2][8][513];
+    static int cache[kMaxDevices][2][2][2][16][513];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || bn <= 0 || bn > 512) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][lay & 7][bn];
-    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32, lay & 7);
+    int &v = cache[dev][with_c ? 1 : 0][mp == 128 ? 1 : 0][f32 ? 1 : 0][lay & 15][bn];
+    if (v == 0) v = bs2_max_active_pairs(bn, with_c, mp, f32, lay & 15);
     return v;
 }
 
@@ -1006,7 +1006,10 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void *a, const void *sfa, int sf
 // Packed rows of the K-grouped scales (sum of ceil(ks[e] / 512)), or -1 if ks
 // is invalid: null with groups, more than 255 groups, a size negative or not a
 // multiple of 128, or more than 65535 packed rows.
-static int64_t k_grouped_rows(const int *ks, int num_groups, KGroupRows *t) {
+// Scale rows of the K-grouped layout with one FP32 scale row per gran_k rows of K
+// (128, or 32 for the pre-packed form): each group's rows are packed on their
+// own, 4 per word.  Returns the packed rows, or -1 for invalid sizes.
+static int64_t k_grouped_rows(const int *ks, int num_groups, KGroupRows *t, int gran_k = kBlockK) {
     if (num_groups < 0 || num_groups > kMaxPsumGroups || (num_groups > 0 && ks == nullptr)) return -1;
     int64_t srow = 0, prow = 0;
     if (t) t->num_groups = num_groups;
@@ -1016,8 +1019,8 @@ static int64_t k_grouped_rows(const int *ks, int num_groups, KGroupRows *t) {
             t->srow[e] = static_cast<int>(srow);
             t->prow[e] = static_cast<int>(prow);
         }
-        srow += ks[e] / kBlockK;
-        prow += (ks[e] / kBlockK + 3) / 4;
+        srow += ks[e] / gran_k;
+        prow += (ks[e] / gran_k + 3) / 4;
         if (prow > 65535) return -1;
     }
     if (t) {
@@ -1031,11 +1034,11 @@ int64_t dg_k_grouped_packed_sf_rows(const int *ks, int num_groups) {
     return k_grouped_rows(ks, num_groups, nullptr);
 }
 
-dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
-                                    int32_t *status_dev, void *stream) {
+static dg_status transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                        int32_t *status_dev, void *stream, int gran_k) {
     if (mn < 0) return DG_ERR_INVALID_ARG;
     KGroupRows t;
-    const int64_t prows = k_grouped_rows(ks, num_groups, &t);
+    const int64_t prows = k_grouped_rows(ks, num_groups, &t, gran_k);
     if (prows < 0) return DG_ERR_INVALID_ARG;
     if (mn % 4 != 0) return DG_ERR_LAYOUT;
     if (mn == 0 || prows == 0) return DG_OK;
@@ -1049,12 +1052,22 @@ dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int 
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
-dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
-                                              int64_t ldb, const void *sfb, const float *c, float *d, int m,
-                                              int n, const int *ks, const int32_t *ks_dev, int num_groups,
-                                              int32_t *status_dev, void *stream) {
+dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                    int32_t *status_dev, void *stream) {
+    return transform_sf_k_grouped(sf, mn, ks, num_groups, out, status_dev, stream, kBlockK);
+}
+
+dg_status dg_transform_sf_k_grouped_k32(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                        int32_t *status_dev, void *stream) {
+    return transform_sf_k_grouped(sf, mn, ks, num_groups, out, status_dev, stream, 32);
+}
+
+// The K-grouped GEMM with scales every 128 (k32 false) or 32 (k32 true) rows of K.
+static dg_status k_grouped_gemm(const void *a, int64_t lda, const void *sfa, const void *b, int64_t ldb,
+                                const void *sfb, const float *c, float *d, int m, int n, const int *ks,
+                                const int32_t *ks_dev, int num_groups, int32_t *status_dev, void *stream, bool k32) {
     if (m < 0 || n < 0) return DG_ERR_INVALID_ARG;
-    const int64_t prows = k_grouped_rows(ks, num_groups, nullptr);
+    const int64_t prows = k_grouped_rows(ks, num_groups, nullptr, k32 ? 32 : kBlockK);
     if (prows < 0) return DG_ERR_INVALID_ARG;
     if (m == 0 || n == 0 || num_groups == 0) return DG_OK;
     if (c == nullptr || d == nullptr) return DG_ERR_INVALID_ARG;   // C is required
@@ -1085,7 +1098,9 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const 
     p.ks = ks_dev;
     p.group_rows = m;
     p.num_m_blocks = static_cast<int>(cdiv64(m, 2 * kBlockM));   // m-units of one group
-    p.layout = 3;                                                 // A [K][M], B [K][N]
+    // A [K][M], B [K][N]; 32-K scales (layout bit 3) take 192-column tiles, the widest
+    // whose two accumulators fit beside their four-times-larger TMEM scale slots
+    p.layout = k32 ? 3 | 8 : 3;
     p.c_f32 = c;
     p.d_f32 = d;
     p.ldc = n;
@@ -1094,7 +1109,21 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const 
                  sfb, static_cast<uint64_t>(n), static_cast<uint64_t>(prows),
                  d,   n,   static_cast<uint64_t>(rows)};
     const int64_t units = static_cast<int64_t>(num_groups) * p.num_m_blocks;
-    return launch_pair(p, o, 256, 224, units, sms, static_cast<cudaStream_t>(stream));
+    return launch_pair(p, o, 256, k32 ? 192 : 224, units, sms, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
+                                              int64_t ldb, const void *sfb, const float *c, float *d, int m,
+                                              int n, const int *ks, const int32_t *ks_dev, int num_groups,
+                                              int32_t *status_dev, void *stream) {
+    return k_grouped_gemm(a, lda, sfa, b, ldb, sfb, c, d, m, n, ks, ks_dev, num_groups, status_dev, stream, false);
+}
+
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous_k32(const void *a, int64_t lda, const void *sfa, const void *b,
+                                                  int64_t ldb, const void *sfb, const float *c, float *d, int m,
+                                                  int n, const int *ks, const int32_t *ks_dev, int num_groups,
+                                                  int32_t *status_dev, void *stream) {
+    return k_grouped_gemm(a, lda, sfa, b, ldb, sfb, c, d, m, n, ks, ks_dev, num_groups, status_dev, stream, true);
 }
 
 }  // extern "C"

@@ -47,7 +47,10 @@ namespace dg {
 // and a scale group holds one B word per column for each of its 4 K-blocks.
 // SB: output staging buffers per epilogue warp, 0 for as many as fit (up to 4)
 // without costing an operand stage.
-template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false, int SB = 0>
+// S32: A and B scales every 32 K (K-grouped scales at a K granularity of 32): a
+// scale group holds one word per row of A and per column of B for each of its 4
+// K-blocks, the word's bytes being the K-block's four 32-K scales.
+template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false, int SB = 0, bool S32 = false>
 struct Bs2Config {
     // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
     // with MP=128 each half of N is whole 16-column epilogue chunks
@@ -72,9 +75,11 @@ struct Bs2Config {
     // B scale words: MP=256 copies each 128-column chunk to all four lane quadrants;
     // MP=128 copies the two halves of N to quadrants {0,1} and {2,3} (one 64-row copy)
     static constexpr int kSfbChunks = MP == 256 ? (BN + 127) / 128 : 2;
-    static constexpr int kSfbKb = B4 ? 4 : 1;                    // B words per column per group
+    static constexpr int kSfbKb = (B4 || S32) ? 4 : 1;           // B words per column per group
+    static constexpr int kSfaKb = S32 ? 4 : 1;                   // A words per row per group
     static_assert(!B4 || BN <= 256, "FP4 B: one MMA per K step");
-    static constexpr int kSfCols = 4 + (MP == 256 ? 4 * kSfbChunks : 4) * kSfbKb;
+    static_assert(!S32 || (MP == 256 && BN <= 256), "32-K scales: 256-row pairs, one MMA per K step");
+    static constexpr int kSfCols = 4 * kSfaKb + (MP == 256 ? 4 * kSfbChunks : 4) * kSfbKb;
     // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
     // destination, already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what
     // the MMA reads).  A scale warp loads a group up to kSfLookahead groups before
@@ -84,7 +89,7 @@ struct Bs2Config {
     // TMEM completes, which is kSfSlots - kSfLookahead groups before the slot
     // is loaded again.  Four TMEM slots where two accumulators fit beside
     // them; two where that makes room for a second accumulator (BN=240).
-    static constexpr int kSfSlots = 8;
+    static constexpr int kSfSlots = S32 ? 4 : 8;    // (32-K scale slots are four times larger)
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots =
         (2 * kAccCols + 4 * kSfCols <= 512 || 2 * kAccCols + 2 * kSfCols > 512) ? 4 : 2;
@@ -95,7 +100,7 @@ struct Bs2Config {
     static constexpr int kStageBytes = kABytes + kBBytes;
     // bytes a K-block's loads deliver (FP4 B: the packed codes, half its stage)
     static constexpr int kTxBytes = kABytes + (B4 ? kBBytes / 2 : kBBytes);
-    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfaBytes = 512 * kSfaKb;
     static constexpr int kSfbBytes = 512 * kSfbChunks * kSfbKb;
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
     static constexpr int kEpiChunk = 16;
@@ -152,7 +157,7 @@ struct Bs2Config {
 // of the FP32-output GEMMs).
 constexpr int kF32StageBufs = 4;
 template <int BN, int MP, int LAY, bool F32>
-using Bs2Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0, F32 ? kF32StageBufs : 0>;
+using Bs2Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0, F32 ? kF32StageBufs : 0, (LAY & 8) != 0>;
 
 struct PairTile {
     int a_row0;      // this CTA's first row in the 2-D view of A (and D)
@@ -290,7 +295,8 @@ __device__ __forceinline__ void build_pair_prefix(const GemmParams &p, int *pref
         else if (threadIdx.x < 64) warp0_prefix_sums(info, E, threadIdx.x - 32);
         __syncthreads();
         // more K than the operands hold: the loads past the end read zeros, the words nothing
-        if (threadIdx.x == 0 && p.status && (prefix[E] > p.num_k_blocks || info[E] > p.sfa_slices))
+        if (threadIdx.x == 0 && p.status &&
+            (prefix[E] > p.num_k_blocks || ((p.layout & 8) ? prefix[E] : info[E]) > p.sfa_slices))
             atomicOr(p.status, DG_DEV_BAD_GROUP);
         return;
     }
@@ -376,7 +382,8 @@ __device__ __forceinline__ void get_pair_tile(const GemmParams &p, const int *pr
         const int m0 = (u - e * p.num_m_blocks) * MP + rank * (MP / 2);
         tile.a_row0 = m0;
         tile.sfa_x = m0;
-        tile.sfa_y0 = info[e];
+        // packed scale rows: per group 4 K-blocks a row; 32-K scales: one row a K-block
+        tile.sfa_y0 = (p.layout & 8) ? prefix[e] : info[e];
         tile.d_row0 = e * p.group_rows + m0;
         const int v = p.group_rows - m0;
         tile.valid_rows = v <= 0 ? 0 : (v < MP / 2 ? v : MP / 2);
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_b2,
                        const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
-    constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0;
+    constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0, S32 = (LAY & 8) != 0;
     static_assert(!B4 || (!A_MN && !B_MN && !F32), "FP4 B: K-major operands, bf16 D");
     using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
     static_assert(!(A_MN || B_MN) || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
@@ -666,15 +673,20 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             const uint32_t idesc = idesc_base | (sf << 4) | (sf << 29);
                             const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(j * (Cfg::kABytes >> 4));
                             const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(j * (Cfg::kB1Bytes >> 4));
-                            // FP4 B: this K-block's B cells, whose byte k scales the k-th 32 K
+                            // FP4 B (and 32-K scales): this K-block's B cells, whose byte k
+                            // scales the k-th 32 K; 32-K scales: the same for A's cells
                             constexpr int kSfbRegionCols = MP == 256 ? 4 * Cfg::kSfbChunks : 4;
-                            const uint32_t sfb_tmem =
-                                sfa_tmem + 4 + (B4 ? static_cast<uint32_t>((kb & 3) * kSfbRegionCols) : 0u);
+                            const uint32_t sfb_tmem = sfa_tmem + 4 * Cfg::kSfaKb +
+                                                      ((B4 || S32) ? static_cast<uint32_t>((kb & 3) * kSfbRegionCols) : 0u);
+                            const uint32_t sfa_cells = sfa_tmem + (S32 ? static_cast<uint32_t>(4 * (kb & 3)) : 0u);
 #pragma unroll
                             for (int k = 0; k < kBlockK / 32; ++k) {
-                                const uint32_t idesc_k =
-                                    B4 ? (idesc_base | (static_cast<uint32_t>(k) << 4) | (sf << 29)) : idesc;
-                                tc_mma_mxf8_pair(d_tmem, a_desc + kStepA * k, b_desc + kStepB * k, idesc_k, sfa_tmem,
+                                // instruction descriptor: B's scale-factor id in bits 4-5, A's in 29-30
+                                const uint32_t sfk = static_cast<uint32_t>(k);
+                                const uint32_t idesc_k = S32  ? (idesc_base | (sfk << 4) | (sfk << 29))
+                                                         : B4 ? (idesc_base | (sfk << 4) | (sf << 29))
+                                                              : idesc;
+                                tc_mma_mxf8_pair(d_tmem, a_desc + kStepA * k, b_desc + kStepB * k, idesc_k, sfa_cells,
                                                  sfb_tmem, (kb | k) != 0);
                                 if constexpr (Cfg::kBN2 > 0) {
                                     // columns [kBN1, BN): their accumulator columns, B rows and
@@ -777,10 +789,13 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     cp_async_4(dst0 + 4u * w, in ? base + static_cast<int64_t>(y) * ld + x : base, in ? 4u : 0u);
                 };
                 const int ya = st.sfa_y0 + lj, yb = st.sfb_y0 + lj;
+                // 32-K scales: one packed row per K-block, the group's 4 rows in 4 regions
 #pragma unroll
-                for (int q = 0; q < Cfg::kARows / 32; ++q)
-                    copy_word(p.sfa_words, p.sfa_ld, p.sfa_slices, st.sfa_x + 32 * q + static_cast<int>(lane), ya,
-                              4 * lane + q);
+                for (int ja = 0; ja < Cfg::kSfaKb; ++ja)
+#pragma unroll
+                    for (int q = 0; q < Cfg::kARows / 32; ++q)
+                        copy_word(p.sfa_words, p.sfa_ld, p.sfa_slices, st.sfa_x + 32 * q + static_cast<int>(lane),
+                                  S32 ? st.sfa_y0 + 4 * lj + ja : ya, 128 * ja + 4 * lane + q);
                 if constexpr (MP == 256) {
                     // FP4 B: one packed row per K-block, the group's 4 rows in 4 regions
 #pragma unroll
@@ -791,8 +806,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                             for (int q = 0; q < 4; ++q)
                                 copy_word(p.sfb_words, p.sfb_ld, p.sfb_slices,
                                           st.n0 + 128 * c + 32 * q + static_cast<int>(lane),
-                                          B4 ? st.sfb_y0 + 4 * lj + jj : yb,
-                                          128 + 128 * (jj * Cfg::kSfbChunks + c) + 4 * lane + q);
+                                          (B4 || S32) ? st.sfb_y0 + 4 * lj + jj : yb,
+                                          128 * Cfg::kSfaKb + 128 * (jj * Cfg::kSfbChunks + c) + 4 * lane + q);
                 } else {
                     constexpr int kHalf = BN / 2;
 #pragma unroll
@@ -824,7 +839,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             fence_proxy_async_smem();                     // visible to tcgen05.cp
             __syncwarp();
             uint32_t *sfa_buf = reinterpret_cast<uint32_t *>(smem_sf + slot * Cfg::kSfSlotBytes);
-            uint32_t *sfb_buf = sfa_buf + 128;
+            uint32_t *sfb_buf = sfa_buf + 128 * Cfg::kSfaKb;
             if (!leader) {
                 // tell the leader this CTA's words for the group are in place
                 if (lane == 0) mbar_arrive_remote(leader_peer + slot * 8);
@@ -837,11 +852,13 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 if (lane == 0) {
                     tc_fence_after_sync();
                     const uint32_t sfa_tmem = tmem_base + sf_col0 + tslot * Cfg::kSfCols;
-                    tc_cp_32x128b_warpx4_pair(sfa_tmem, make_desc_sf_32x128b(smem_u32(sfa_buf)));
+#pragma unroll
+                    for (int ja = 0; ja < Cfg::kSfaKb; ++ja)
+                        tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 * ja, make_desc_sf_32x128b(smem_u32(sfa_buf + 128 * ja)));
                     if constexpr (MP == 256) {
 #pragma unroll
                         for (int c = 0; c < Cfg::kSfbKb * Cfg::kSfbChunks; ++c)
-                            tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 + 4 * c,
+                            tc_cp_32x128b_warpx4_pair(sfa_tmem + 4 * Cfg::kSfaKb + 4 * c,
                                                       make_desc_sf_32x128b(smem_u32(sfb_buf + c * 128)));
                     } else {
 #pragma unroll

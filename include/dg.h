@@ -334,7 +334,7 @@ int64_t dg_packed_sf_words(int batch, int mn, int k);
  *   d    FP32 [num_groups][m][n] contiguous.
  *   c, d, a, b, sfa, sfb 16-byte aligned; m, n multiples of 4.
  *   m == 0, n == 0 or num_groups == 0 is a no-op; all ks 0 gives D = C.
- *   Runs on 256x256 CTA pairs, one persistent launch over all groups.
+ *   Runs on 256x224 CTA pairs, one persistent launch over all groups.
  */
 dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const void *sfa, const void *b,
                                               int64_t ldb, const void *sfb, const float *c, float *d, int m,
@@ -355,6 +355,43 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void *a, int64_t lda, const 
  */
 dg_status dg_transform_sf_k_grouped(const float *sf, int mn, const int *ks, int num_groups, void *out,
                                     int32_t *status_dev, void *stream);
+
+/*
+ * dg_k_grouped_fp8_gemm_tn_contiguous_k32 -- the K-grouped GEMM above with its
+ * scales at a K granularity of 32, the form in which the pages' library takes
+ * pre-packed int32 scales for this layout (PaperTrace "02 · DeepGEMM 技术解析"
+ * §3.3: the int32 path is accepted only at gran_k = 32):
+ *
+ *   D[e][m,n] = C[e][m,n] + sum over group e's k of A[k,m] sa(k/32, m) * B[k,n] sb(k/32, n)
+ *
+ *   Arguments as for dg_k_grouped_fp8_gemm_tn_contiguous, except the scales:
+ *   sfa, sfb  packed UE8M0 int32 [K_total/128][m] and [K_total/128][n] (no MN
+ *        padding, m and n multiples of 4): row r holds, in byte j, the scale of
+ *        K rows 128r + 32j .. 128r + 32j + 31 (each group's 32-row scale rows
+ *        packed 4 per word on their own; group sizes being multiples of 128, no
+ *        word is partial).  Build them from FP32 scales with
+ *        dg_transform_sf_k_grouped_k32.
+ *   Runs on 256x192 CTA pairs.
+ */
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous_k32(const void *a, int64_t lda, const void *sfa, const void *b,
+                                                  int64_t ldb, const void *sfb, const float *c, float *d, int m,
+                                                  int n, const int *ks, const int32_t *ks_dev, int num_groups,
+                                                  int32_t *status_dev, void *stream);
+
+/*
+ * dg_transform_sf_k_grouped_k32 -- FP32 scales of the K-grouped layout at a K
+ * granularity of 32 into the packed form of dg_k_grouped_fp8_gemm_tn_contiguous_k32
+ * (PaperTrace §3.3: each group packed on its own, 4 rows per int32, no MN padding).
+ *   sf   FP32 [K_total/32][mn], mn contiguous; row r = the scales of K rows
+ *        32r .. 32r + 31 of the concatenated groups.
+ *   ks   HOST int array [num_groups], multiples of 128.
+ *   out  int32 [K_total/128][mn]: byte j of row q of group e =
+ *        (bits(sf[K_e/32 + 4q + j][i]) >> 23) & 0xff; a non-power-of-two scale
+ *        is truncated and sets DG_DEV_INEXACT_SCALE.
+ *   mn % 4 == 0 (else DG_ERR_LAYOUT); ks invalid -> DG_ERR_INVALID_ARG.
+ */
+dg_status dg_transform_sf_k_grouped_k32(const float *sf, int mn, const int *ks, int num_groups, void *out,
+                                        int32_t *status_dev, void *stream);
 
 /* Packed scale rows of the K-grouped layout: sum_e ceil(ks[e] / 512), or -1
  * if ks is invalid (see dg_k_grouped_fp8_gemm_tn_contiguous) or the count

@@ -106,6 +106,16 @@ def test_k_grouped_host_validation_without_gpu(lib):
     assert call(m=-4) == 1
     assert lib.dg_transform_sf_k_grouped(P(16), 6, ks, 4, P(16), None, None) == 3
     assert lib.dg_transform_sf_k_grouped(P(16), 8, bad, 2, P(16), None, None) == 1
+    # the same rules for the scales at a K granularity of 32
+    def call32(m=256, n=256, c=16, ks_arr=ks, groups=4):
+        return lib.dg_k_grouped_fp8_gemm_tn_contiguous_k32(P(16), 256, P(16), P(16), 256, P(16), P(c), P(16), m,
+                                                           n, ks_arr, P(16), groups, None, None)
+    assert call32(c=0) == 1
+    assert call32(ks_arr=bad, groups=2) == 1
+    assert call32(n=258) == 3
+    assert call32(m=0) == 0
+    assert lib.dg_transform_sf_k_grouped_k32(P(16), 6, ks, 4, P(16), None, None) == 3
+    assert lib.dg_transform_sf_k_grouped_k32(P(16), 8, bad, 2, P(16), None, None) == 1
 
 
 def test_fp4_and_layout_host_validation_without_gpu(lib):

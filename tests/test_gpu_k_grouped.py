@@ -163,3 +163,75 @@ def test_k_grouped_workload_sampled(orc):
                                         case.sfb.double().numpy(), case.ks, case.c.numpy(), es, ms, ns)
     got = d[torch.from_numpy(es).to(DEV), torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)].cpu().numpy()
     _close_f32(got, ref, "weight-gradient workload")
+
+
+# ---------------------------------------------------------------- scales at a K granularity of 32
+
+def _run32(case, pad=0, in_place=False):
+    E = len(case.ks)
+    M, N = case.a.shape[1], case.b.shape[1]
+    a, b = _padded(case.a, pad), _padded(case.b, pad)
+    sfa = binding.dg_transform_sf_k_grouped_k32(case.sfa.to(DEV), case.ks)
+    sfb = binding.dg_transform_sf_k_grouped_k32(case.sfb.to(DEV), case.ks)
+    c = case.c.to(DEV)
+    d = c if in_place else torch.full((E, M, N), 7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.dg_k_grouped_fp8_gemm_tn_contiguous_k32(a, sfa, b, sfb, d, case.ks, c=c, status=st)
+    cfg = binding.last_config()
+    torch.cuda.synchronize()
+    return d, sfa, sfb, int(st.item()), cfg
+
+
+@pytest.mark.parametrize("E,M,N,ks,pad", [(3, 256, 256, [128, 256, 384], 0),
+                                          (4, 320, 264, [256, 0, 640, 128], 0),
+                                          (2, 1000, 520, [1152, 128], 32),
+                                          (5, 64, 1032, [128, 128, 0, 0, 896], 16)])
+def test_k_grouped_k32_matches_oracle(orc, E, M, N, ks, pad):
+    """Scales every 32 rows of K (PaperTrace DeepGEMM §3.3): packing bit for bit
+    against the oracle's, D against the oracle at the FP32 bar, in place and not."""
+    case = inputs.k_grouped_case(E, M, N, seed=E + M + N + 32, ks=ks, gran_k=32)
+    d, sfa, sfb, status, cfg = _run32(case, pad)
+    assert status == 0
+    assert cfg["kind"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 192, cfg
+    assert np.array_equal(sfa.cpu().numpy(), orc.k_grouped_pack_sf(case.sfa.numpy(), ks, gran_k=32))
+    assert np.array_equal(sfb.cpu().numpy(), orc.k_grouped_pack_sf(case.sfb.numpy(), ks, gran_k=32))
+    ref = orc.k_grouped_gemm_tn_k32(u8(case.a), case.sfa.double().numpy(), u8(case.b), case.sfb.double().numpy(),
+                                    ks, case.c.numpy())
+    got = d.cpu().numpy()
+    for e in range(E):
+        if ks[e] == 0:
+            assert np.array_equal(got[e], case.c[e].numpy()), f"empty group {e}: D must be C"
+        else:
+            _close_f32(got[e], ref[e], f"group {e} of {ks}")
+    d_in, _, _, st_in, _ = _run32(case, pad, in_place=True)
+    assert st_in == 0 and torch.equal(d_in, d)
+
+
+def test_k_grouped_k32_equals_k128_on_equal_scales():
+    """32-row scales whose four rows in each 128-row block are equal give the
+    128-row GEMM's result bit for bit (the same products in the same order; the
+    two calls run different tile widths)."""
+    ks = [256, 384, 0, 128]
+    E, M, N = 4, 512, 776
+    case = inputs.k_grouped_case(E, M, N, seed=76, ks=ks)
+    d128, _, _, st128, _ = _run(case)
+    case32 = inputs.KGroupedCase(case.a, case.sfa.repeat_interleave(4, 0).contiguous(), case.b,
+                                 case.sfb.repeat_interleave(4, 0).contiguous(), case.c, ks)
+    d32, _, _, st32, cfg = _run32(case32)
+    assert st128 == 0 and st32 == 0 and cfg["block_n"] == 192
+    assert torch.equal(d32, d128)
+
+
+def test_k_grouped_k32_workload_sampled(orc):
+    """The weight-gradient workload (8 groups, M=4096, N=7168) with 32-row scales,
+    in place, on sampled outputs."""
+    E, M, N = 8, 4096, 7168
+    case = inputs.k_grouped_case(E, M, N, seed=33, gran_k=32)
+    d, _, _, status, _ = _run32(case, in_place=True)
+    assert status == 0
+    rng = np.random.default_rng(6)
+    es, ms, ns = rng.integers(0, E, 3000), rng.integers(0, M, 3000), rng.integers(0, N, 3000)
+    ref = orc.k_grouped_gemm_tn_k32_sampled(u8(case.a), case.sfa.double().numpy(), u8(case.b),
+                                            case.sfb.double().numpy(), case.ks, case.c.numpy(), es, ms, ns)
+    got = d[torch.from_numpy(es).to(DEV), torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)].cpu().numpy()
+    _close_f32(got, ref, "weight-gradient workload, 32-row scales")
