@@ -557,6 +557,14 @@ def run_ours(args, rank, world, local_rank):
             gemm_ms[i] += gemm_ev[i][0].elapsed_time(gemm_ev[i][1]) / reps
     del graph
 
+    # ---------------- per-kernel device time of each GEMM inside the step
+    # The step's six launches captured with a timing event between launches (event
+    # record nodes, so each GEMM starts when the previous one has finished), replayed
+    # behind the L2 flush like the timed steps: the time between two events is one
+    # GEMM's launch inside the step.  None where torch cannot record timing events in
+    # a captured graph.
+    step_gemm_ms = measure_step_launches(probs, flush, reps, status, stream)
+
     # ---------------- end to end through the public API with host buffers
     for p in probs:
         p["sfa_packed_host"] = p["sfa"].cpu().pin_memory()
@@ -582,19 +590,26 @@ def run_ours(args, rank, world, local_rank):
     # (tensor-bound); the three M=128 GEMMs run the single-CTA kernel (HBM-bound).
     big = [i for i, p in enumerate(probs) if p["shape"][0] > 128]
     skinny = [i for i, p in enumerate(probs) if p["shape"][0] <= 128]
-    big_ms = sum(gemm_ms[i] for i in big)
+    launch_ms = step_gemm_ms if step_gemm_ms is not None else gemm_ms
+    big_ms = sum(launch_ms[i] for i in big)
     achieved = sum(flops(*probs[i]["shape"]) for i in big) / (big_ms * 1e-3) / 1e12
-    skinny_ms = sum(gemm_ms[i] for i in skinny)
+    skinny_ms = sum(launch_ms[i] for i in skinny)
     skinny_gbs = sum(gemm_bytes(*probs[i]["shape"]) for i in skinny) / (skinny_ms * 1e-3) / 1e9
     other = measure_other_workloads(dev, flush, min(20, max(5, args.steps // 4)), stream) if rank == 0 else []
     lib_fp8 = measure_library_fp8_peak(dev, stream) if rank == 0 else None
     per_gemm = []
-    for p, ms, cfg in zip(probs, gemm_ms, bn_used):
+    for i, (p, ms, cfg) in enumerate(zip(probs, gemm_ms, bn_used)):
         m, n, k = p["shape"]
-        per_gemm.append({"m": m, "n": n, "k": k, "us": round(ms * 1e3, 2),
-                         "tflops": round(flops(m, n, k) / (ms * 1e-3) / 1e12, 1),
-                         "gbs": round(gemm_bytes(m, n, k) / (ms * 1e-3) / 1e9, 1),
+        lm = launch_ms[i]
+        per_gemm.append({"m": m, "n": n, "k": k, "us": round(lm * 1e3, 2),
+                         "tflops": round(flops(m, n, k) / (lm * 1e-3) / 1e12, 1),
+                         "gbs": round(gemm_bytes(m, n, k) / (lm * 1e-3) / 1e9, 1),
+                         "isolated_us": round(ms * 1e3, 2),
                          "block_n": cfg["block_n"], "grid": cfg["grid"]})
+    launch_timing = ("each GEMM's launch inside the step (CUDA events between the step's launches, "
+                     "replayed behind the L2 flush); per_gemm.isolated_us: one launch alone after the flush"
+                     if step_gemm_ms is not None else
+                     "one launch alone after the L2 flush (CUDA events around it)")
     traffic = load_traffic()
     big_traffic = skinny_traffic = None
     if traffic is not None:
@@ -626,6 +641,7 @@ def run_ours(args, rank, world, local_rank):
                          "peak_note": f"fp8 = {peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio), of {peaks['source']}",
                          "kernel": "dg_bs2_gemm_kernel (CTA pairs): the three M=4096 GEMMs, "
                                    "flops / summed launch time",
+                         "timing": launch_timing,
                          "traffic": big_traffic},
             "roofline_skinny": {"bound": "hbm", "achieved": round(skinny_gbs, 1),
                                 "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
@@ -633,6 +649,7 @@ def run_ours(args, rank, world, local_rank):
                                 "kernel": "the three M=128 GEMMs (dg_bs2_gemm_kernel on 128-row CTA pairs "
                                           "where the load model prefers them, else dg_bs_gemm_kernel): "
                                           "algorithmic bytes / summed launch time, of " + peaks["source"],
+                                "timing": launch_timing,
                                 "traffic": skinny_traffic},
             "per_gemm": per_gemm,
             "other_workloads": other,
@@ -863,6 +880,39 @@ def run_case(args):
                       "tflops": round(flops(m, n, k) / (us * 1e-6) / 1e12, 1),
                       "gbs": round((m * k + n * k // 2 + 2 * m * n if args.fp4 else gemm_bytes(m, n, k))
                                    / (us * 1e-6) / 1e9, 1), "config": cfg}))
+
+
+def measure_step_launches(probs, flush, reps, status, stream):
+    """Device time (ms, mean over `reps` replays) of each GEMM launch of the step:
+    the six launches captured in a CUDA graph with a timing event recorded between
+    consecutive launches, each replay behind the L2 flush.  None if torch cannot
+    record timing events inside a captured graph."""
+    import torch
+
+    from block_scaled_fp8_gb300 import binding
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(probs) + 1)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            evs[0].record()
+            for i, p in enumerate(probs):
+                binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
+                evs[i + 1].record()
+        torch.cuda.synchronize()
+        out = [0.0] * len(probs)
+        for r in range(reps + 1):
+            flush.fill_(r)
+            g.replay()
+            torch.cuda.synchronize()
+            if r == 0:
+                continue   # the graph's first replay uploads it
+            for i in range(len(probs)):
+                out[i] += evs[i].elapsed_time(evs[i + 1]) / reps
+        del g
+        return out
+    except (TypeError, RuntimeError):
+        torch.cuda.synchronize()
+        return None
 
 
 def measure_pinned_copies(dev, stream, nbytes=256 * 1024 * 1024, reps=5):
