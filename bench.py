@@ -251,6 +251,10 @@ def measure_other_workloads(dev, flush, reps, stream):
     record(f"dense NT + C {m}x{n}x{k}, FP32 C and D",
            lambda: binding.dg_fp8_gemm_nt_f32(c_.a, sfa, c_.b, sfb, d32, c=c32, status=status),
            flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n + 4 * m * n, {"d": "fp32"})
+    # the same with C = D (accumulated in place at L2; D keeps growing, which the timing ignores)
+    record(f"dense NT + C {m}x{n}x{k}, FP32 C = D in place",
+           lambda: binding.dg_fp8_gemm_nt_f32(c_.a, sfa, c_.b, sfb, c32, c=c32, status=status),
+           flops(m, n, k), gemm_bytes(m, n, k) + 2 * m * n + 4 * m * n, {"d": "fp32, in place"})
     # the same GEMM with M- / N-contiguous operands (A stored [K, M], B [K, N])
     a_t = c_.a.view(torch.uint8).t().contiguous().view(torch.float8_e4m3fn)
     b_t = c_.b.view(torch.uint8).t().contiguous().view(torch.float8_e4m3fn)

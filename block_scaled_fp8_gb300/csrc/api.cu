@@ -328,10 +328,14 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
                             b2_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     }
     if (!b2_rows) maps.b2 = maps.b;   // not read
-    // D store boxes: 32 rows of 32 bytes (16 bf16 or 8 FP32 columns)
+    // D store boxes: 32 rows of 32 bytes (16 bf16 columns), or 64 bytes (16 FP32 columns, or
+    // 32 bf16 columns with C)
     if (f32)
-        ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, o.d, p.n, o.d_rows, o.ldd * 4, 8, 32,
-                        CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+        ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, o.d, p.n, o.d_rows, o.ldd * 4, 16, 32,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    else if (with_c)   // the bf16 C epilogue stores two adjacent chunks per box
+        ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 32,
+                        32, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     else
         ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                         32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);

@@ -894,8 +894,10 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         uint32_t buf = 0;
         uint8_t *stage_out = smem_stage_out + ew * Cfg::kStageBufs * Cfg::kStageBufBytes;
         // C (bf16) of one chunk of this thread's row; zero outside [rows, n)
+        // (the bf16 C epilogue gives each warp of a quadrant a contiguous half of the
+        // chunks, so that two adjacent chunks go out in one store box)
         auto load_c = [&](const PairTile &tl, int j, uint32_t (&dst)[8]) {
-            const int c = 2 * j + half;
+            const int c = j + static_cast<int>(half) * Cfg::kChunksPerWarp;
             const int row = tl.d_row0 + row_off + lane;
             const int col0 = tl.n0 + col_off + c * Cfg::kEpiChunk;
             if (p.c_v8 && c < Cfg::kNumChunks && row < p.rows && col0 + 16 <= p.n) {
@@ -1002,6 +1004,20 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                     }
                     return;
                 }
+                if constexpr (WITH_C && !F32) {
+                    // the C epilogue's store map is 32 columns wide: a lone chunk goes out
+                    // directly (it lies inside the tile, and columns past n are skipped)
+                    const int drow = tile.d_row0 + row_off + static_cast<int>(lane);
+                    if (drow < p.rows) {
+                        uint16_t *dp = p.d + static_cast<int64_t>(drow) * p.ldd + col0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (col0 + 8 * h < p.n)
+                                *reinterpret_cast<uint4 *>(dp + 8 * h) =
+                                    make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+                    }
+                    return;
+                }
                 uint8_t *sbuf = stage_out + buf * Cfg::kStageBufBytes;
                 if (lane == 0) bulk_wait_group_read<Cfg::kStageBufs - 1>();
                 __syncwarp();
@@ -1036,8 +1052,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 if (has_next) prefetch_c(next_tile);
             }
             if constexpr (F32) {
-                // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> two
-                // 8-column FP32 boxes through the staging buffers; the accumulator is
+                // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> one
+                // 16-column FP32 box through a pair of staging buffers; the accumulator is
                 // released after its last chunk is read
                 const int row = tile.d_row0 + row_off + static_cast<int>(lane);
                 // D = C in place: an empty group leaves D as it is; the next tile's rows go to L2
@@ -1103,27 +1119,30 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                         }
                         continue;
                     }
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        if (col0 + 8 * part >= p.n) break;
-                        uint8_t *sbuf = stage_out + buf * Cfg::kStageBufBytes;
-                        if (lane == 0) bulk_wait_group_read<Cfg::kStageBufs - 1>();
+                    {
+                        // one 16-column FP32 box (32 rows of 64 bytes) per chunk, through
+                        // staging buffer pairs: a TMA store or reduce costs the SM's TMA unit
+                        // per operation, so fewer, larger boxes drain the tile sooner
+                        constexpr int NB2 = Cfg::kStageBufs / 2;
+                        static_assert(NB2 >= 1, "FP32 staging: pairs of buffers");
+                        uint8_t *sbuf = stage_out + buf * 2 * Cfg::kStageBufBytes;
+                        if (lane == 0) bulk_wait_group_read<NB2 - 1>();
                         __syncwarp();
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            // 32-byte swizzle: 16-byte unit h of row r sits at unit h ^ ((r >> 2) & 1)
-                            const uint32_t off = lane * 32 + ((h ^ ((lane >> 2) & 1)) * 16);
-                            const float *x = f + 8 * part + 4 * h;
+                        for (int h = 0; h < 4; ++h) {
+                            // 64-byte swizzle: 16-byte unit h of row r sits at unit h ^ ((r >> 1) & 3)
+                            const uint32_t off = lane * 64 + ((h ^ ((lane >> 1) & 3)) * 16);
+                            const float *x = f + 4 * h;
                             *reinterpret_cast<float4 *>(sbuf + off) = make_float4(x[0], x[1], x[2], x[3]);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if (in_place) tma_reduce_add_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
-                            else tma_store_2d(&tm_d, sbuf, col0 + 8 * part, tile.d_row0 + row_off);
+                            if (in_place) tma_reduce_add_2d(&tm_d, sbuf, col0, tile.d_row0 + row_off);
+                            else tma_store_2d(&tm_d, sbuf, col0, tile.d_row0 + row_off);
                             bulk_commit_group();
                         }
-                        buf = buf + 1 == Cfg::kStageBufs ? 0 : buf + 1;
+                        buf = buf + 1 == NB2 ? 0 : buf + 1;
                     }
                 }
                 tc_fence_before_sync();
@@ -1133,13 +1152,15 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             } else if constexpr (WITH_C) {
                 // each chunk's bf16(acc + C) overwrites that chunk's C registers; the
                 // accumulator is released once every chunk is read (the MMAs of the tile
-                // after next need it), and only then are the chunks stored
+                // after next need it), and only then are the chunks stored, two adjacent
+                // chunks (32 columns, 64-byte rows) per TMA store: the SM's TMA unit, where
+                // the stores queue behind the operand loads, costs per operation
 #pragma unroll
                 for (int j0 = 0; j0 < Cfg::kChunksPerWarp; j0 += 2) {
                     uint32_t v[2][16];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int c = 2 * (j0 + u) + half;
+                        const int c = (j0 + u) + static_cast<int>(half) * Cfg::kChunksPerWarp;
                         if (j0 + u < Cfg::kChunksPerWarp && c < Cfg::kNumChunks)
                             tmem_ld_32x32b_x16(tmem_base + ((quad * 32) << 16) + acc * ACC + c * Cfg::kEpiChunk, v[u]);
                     }
@@ -1147,7 +1168,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int j = j0 + u;
-                        const int c = 2 * j + half;
+                        const int c = j + static_cast<int>(half) * Cfg::kChunksPerWarp;
                         if (j >= Cfg::kChunksPerWarp || c >= Cfg::kNumChunks) continue;
                         reg_fence16(v[u]);
 #pragma unroll
@@ -1164,9 +1185,37 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                 if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
                 if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
 #pragma unroll
-                for (int j = 0; j < Cfg::kChunksPerWarp; ++j) {
-                    const int c = 2 * j + half;
-                    if (c < Cfg::kNumChunks) store_chunk(cpk[j], c);
+                for (int j = 0; j < Cfg::kChunksPerWarp; j += 2) {
+                    const int c = j + static_cast<int>(half) * Cfg::kChunksPerWarp;
+                    if (c >= Cfg::kNumChunks) continue;
+                    const bool pair = j + 1 < Cfg::kChunksPerWarp && c + 1 < Cfg::kNumChunks;
+                    const int col0 = tile.n0 + col_off + c * Cfg::kEpiChunk;
+                    if (!pair || tile.valid_rows < MP / 2) {
+                        // a lone chunk, or rows ending inside the tile: chunk by chunk
+                        store_chunk(cpk[j], c);
+                        if (pair) store_chunk(cpk[j + 1], c + 1);
+                        continue;
+                    }
+                    if (tile.valid_rows == 0 || col0 >= p.n) continue;
+                    constexpr int NB2 = Cfg::kStageBufs / 2;
+                    static_assert(NB2 >= 1, "bf16 C staging: pairs of buffers");
+                    uint8_t *sbuf = stage_out + (buf % NB2) * 2 * Cfg::kStageBufBytes;
+                    if (lane == 0) bulk_wait_group_read<NB2 - 1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        // 64-byte swizzle: 16-byte unit h of row r sits at unit h ^ ((r >> 1) & 3)
+                        const uint32_t off = lane * 64 + ((h ^ ((lane >> 1) & 3)) * 16);
+                        const uint32_t *x = (h < 2 ? cpk[j] : cpk[j + 1]) + 4 * (h & 1);
+                        *reinterpret_cast<uint4 *>(sbuf + off) = make_uint4(x[0], x[1], x[2], x[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, sbuf, col0, tile.d_row0 + row_off);
+                        bulk_commit_group();
+                    }
+                    ++buf;
                 }
             } else {
                 // the whole row segment to registers, release the accumulator, then store
