@@ -339,6 +339,16 @@ dg_status launch_pair(GemmParams &p, const BsOperands &o, int mp, int bn, int64_
     else
         ok &= encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.d, p.n, o.d_rows, o.ldd * 2, 16,
                         32, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    // bf16 C of a dense GEMM whose tile is whole 32-column boxes: the kernel keeps the
+    // C tile in shared memory, loaded by TMA (boxes of 32 rows x 32 columns, as D's)
+    const bool c_tile = !f32 && with_c && mp == 256 && bn % 32 == 0 && bn <= 256;
+    if (c_tile && p.mode != kModeDense) return DG_ERR_UNSUPPORTED;   // (that layout has no grouped prefix)
+    p.c_tma = (c_tile && (reinterpret_cast<uintptr_t>(p.c) & 15u) == 0 && (p.ldc * 2) % 16 == 0) ? 1 : 0;
+    if (p.c_tma)
+        ok &= encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.c, p.n, o.d_rows, p.ldc * 2, 32, 32,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    else
+        maps.c = maps.d;   // not read
     if (!ok) return DG_ERR_CUDA;
     set_scale_words(p, o);
     p.c_v8 = (p.c != nullptr && (reinterpret_cast<uintptr_t>(p.c) & 31u) == 0 && p.ldc % 16 == 0) ? 1 : 0;

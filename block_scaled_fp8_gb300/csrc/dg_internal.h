@@ -47,6 +47,7 @@ struct GemmParams {
     int ab_3d;           // A/B tensor maps are the 3-D K-blocked views: one load per ring slot
     int c_v8;            // bf16 C rows are 32-byte aligned (base and ldc): 16 columns in one load
     int c_in_place;      // FP32 C is D itself (same pointer and stride): D is accumulated into at L2
+    int c_tma;           // bf16 C goes through shared memory by TMA (dense pair GEMMs, 16-byte aligned rows)
     int layout;          // operand layouts: bit 0 A MN-major ([K][M]), bit 1 B MN-major ([K][N]),
                          // bit 2 B FP4 (E2M1, one scale per 32 K)
     // packed UE8M0 scale words, [slices][ld] int32 with ld = align4(mn); the
@@ -64,6 +65,7 @@ struct GemmParams {
 struct TensorMaps {
     CUtensorMap a, b, d;
     CUtensorMap b2;   // pair tiles wider than 256 columns: the second MMA's rows of B
+    CUtensorMap c;    // the pair kernel's bf16 C boxes (C tile in shared memory)
 };
 
 // Per-instantiation launch information.

@@ -25,6 +25,9 @@
 // Ring slots group kGroupKb K-blocks under one barrier pair to keep the MMA
 // warp's per-K-block work below the tensor time.  Roles: warp 0 producer,
 // warp 1 MMA issuer (leader), warps 2-9 epilogue, warps 10-11 scale words.
+// A dense GEMM with bf16 C whose tile is whole 32-column boxes keeps each CTA's
+// C tile in shared memory: loaded by TMA a tile ahead, summed with the
+// accumulator in place, and stored by TMA from there.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -50,7 +53,11 @@ namespace dg {
 // S32: A and B scales every 32 K (K-grouped scales at a K granularity of 32): a
 // scale group holds one word per row of A and per column of B for each of its 4
 // K-blocks, the word's bytes being the K-block's four 32-K scales.
-template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false, int SB = 0, bool S32 = false>
+// CT: the bf16 C epilogue of a dense GEMM keeps this CTA's whole C tile in shared
+// memory (loaded by TMA a tile ahead, summed in place, stored by TMA from there);
+// the region doubles as the output staging of the register C path.
+template <int BN, int MP = 256, bool B_ATOM = false, bool B4 = false, int SB = 0, bool S32 = false,
+          bool CT = false>
 struct Bs2Config {
     // BN/2 rows of B per CTA fill whole 8-row swizzle atoms; pair MMAs take N % 16 == 0, N <= 256;
     // with MP=128 each half of N is whole 16-column epilogue chunks
@@ -79,6 +86,7 @@ struct Bs2Config {
     static constexpr int kSfaKb = S32 ? 4 : 1;                   // A words per row per group
     static_assert(!B4 || BN <= 256, "FP4 B: one MMA per K step");
     static_assert(!S32 || (MP == 256 && BN <= 256), "32-K scales: 256-row pairs, one MMA per K step");
+    static_assert(!CT || (MP == 256 && BN % 32 == 0 && BN <= 256), "C tile: 32-column boxes of a 256-row pair");
     static constexpr int kSfCols = 4 * kSfaKb + (MP == 256 ? 4 * kSfbChunks : 4) * kSfbKb;
     // Scale words pass through two rings: kSfSlots shared-memory slots (cp.async
     // destination, already in tcgen05.cp order) and kSfTmemSlots TMEM slots (what
@@ -89,7 +97,8 @@ struct Bs2Config {
     // TMEM completes, which is kSfSlots - kSfLookahead groups before the slot
     // is loaded again.  Four TMEM slots where two accumulators fit beside
     // them; two where that makes room for a second accumulator (BN=240).
-    static constexpr int kSfSlots = S32 ? 4 : 8;    // (32-K scale slots are four times larger)
+    // (32-K scale slots are four times larger; the C tile takes the room of two)
+    static constexpr int kSfSlots = S32 ? 4 : (CT ? 6 : 8);
     static constexpr int kSfLookahead = kSfSlots - 3;
     static constexpr int kSfTmemSlots =
         (2 * kAccCols + 4 * kSfCols <= 512 || 2 * kAccCols + 2 * kSfCols > 512) ? 4 : 2;
@@ -107,8 +116,9 @@ struct Bs2Config {
     static constexpr int kNumChunks = kAccCols / kEpiChunk;      // per TMEM lane quadrant
     static constexpr int kChunksPerWarp = (kNumChunks + 1) / 2;
     static constexpr int kSmemLimit = 232448;
-    // grouped-layout unit prefix + info (the 128-row pairs run dense problems only)
-    static constexpr int kPrefixBytes = MP == 256 ? (2 * kMaxPairPrefix + 1) * 4 : 0;
+    // grouped-layout unit prefix + info (the 128-row pairs, and the C tile's dense
+    // GEMMs, run dense problems only)
+    static constexpr int kPrefixBytes = (MP == 256 && !CT) ? (2 * kMaxPairPrefix + 1) * 4 : 0;
     // Operand stages: 256-row pairs keep up to 12 (slots of 4, 2 or 1 K-blocks, so
     // the MMA warp waits and commits once per slot).  128-row pairs stream B from
     // DRAM at a few bytes per MMA cycle, so what bounds them is the bytes in flight:
@@ -121,8 +131,16 @@ struct Bs2Config {
     // loads in the TMA unit, so more buffers keep more stores in flight.  As many
     // as fit (up to 4) without costing an operand stage.
     static constexpr int kStageBufBytes = 32 * kEpiChunk * 2;
+    // C tile: 32-column boxes of this CTA's rows (64-byte rows, 64-byte swizzle); a
+    // warp's 32 rows of a box are one TMA box of their own
+    static constexpr int kCBoxes = CT ? BN / 32 : 0;
+    static constexpr int kCBoxBytes = kARows * 64;
+    static constexpr int kCTileBytes = kCBoxes * kCBoxBytes;
+    static constexpr int region_bytes(int bufs) {
+        return kEpiWarps * bufs * kStageBufBytes > kCTileBytes ? kEpiWarps * bufs * kStageBufBytes : kCTileBytes;
+    }
     static constexpr int fixed_bytes(int bufs) {
-        return 1024 + kEpiWarps * bufs * kStageBufBytes + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
+        return 1024 + region_bytes(bufs) + kSfSlots * kSfSlotBytes + 512 + kPrefixBytes;
     }
     static constexpr int stages_by_smem(int bufs) { return (kSmemLimit - fixed_bytes(bufs)) / kStageBytes; }
     static constexpr int stages_cap(int bufs) {
@@ -130,8 +148,9 @@ struct Bs2Config {
     }
     static constexpr int kStageBufs =
         SB > 0 ? SB
+        : CT   ? 4
                : (MP == 128 ? 2 : (stages_cap(4) >= stages_cap(2) ? 4 : (stages_cap(3) >= stages_cap(2) ? 3 : 2)));
-    static constexpr int kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
+    static constexpr int kStagingBytes = region_bytes(kStageBufs);
     static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > kMaxStages ? kMaxStages : kStagesBySmem;
@@ -145,9 +164,11 @@ struct Bs2Config {
     static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(kSmemBytes > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
-    // full, empty, tfull, tempty, sf_peer, sfree, sf_ready, sf_tfree, drain; then
-    // the TMEM holder and abort flag, all before the unit prefix 512 bytes on
-    static constexpr int kNumBars = 2 * kRing + 2 * kNumAcc + 2 * kSfSlots + 2 * kSfTmemSlots + 1 + kSfWarps;
+    // full, empty, tfull, tempty, sf_peer, sfree, sf_ready, sf_tfree, drain, C tile
+    // (one per epilogue warp); then the TMEM holder and abort flag, all before the
+    // unit prefix 512 bytes on
+    static constexpr int kNumBars =
+        2 * kRing + 2 * kNumAcc + 2 * kSfSlots + 2 * kSfTmemSlots + 1 + kSfWarps + (CT ? kEpiWarps : 0);
     static_assert(kNumBars * 8 + 8 <= 512, "barrier region");
     static_assert(kSfSlots * kSfSlotBytes >= 2 * (kMaxPsumGroups + 1) * 4, "PSUM segments fit the scale ring");
 };
@@ -156,8 +177,13 @@ struct Bs2Config {
 // stage fewer where that is their price (that epilogue, not the MMAs, sets the pace
 // of the FP32-output GEMMs).
 constexpr int kF32StageBufs = 4;
-template <int BN, int MP, int LAY, bool F32>
-using Bs2Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0, F32 ? kF32StageBufs : 0, (LAY & 8) != 0>;
+// The bf16 C epilogue keeps its C tile in shared memory where the tile's columns
+// are whole 32-column boxes.
+template <int BN, int MP, bool WITH_C, bool F32>
+constexpr bool kCTile = WITH_C && !F32 && MP == 256 && BN % 32 == 0 && BN <= 256;
+template <int BN, int MP, int LAY, bool F32, bool WITH_C = false>
+using Bs2Cfg = Bs2Config<BN, MP, (LAY & 2) != 0, (LAY & 4) != 0, F32 ? kF32StageBufs : 0, (LAY & 8) != 0,
+                         kCTile<BN, MP, WITH_C, F32>>;
 
 struct PairTile {
     int a_row0;      // this CTA's first row in the 2-D view of A (and D)
@@ -445,10 +471,11 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     dg_bs2_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                        const __grid_constant__ CUtensorMap tm_b,
                        const __grid_constant__ CUtensorMap tm_b2,
-                       const __grid_constant__ CUtensorMap tm_d, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap tm_d,
+                       const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
     constexpr bool A_MN = (LAY & 1) != 0, B_MN = (LAY & 2) != 0, B4 = (LAY & 4) != 0, S32 = (LAY & 8) != 0;
     static_assert(!B4 || (!A_MN && !B_MN && !F32), "FP4 B: K-major operands, bf16 D");
-    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32, WITH_C>;
     static_assert(!(A_MN || B_MN) || (MP == 256 && BN <= 256), "MN-major operands: 256-row pair tiles, one MMA");
     constexpr int S = Cfg::kStages;
     constexpr int R = Cfg::kRing;
@@ -477,7 +504,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     uint64_t *sf_ready_bar = sf_sfree_bar + NSF;      // [NTS] leader: words in both TMEMs
     uint64_t *sf_tfree_bar = sf_ready_bar + NTS;      // [NTS] leader: MMAs done with the slot
     uint64_t *drain_bar = sf_tfree_bar + NTS;         // [1 + kSfWarps] MMA warp, scale warps
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1 + Cfg::kSfWarps);
+    uint64_t *cfull_bar = drain_bar + 1 + Cfg::kSfWarps;   // [kEpiWarps, C tile] a warp's C boxes landed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(cfull_bar + (Cfg::kCBoxes > 0 ? Cfg::kEpiWarps : 0));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + 512);  // grouped layouts
     int *pinfo = prefix + kMaxPairPrefix + 1;
@@ -493,9 +521,9 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
     const int psf_k = groups_per_tile;
 
     if (warp == 0) {
-        // the barriers are contiguous from full_bar to drain_bar; the lanes of warp 0
-        // initialise them, each fencing its own inits
-        const int num_bars = static_cast<int>(drain_bar + 1 + Cfg::kSfWarps - bars);  // <= Cfg::kNumBars
+        // the barriers are contiguous from full_bar to the TMEM holder; the lanes of
+        // warp 0 initialise them, each fencing its own inits
+        const int num_bars = static_cast<int>(reinterpret_cast<uint64_t *>(tmem_holder) - bars);  // <= kNumBars
         for (int i = static_cast<int>(lane); i < num_bars; i += 32) {
             uint64_t *b = bars + i;
             mbar_init(b, b >= tempty_bar && b < tempty_bar + NUM_ACC ? 2 * Cfg::kEpiWarps : 1);
@@ -508,6 +536,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         tma_prefetch_desc(&tm_b);
         if constexpr (Cfg::kBN2 > 0) tma_prefetch_desc(&tm_b2);
         tma_prefetch_desc(&tm_d);
+        if (Cfg::kCBoxes > 0 && p.c_tma) tma_prefetch_desc(&tm_c);
     }
     // Nothing above reads global memory: it overlaps the previous grid's tail when
     // launched as a programmatic dependent.  From here on every thread may read
@@ -619,8 +648,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
         // the leader waits for the last fill of every slot (both CTAs' bytes count there)
         if (lane == 0 && leader)
             for (int s = 0; s < R; ++s)
-                if (issued & (1u << s))
-                    mbar_wait(&full_bar[s], s < slot ? phase : phase ^ 1, ctl, DG_DEV_TIMEOUT);
+                if (issued & (1u << s)) mbar_wait_drain(&full_bar[s], s < slot ? phase : phase ^ 1, ctl);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader, whole warp)
@@ -966,10 +994,35 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                                                     col0 + 4 * q));
             }
         };
+        // C tile (dense bf16 C, TMA-aligned): this warp's 32 rows of every other
+        // 32-column box of the tile (boxes half, half + 2, ...) land in shared memory by
+        // TMA, are summed in place and go out by TMA from there; the next tile's boxes
+        // are loaded as soon as the stores have read them, a tile ahead of their use
+        const bool c_tma = Cfg::kCBoxes > 0 && p.c_tma;
+        constexpr int kMyBoxes = (Cfg::kCBoxes + 1) / 2;
+        uint8_t *const ctile = smem_stage_out + quad * 32 * 64;
+        uint32_t c_phase = 0;
+        bool c_pending = false;
+        auto load_ctile = [&](const PairTile &tl) {
+            if (lane == 0) {
+                const int nb = (Cfg::kCBoxes - static_cast<int>(half) + 1) / 2;
+                mbar_arrive_expect_tx(&cfull_bar[ew], static_cast<uint32_t>(nb) * 32u * 64u);
+#pragma unroll
+                for (int q = 0; q < kMyBoxes; ++q) {
+                    const int j = 2 * q + static_cast<int>(half);
+                    if (j < Cfg::kCBoxes)
+                        tma_load_2d(ctile + j * Cfg::kCBoxBytes, &tm_c, &cfull_bar[ew], tl.n0 + 32 * j,
+                                    tl.d_row0 + row_off);
+                }
+            }
+            __syncwarp();
+            c_pending = true;
+        };
         PairTile tile;
         if (pair_id < num_tiles) {
             get_pair_tile<BN, MP>(p, prefix, pinfo, num_units, psf_k, pair_id, rank, tile);
             if constexpr (WITH_C && !F32) prefetch_c(tile);
+            if (c_tma) load_ctile(tile);
             if constexpr (WITH_C && F32) {
                 prefetch_d32(tile);
                 if (!p.c_in_place) {
@@ -1037,7 +1090,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             // bf16 C of this tile into registers (the first tile's once its accumulator is
             // complete, so that its loads do not compete with the first operand loads)
             if constexpr (WITH_C && !F32) {
-                if (t != pair_id) {
+                if (t != pair_id && !c_tma) {
 #pragma unroll
                     for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
                 }
@@ -1045,11 +1098,71 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[acc], acc_phase, ctl, DG_DEV_TIMEOUT))) break;
             tc_fence_after_sync();
             if constexpr (WITH_C && !F32) {
-                if (t == pair_id) {
+                if (t == pair_id && !c_tma) {
 #pragma unroll
                     for (int j = 0; j < Cfg::kChunksPerWarp; ++j) load_c(tile, j, cpk[j]);
                 }
                 if (has_next) prefetch_c(next_tile);
+            }
+            if constexpr (Cfg::kCBoxes > 0) {
+                if (c_tma) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&cfull_bar[ew], c_phase, ctl, DG_DEV_TIMEOUT))) break;
+                    c_phase ^= 1;
+                    c_pending = false;
+                    // bf16(acc + C) over each box's two 16-column chunks, back into the box
+#pragma unroll
+                    for (int q = 0; q < kMyBoxes; ++q) {
+                        const int j = 2 * q + static_cast<int>(half);
+                        if (j >= Cfg::kCBoxes) break;
+                        uint32_t v[2][16];
+                        const uint32_t tcol = tmem_base + ((quad * 32) << 16) + acc * ACC + j * 32;
+                        tmem_ld_32x32b_x16(tcol, v[0]);
+                        tmem_ld_32x32b_x16(tcol + 16, v[1]);
+                        tmem_ld_wait();
+                        reg_fence16(v[0]);
+                        reg_fence16(v[1]);
+                        uint8_t *rowp = ctile + j * Cfg::kCBoxBytes + lane * 64;
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            // 64-byte swizzle: 16-byte unit h (columns 8h..8h+7) of row r at h ^ ((r >> 1) & 3)
+                            uint4 *up = reinterpret_cast<uint4 *>(rowp + ((h ^ ((lane >> 1) & 3)) * 16));
+                            const uint4 cv = *up;
+                            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+                            const uint32_t *x = v[h >> 1] + 8 * (h & 1);
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float lo = __uint_as_float(x[2 * i]) + __uint_as_float(cw[i] << 16);
+                                const float hi = __uint_as_float(x[2 * i + 1]) + __uint_as_float(cw[i] & 0xFFFF0000u);
+                                __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                                ow[i] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                            *up = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(leader_tempty + acc * 8);
+                    if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1; }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // boxes wholly past the last row or column store nothing
+#pragma unroll
+                        for (int q = 0; q < kMyBoxes; ++q) {
+                            const int j = 2 * q + static_cast<int>(half);
+                            if (j < Cfg::kCBoxes && tile.n0 + 32 * j < p.n && tile.d_row0 + row_off < p.rows)
+                                tma_store_2d(&tm_d, ctile + j * Cfg::kCBoxBytes, tile.n0 + 32 * j,
+                                             tile.d_row0 + row_off);
+                        }
+                        bulk_commit_group();
+                        if (has_next) bulk_wait_group_read<0>();   // the boxes may be refilled
+                    }
+                    __syncwarp();
+                    if (has_next) load_ctile(next_tile);
+                    tile = next_tile;
+                    continue;
+                }
             }
             if constexpr (F32) {
                 // FP32 D (and FP32 C): each chunk goes TMEM -> registers (+ C) -> one
@@ -1254,6 +1367,8 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
             }
             tile = next_tile;
         }
+        // (an aborted loop leaves no C load landing in shared memory after the CTA is gone)
+        if (c_pending && lane == 0) mbar_wait_drain(&cfull_bar[ew], c_phase, ctl);
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }
@@ -1271,7 +1386,7 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, int grid,
                                  cudaStream_t stream) {
-    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32, WITH_C>;
     cudaError_t e = cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
@@ -1288,12 +1403,13 @@ cudaError_t launch_bs2_gemm_impl(const TensorMaps &maps, const GemmParams &p, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>, maps.a, maps.b, maps.b2, maps.d, p);
+    return cudaLaunchKernelEx(&cfg, dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>, maps.a, maps.b, maps.b2, maps.d,
+                              maps.c, p);
 }
 
 template <int BN, bool WITH_C, int MP, bool F32, int LAY>
 int max_active_pairs_impl() {
-    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32, WITH_C>;
     if (cudaFuncSetAttribute(dg_bs2_gemm_kernel<BN, WITH_C, MP, F32, LAY>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
         return 0;
@@ -1313,9 +1429,9 @@ int max_active_pairs_impl() {
     return n;
 }
 
-template <int BN, int MP, int LAY = 0, bool F32 = false>
+template <int BN, int MP, int LAY = 0, bool F32 = false, bool WITH_C = false>
 void fill_bs2_info(KernelInfo *info) {
-    using Cfg = Bs2Cfg<BN, MP, LAY, F32>;
+    using Cfg = Bs2Cfg<BN, MP, LAY, F32, WITH_C>;
     info->block_n = BN;
     info->stages = Cfg::kStages;
     info->smem_bytes = Cfg::kSmemBytes;

@@ -30,7 +30,7 @@ DG_BS2_LIST(DG_EXTERN2)
 
 bool get_bs2_kernel_info(int block_n, bool with_c, int mp, KernelInfo *info, bool f32, int lay) {
 #define DG_CASE2(BN, C, MP, F32, LAY) \
-    if (block_n == BN && with_c == C && mp == MP && f32 == F32 && lay == LAY) { fill_bs2_info<BN, MP, LAY, F32>(info); return true; }
+    if (block_n == BN && with_c == C && mp == MP && f32 == F32 && lay == LAY) { fill_bs2_info<BN, MP, LAY, F32, C>(info); return true; }
     DG_BS2_LIST(DG_CASE2)
 #undef DG_CASE2
     return false;

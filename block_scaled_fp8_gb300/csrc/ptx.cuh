@@ -100,6 +100,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     return mbar_wait_slow(a, parity, ctl, timeout_flag);
 }
 
+// Waits for copies already issued to land whatever the abort flag says (a CTA
+// must not leave while a copy into its shared memory is in flight); gives up
+// after the time limit.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, const WaitCtl &ctl) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_timer_ns() - t0 > ctl.timeout_ns) return;
+}
+
 // As mbar_wait, with cluster-scope acquire (arrivals come from the peer CTA).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &ctl,
                                                   int32_t timeout_flag) {
