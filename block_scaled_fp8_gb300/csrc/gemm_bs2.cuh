@@ -119,8 +119,11 @@ struct Bs2Config {
     // grouped-layout unit prefix + info (the 128-row pairs, and the C tile's dense
     // GEMMs, run dense problems only)
     static constexpr int kPrefixBytes = (MP == 256 && !CT) ? (2 * kMaxPairPrefix + 1) * 4 : 0;
-    // Operand stages: 256-row pairs keep up to 12 (slots of 4, 2 or 1 K-blocks, so
-    // the MMA warp waits and commits once per slot).  128-row pairs stream B from
+    // Operand stages: 256-row pairs keep up to 12, in slots of 4 K-blocks when all
+    // 12 fit (the MMA warp waits and commits once per slot), else of one: a slot
+    // frees only when all its K-blocks' MMAs are done, so with six stages in slots
+    // of two a refill had two slots' MMA time to land, against five K-blocks' with
+    // slots of one.  128-row pairs stream B from
     // DRAM at a few bytes per MMA cycle, so what bounds them is the bytes in flight:
     // up to 20 stages in slots of 2 K-blocks (a slot frees as soon as its two
     // K-blocks' MMAs complete).
@@ -154,7 +157,7 @@ struct Bs2Config {
     static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > kMaxStages ? kMaxStages : kStagesBySmem;
-    static constexpr int kGroupKb = MP == 128 ? 2 : (kStagesCap >= 12 ? 4 : (kStagesCap >= 6 ? 2 : 1));
+    static constexpr int kGroupKb = MP == 128 ? 2 : (kStagesCap >= 12 ? 4 : 1);
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;
     static constexpr int kNumAcc = (2 * kAccCols + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
