@@ -568,6 +568,11 @@ def run_ours(args, rank, world, local_rank):
     # GEMM's launch inside the step.  None where torch cannot record timing events in
     # a captured graph.
     step_gemm_ms = measure_step_launches(probs, flush, reps, status, stream)
+    # the same with events only where the kernel changes (after the M=128 GEMMs, which
+    # come first, and after the M=4096 ones): each kernel's launches keep their overlap
+    n_skinny = sum(1 for p in probs if p["shape"][0] <= 128)
+    assert all(p["shape"][0] <= 128 for p in probs[:n_skinny]), "the M=128 GEMMs lead the step"
+    step_group_ms = measure_step_launches(probs, flush, reps, status, stream, cuts=[n_skinny, len(probs)])
 
     # ---------------- end to end through the public API with host buffers
     for p in probs:
@@ -595,9 +600,12 @@ def run_ours(args, rank, world, local_rank):
     big = [i for i, p in enumerate(probs) if p["shape"][0] > 128]
     skinny = [i for i, p in enumerate(probs) if p["shape"][0] <= 128]
     launch_ms = step_gemm_ms if step_gemm_ms is not None else gemm_ms
-    big_ms = sum(launch_ms[i] for i in big)
+    if step_group_ms is not None:
+        skinny_ms, big_ms = step_group_ms
+    else:
+        big_ms = sum(launch_ms[i] for i in big)
+        skinny_ms = sum(launch_ms[i] for i in skinny)
     achieved = sum(flops(*probs[i]["shape"]) for i in big) / (big_ms * 1e-3) / 1e12
-    skinny_ms = sum(launch_ms[i] for i in skinny)
     skinny_gbs = sum(gemm_bytes(*probs[i]["shape"]) for i in skinny) / (skinny_ms * 1e-3) / 1e9
     other = measure_other_workloads(dev, flush, min(20, max(5, args.steps // 4)), stream) if rank == 0 else []
     lib_fp8 = measure_library_fp8_peak(dev, stream) if rank == 0 else None
@@ -610,7 +618,13 @@ def run_ours(args, rank, world, local_rank):
                          "gbs": round(gemm_bytes(m, n, k) / (lm * 1e-3) / 1e9, 1),
                          "isolated_us": round(ms * 1e3, 2),
                          "block_n": cfg["block_n"], "grid": cfg["grid"]})
-    launch_timing = ("each GEMM's launch inside the step (CUDA events between the step's launches, "
+    launch_timing = ("the kernel's three launches inside the step, between CUDA events recorded before "
+                     "and after them in the step's graph (replayed behind the L2 flush; the launches "
+                     "between the events keep their programmatic overlap); per_gemm.us: each launch "
+                     "between events after every launch; per_gemm.isolated_us: one launch alone "
+                     "after the flush"
+                     if step_group_ms is not None else
+                     "each GEMM's launch inside the step (CUDA events between the step's launches, "
                      "replayed behind the L2 flush); per_gemm.isolated_us: one launch alone after the flush"
                      if step_gemm_ms is not None else
                      "one launch alone after the L2 flush (CUDA events around it)")
@@ -644,16 +658,18 @@ def run_ours(args, rank, world, local_rank):
                          "frac": round(achieved / fp8_peak, 4),
                          "peak_note": f"fp8 = {peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio), of {peaks['source']}",
                          "kernel": "dg_bs2_gemm_kernel (CTA pairs): the three M=4096 GEMMs, "
-                                   "flops / summed launch time",
+                                   "flops / the three launches' time in the step",
                          "timing": launch_timing,
+                         "launches_us": round(big_ms * 1e3, 2),
                          "traffic": big_traffic},
             "roofline_skinny": {"bound": "hbm", "achieved": round(skinny_gbs, 1),
                                 "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
                                 "frac": round(skinny_gbs / peaks["hbm_gbs"], 4),
                                 "kernel": "the three M=128 GEMMs (dg_bs2_gemm_kernel on 128-row CTA pairs "
                                           "where the load model prefers them, else dg_bs_gemm_kernel): "
-                                          "algorithmic bytes / summed launch time, of " + peaks["source"],
+                                          "algorithmic bytes / the three launches' time in the step, of " + peaks["source"],
                                 "timing": launch_timing,
+                                "launches_us": round(skinny_ms * 1e3, 2),
                                 "traffic": skinny_traffic},
             "per_gemm": per_gemm,
             "other_workloads": other,
@@ -886,31 +902,39 @@ def run_case(args):
                                    / (us * 1e-6) / 1e9, 1), "config": cfg}))
 
 
-def measure_step_launches(probs, flush, reps, status, stream):
-    """Device time (ms, mean over `reps` replays) of each GEMM launch of the step:
-    the six launches captured in a CUDA graph with a timing event recorded between
-    consecutive launches, each replay behind the L2 flush.  None if torch cannot
-    record timing events inside a captured graph."""
+def measure_step_launches(probs, flush, reps, status, stream, cuts=None):
+    """Device time (ms, mean over `reps` replays) of runs of the step's GEMM
+    launches: the six launches captured in a CUDA graph with a timing event before
+    the first and after each launch count in `cuts` (default: after every launch),
+    each replay behind the L2 flush.  An event between two launches makes the second
+    wait for the first to finish, where the plain step lets it start early
+    (programmatic dependent launch); launches between two events keep that overlap.
+    Returns one time per run; None if torch cannot record timing events inside a
+    captured graph."""
     import torch
 
     from block_scaled_fp8_gb300 import binding
+    cuts = list(range(1, len(probs) + 1)) if cuts is None else list(cuts)
     try:
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(probs) + 1)]
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(cuts) + 1)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             evs[0].record()
+            j = 0
             for i, p in enumerate(probs):
                 binding.dg_fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], status=status)
-                evs[i + 1].record()
+                if j < len(cuts) and i + 1 == cuts[j]:
+                    j += 1
+                    evs[j].record()
         torch.cuda.synchronize()
-        out = [0.0] * len(probs)
+        out = [0.0] * len(cuts)
         for r in range(reps + 1):
             flush.fill_(r)
             g.replay()
             torch.cuda.synchronize()
             if r == 0:
                 continue   # the graph's first replay uploads it
-            for i in range(len(probs)):
+            for i in range(len(cuts)):
                 out[i] += evs[i].elapsed_time(evs[i + 1]) / reps
         del g
         return out
