@@ -674,6 +674,7 @@ def run_ours(args, rank, world, local_rank):
             "per_gemm": per_gemm,
             "other_workloads": other,
             "library_fp8_matmul_8192_tflops": lib_fp8,
+            "pct_of_library_fp8_8192": (round(100.0 * value / lib_fp8, 2) if lib_fp8 else None),
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "pipeline": "per GEMM: copy A and packed scales in, dg_fp8_gemm_nt, copy D out; "
