@@ -737,6 +737,33 @@ def oracle_sample(target_s: float, seed: int = 0):
     return fl / dt / 1e12, threads, desc
 
 
+def oracle_small_config_s(seed: int = 0):
+    """Seconds the oracle takes for the whole of the small workload (M=128, N=256,
+    K=512, full D), on one thread and on all of them."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from block_scaled_fp8_gb300 import inputs
+
+    oracle.build()
+    m, n, k = 128, 256, 512
+    case = inputs.dense_case(m, n, k, seed=seed)
+    a, b = case.a.view(torch.uint8).numpy(), case.b.view(torch.uint8).numpy()
+    sa, sb = case.sfa.double().numpy(), case.sfb.double().numpy()[np.arange(n) // 128]
+    out = {}
+    # (an explicit count each time: a count of 0 keeps the previous call's setting)
+    for label, thr in (("1_thread", 1), ("all_threads", oracle.max_threads())):
+        best = None
+        for _ in range(3):
+            t0 = time.perf_counter()
+            oracle.gemm_nt(a, sa, b, sb, nthreads=thr)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        out[label] = round(best, 5)
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -1105,7 +1132,8 @@ def main():
         if not args.no_cpu_baseline:
             v, thr, desc = oracle_sample(10.0)
             res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-                                   "sample": desc}
+                                   "sample": desc,
+                                   "small_workload_128x256x512_full_s": oracle_small_config_s()}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
