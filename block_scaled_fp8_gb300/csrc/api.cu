@@ -241,7 +241,8 @@ int choose_pair_block_n(const GemmParams &p, bool with_c, int64_t m_pairs, int n
 // Skinny dense problems (one 128-row block, no C): the single-CTA kernel with
 // BLOCK_N bn1, or the 128-row pair kernel, whose CTAs load 64 rows of A each.
 // With one row block every CTA re-reads the same A tile, and a CTA's loads are
-// capped at about 60 bytes per cycle, so the time of a K-block is modelled as
+// capped near 60 bytes per cycle (a load-only probe; ~48 with the MMAs reading
+// shared memory beside them), so the time of a K-block is modelled as
 // max(bytes a CTA loads / 60, MMA cycles) times the waves of tiles.  Returns
 // the pair kernel's BLOCK_N, or 0 to keep the single-CTA kernel.
 int choose_skinny_pair_block_n(const GemmParams &p, int bn1, int num_sms) {

@@ -9,7 +9,7 @@
 // issued by the leader CTA (MP = 256, or 128 for skinny problems):
 //   - each CTA loads its own MP/2 rows of A and half of the tile's B columns
 //     (BN/2 rows of B) per 128-K stage; the pair's loads complete on the
-//     leader's barrier.  An SM's TMA ingest is capped near 60 bytes per cycle,
+//     leader's barrier.  An SM's TMA ingest is capped near 48-60 bytes per cycle,
 //     so halving the B bytes each SM loads is what the pair buys;
 //   - the MMA reads the leader's A rows and B rows 0..BN/2-1 from the leader's
 //     shared memory, the peer's A rows and B rows BN/2..BN-1 from the peer's,
