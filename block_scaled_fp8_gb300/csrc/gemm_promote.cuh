@@ -143,11 +143,12 @@ __global__ void __launch_bounds__(PromoteConfig<BN>::kThreads, 1)
                     goto mma_done;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase, ctl, DG_DEV_TIMEOUT)))
                     goto mma_done;
-                if (lane == 0) {
-                    tc_fence_after_sync();
-                    const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
-                    const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
-                    const uint32_t d_tmem = tmem_base + pj * BN;
+                // all lanes compute the (warp-uniform) descriptors; one elected lane issues
+                tc_fence_after_sync();
+                const uint64_t a_desc = make_desc_kmajor_sw128(smem_u32(smem_a + stage * Cfg::kABytes));
+                const uint64_t b_desc = make_desc_kmajor_sw128(smem_u32(smem_b + stage * Cfg::kBBytes));
+                const uint32_t d_tmem = tmem_base + pj * BN;
+                if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < kBlockK / 32; ++k)
                         tc_mma_f8(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k != 0);
