@@ -982,9 +982,16 @@ __global__ void __launch_bounds__(Bs2Config<BN, MP>::kThreads, 1) __cluster_dims
                                                                                   : (MP == 256 ? BN : BN / 2);
             const float *src = p.c_in_place ? p.d_f32 : p.c_f32;
             const int64_t ld = p.c_in_place ? p.ldd : p.ldc;
-            if (row < p.rows && cols > 0)
-                prefetch_l2_bulk(src + static_cast<int64_t>(row) * ld + tl.n0 + col_off,
-                                 static_cast<uint32_t>(cols) * 4u);
+            if (row < p.rows && cols > 0) {
+                const float *r0 = src + static_cast<int64_t>(row) * ld + tl.n0 + col_off;
+                if (p.c_in_place) {
+                    prefetch_l2_bulk(r0, static_cast<uint32_t>(cols) * 4u);
+                } else {
+                    // a C of its own: one L2 prefetch per 128-byte line from this thread
+                    // (measured faster here than the bulk request, which is faster in place)
+                    for (int c = 0; c < cols; c += 32) prefetch_l2_line(r0 + c);
+                }
+            }
         };
         auto load_c32 = [&](const PairTile &tl, int j, float4 (&dst)[4]) {
             const int row = tl.d_row0 + row_off + static_cast<int>(lane);

@@ -216,6 +216,11 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) 
 }
 
 // 32-byte global load (p 32-byte aligned), cached at L2 only.
+// L2 prefetch of the 128-byte line holding p, from this thread.
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 __device__ __forceinline__ void ld_global_cg_v8(const void *p, uint32_t (&r)[8]) {
     asm volatile("ld.global.cg.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
