@@ -123,10 +123,10 @@ struct Bs2Config {
     // 12 fit (the MMA warp waits and commits once per slot), else of one: a slot
     // frees only when all its K-blocks' MMAs are done, so with six stages in slots
     // of two a refill had two slots' MMA time to land, against five K-blocks' with
-    // slots of one.  128-row pairs stream B from
-    // DRAM at a few bytes per MMA cycle, so what bounds them is the bytes in flight:
-    // up to 20 stages in slots of 2 K-blocks (a slot frees as soon as its two
-    // K-blocks' MMAs complete).
+    // slots of one.  128-row pairs stream B from DRAM at a few bytes per MMA cycle,
+    // so what bounds them is the bytes in flight: up to 20 stages in slots of 2
+    // K-blocks (a slot frees as soon as its two K-blocks' MMAs complete), 4 at 32
+    // columns.
     static constexpr int kMaxStages = MP == 256 ? 12 : 20;
     // Output staging: kStageBufs buffers of one 32-row x 32-byte store box per
     // epilogue warp.  A buffer is rewritten once the TMA store issued from it
@@ -157,7 +157,12 @@ struct Bs2Config {
     static constexpr int kFixedBytes = fixed_bytes(kStageBufs);
     static constexpr int kStagesBySmem = (kSmemLimit - kFixedBytes) / kStageBytes;
     static constexpr int kStagesCap = kStagesBySmem > kMaxStages ? kMaxStages : kStagesBySmem;
-    static constexpr int kGroupKb = MP == 128 ? 2 : (kStagesCap >= 12 ? 4 : 1);
+    // (128-row pairs at 32 columns: four small MMAs per K-block, so the MMA warp's
+    // per-slot waits and commits set the pace and slots of 4 K-blocks go faster)
+    static constexpr int kGroupKb = MP == 128 ? (BN == 32 ? 4 : 2) : (kStagesCap >= 12 ? 4 : 1);
+    // the MMA warp waits for a scale group at slot starts and releases it at the
+    // group's last K-block: a slot must not span two 4-K-block scale groups
+    static_assert(kGroupKb == 1 || kGroupKb == 2 || kGroupKb == 4, "ring slots divide a scale group");
     static constexpr int kStages = kStagesCap / kGroupKb * kGroupKb;
     static constexpr int kRing = kStages / kGroupKb;
     static constexpr int kNumAcc = (2 * kAccCols + kSfTmemSlots * kSfCols <= 512) ? 2 : 1;
