@@ -116,7 +116,7 @@ constexpr int kMaxBlockNWithC = 160;
 // with BLOCK_N (larger tiles re-read less operand data per FLOP).  Split-K is
 // never used: with few M blocks, narrow BLOCK_N is what fills the SMs (the
 // non-power-of-two block idea of "02 · DeepGEMM 技术解析" §4.3).
-int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c) {
+int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c, bool count_waves) {
     static const int forced_bn = [] {
         const char *e = std::getenv("DG_BLOCK_N");
         return e ? std::atoi(e) : 0;
@@ -129,7 +129,9 @@ int choose_block_n(int64_t m_blocks, int n, int num_sms, bool with_c) {
         const int64_t nb = cdiv64(n, bn);
         const int64_t tiles = m_blocks * nb;
         const int64_t waves = cdiv64(tiles, num_sms);
-        const double wave_eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
+        // (masked layouts: the row blocks come from masked_m on the device, so the tile
+        // count and its waves are unknown here; the weight stream sets the time)
+        const double wave_eff = count_waves ? static_cast<double>(tiles) / static_cast<double>(waves * num_sms) : 1.0;
         const double pad_eff = static_cast<double>(n) / static_cast<double>(nb * bn);
         const double tile_eff = static_cast<double>(bn) / (bn + 64.0);
         const double score = wave_eff * pad_eff * tile_eff;
@@ -393,7 +395,7 @@ dg_status launch_block_scaled(GemmParams &p, const BsOperands &o, int64_t m_bloc
                            num_sms, stream);
     }
     const bool with_c = p.c != nullptr;
-    const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c);
+    const int bn = choose_block_n(m_blocks_hint, p.n, num_sms, with_c, p.mode != kModeMasked);
     if (p.mode == kModeDense && !with_c && p.rows <= kBlockM &&
         !(g_debug_flags.load() & DG_DEBUG_SINGLE_CTA)) {
         const int bn2 = choose_skinny_pair_block_n(p, bn, num_sms);
